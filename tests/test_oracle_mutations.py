@@ -1,0 +1,127 @@
+"""Each pin must have teeth: plant a plausible mistake in a copy of the oracle
+(on the CPU) and check that at least one pin fails on it."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import moe_oracle as mo
+import test_oracle_ffn as ffn_pins
+import test_oracle_layout as layout_pins
+import test_oracle_route as route_pins
+
+
+def fails(pins, fn):
+    for pin in pins:
+        try:
+            pin(fn)
+        except (AssertionError, ValueError, IndexError):
+            return True
+    return False
+
+
+def route_ties_to_higher_index(logits, k):
+    L = np.asarray(logits, np.float32)
+    E = L.shape[1]
+    order = np.lexsort((-np.broadcast_to(np.arange(E), L.shape), -L.astype(np.float64)), axis=-1)
+    ids = order[:, :k]
+    sel = np.take_along_axis(L, ids, 1).astype(np.float64)
+    z = np.exp(sel - sel.max(1, keepdims=True))
+    return ids.astype(np.int32), z / z.sum(1, keepdims=True)
+
+
+def route_softmax_over_all(logits, k):
+    ids, _ = oracle.route(logits, k)
+    L = np.asarray(logits, np.float64)
+    p = np.exp(L - L.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    return ids, np.take_along_axis(p, ids.astype(np.int64), 1)
+
+
+def route_sign_error(logits, k):
+    ids, _ = oracle.route(logits, k)
+    sel = np.take_along_axis(np.asarray(logits, np.float64), ids.astype(np.int64), 1)
+    z = np.exp(sel.max(1, keepdims=True) - sel)
+    return ids, z / z.sum(1, keepdims=True)
+
+
+@pytest.mark.parametrize("mutant", [route_ties_to_higher_index, route_softmax_over_all,
+                                    route_sign_error])
+def test_route_mutants_are_caught(mutant):
+    assert fails(route_pins.PINS, mutant)
+
+
+_SWIGLU = mo.swiglu_mlp
+
+
+def _swap_gate_up(X, wg, wu, wd):
+    return _SWIGLU(X, wu, wg, wd)
+
+
+def _silu_sign(X, wg, wu, wd):
+    g, u = X @ wg.T, X @ wu.T
+    h = g / (1.0 + np.exp(g)) * u
+    return h, h @ wd.T
+
+
+def _down_not_transposed(X, wg, wu, wd):
+    g, u = X @ wg.T, X @ wu.T
+    h = mo.silu(g) * u
+    return h, h @ wd          # shape error unless square: wrong either way
+
+
+@pytest.mark.parametrize("mutant", [_swap_gate_up, _silu_sign, _down_not_transposed])
+def test_ffn_mutants_are_caught(mutant, monkeypatch):
+    monkeypatch.setattr(mo, "swiglu_mlp", mutant)
+    # the dense brute force shares swiglu_mlp, so use the pins that do not
+    pins = [ffn_pins.check_single_expert_is_plain_swiglu, ffn_pins.check_two_experts_by_hand]
+    assert fails(pins, mo.layer_forward)
+
+
+def test_combine_dropping_a_term_is_caught(monkeypatch):
+    def combine_missing_last(y, topk_w, pair_row, residual=None):
+        w = np.array(topk_w, copy=True)
+        w[:, -1] = 0.0
+        return original(y, w, pair_row, residual)
+    original = mo.combine
+    monkeypatch.setattr(mo, "combine", combine_missing_last)
+    assert fails([ffn_pins.check_dense_brute_force, ffn_pins.check_two_experts_by_hand],
+                 mo.layer_forward)
+
+
+def test_combine_without_residual_is_caught(monkeypatch):
+    original = mo.combine
+    monkeypatch.setattr(mo, "combine", lambda y, w, pr, residual=None: original(y, w, pr, None))
+    assert fails([ffn_pins.check_zero_down_projection_leaves_residual], mo.layer_forward)
+
+
+def layout_tokens_descending(ids, placement, E, W):
+    lay = oracle.dispatch_layout(ids, placement, E, W)
+    N, k = ids.shape
+    # reverse the order of rows inside every expert segment
+    rt = lay["row_token"].copy()
+    pr = lay["pair_row"].copy()
+    for e in range(E):
+        a, n = lay["expert_offsets"][e], lay["expert_counts"][e]
+        rt[a:a + n] = rt[a:a + n][::-1]
+    for t in range(N):
+        for j in range(k):
+            e = ids[t, j]
+            a, n = lay["expert_offsets"][e], lay["expert_counts"][e]
+            pr[t, j] = a + (n - 1 - (lay["pair_row"][t, j] - a))
+    lay["row_token"], lay["pair_row"] = rt, pr
+    return lay
+
+
+def layout_rank_by_expert_mod(ids, placement, E, W):
+    """Plausible slip: rank(e) = e mod W instead of slot(e) // (E / W)."""
+    fake = np.array([(e % W) * (E // W) + e // W for e in range(E)])
+    inv = np.empty(E, np.int64)
+    inv[fake] = np.arange(E)
+    return oracle.dispatch_layout(ids, inv, E, W)
+
+
+@pytest.mark.parametrize("mutant", [layout_tokens_descending, layout_rank_by_expert_mod])
+def test_layout_mutants_are_caught(mutant):
+    ids = layout_pins.random_ids(40, 8, 3, seed=9)
+    with pytest.raises(AssertionError):
+        layout_pins.check_invariants(mutant, ids, np.arange(8), 8, 4)
