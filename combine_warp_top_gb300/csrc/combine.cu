@@ -1,0 +1,211 @@
+// Combine: the router-weighted sum of each token's k expert outputs, fused
+// with the residual add.
+//
+// "Kernel fusion for expert parallelism", section "Expert parallelism:
+// dispatch and combine" (the combine returns the weighted outputs to the token's
+// owner, which sums them; Sigma_t = sigma^0_t + ... + sigma^{W-1}_t) and stage 7
+// "reduce" of "Fusing the layer into one kernel" (each expert output scaled by
+// its routing weight and accumulated into the rank's partial); "Expert
+// Coupling" Sec. V-A (dedup: one partial per (token, rank), summed by the
+// owner); FarSkip-Collective Sec. 3 (the layer output is added into the
+// residual stream).
+//
+// One warp per output row.  Each lane owns 16-byte chunks (8 bf16) of the row;
+// the k source rows of a chunk are loaded together, then accumulated in fp32
+// in j order.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kBatch = 8;  // source rows loaded together
+
+__device__ __forceinline__ int clamp_row(int r, int bound) {
+    return (unsigned)r < (unsigned)bound ? r : 0;
+}
+
+__device__ __forceinline__ void acc_bf16x8(float (&acc)[8], const uint4& v, float w) {
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(p[i]);
+        acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
+        acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+    }
+}
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& v) {
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(p[i]);
+        acc[2 * i] += f.x;
+        acc[2 * i + 1] += f.y;
+    }
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
+    uint4 o;
+    __nv_bfloat162* q = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    return o;
+}
+
+// acc += sum over the set bits j of `srcs` (ascending) of w_j * rows[row_j][c]
+// where lane j holds row_j / w_j.  Warp-uniform control flow.
+__device__ __forceinline__ void gather_weighted(float (&acc)[8], const uint4* __restrict__ rows,
+                                                int C, int c, bool active, uint32_t srcs,
+                                                int my_row, float my_w) {
+    while (srcs) {
+        uint4 v[kBatch];
+        int js[kBatch];
+        int n = 0;
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            js[b] = -1;
+            if (srcs) {
+                js[b] = __ffs(srcs) - 1;
+                srcs &= srcs - 1;
+                n = b + 1;
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            if (b < n) {
+                const int r = __shfl_sync(0xffffffffu, my_row, js[b]);
+                if (active) v[b] = rows[(size_t)r * C + c];
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            if (b < n) {
+                const float w = __shfl_sync(0xffffffffu, my_w, js[b]);
+                if (active) acc_bf16x8(acc, v[b], w);
+            }
+        }
+    }
+}
+
+// Plain combine: out[t] = bf16(residual[t] + sum_j w[t,j] * y[pair_row[t,j]]).
+__global__ void __launch_bounds__(kThreads) combine_kernel(
+    const uint4* __restrict__ y, const float* __restrict__ topk_w,
+    const int32_t* __restrict__ pair_row, int N, int C, int k, int R,
+    const uint4* residual, uint4* out) {
+    const int lane = threadIdx.x & 31;
+    const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    if (t >= N) return;
+    const int my_row = lane < k ? clamp_row(pair_row[(size_t)t * k + lane], R) : 0;
+    const float my_w = lane < k ? topk_w[(size_t)t * k + lane] : 0.f;
+    const uint32_t all = k >= 32 ? 0xffffffffu : ((1u << k) - 1u);
+    for (int c0 = 0; c0 < C; c0 += 32) {
+        const int c = c0 + lane;
+        const bool active = c < C;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        gather_weighted(acc, y, C, c, active, all, my_row, my_w);
+        if (active) {
+            if (residual) add_bf16x8(acc, residual[(size_t)t * C + c]);
+            out[(size_t)t * C + c] = pack_bf16x8(acc);
+        }
+    }
+}
+
+// Dedup, expert-rank side: partial[d] = bf16(sum over the j of token t carried
+// by dedup row d of w[t,j] * y[pair_row[t,j]]), j ascending.
+__global__ void __launch_bounds__(kThreads) rank_reduce_kernel(
+    const uint4* __restrict__ y, const float* __restrict__ topk_w,
+    const int32_t* __restrict__ pair_row, const int32_t* __restrict__ pair_dedup_row,
+    const int32_t* __restrict__ dedup_row_token, const int32_t* __restrict__ n_dedup_rows, int N,
+    int C, int k, int R, uint4* __restrict__ partial) {
+    const int lane = threadIdx.x & 31;
+    const int d = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    const int Rd = *n_dedup_rows;
+    if (d >= Rd) return;
+    const int t = clamp_row(dedup_row_token[d], N);
+    const int my_row = lane < k ? clamp_row(pair_row[(size_t)t * k + lane], R) : 0;
+    const float my_w = lane < k ? topk_w[(size_t)t * k + lane] : 0.f;
+    const bool mine = lane < k && pair_dedup_row[(size_t)t * k + lane] == d;
+    const uint32_t srcs = __ballot_sync(0xffffffffu, mine);
+    for (int c0 = 0; c0 < C; c0 += 32) {
+        const int c = c0 + lane;
+        const bool active = c < C;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        gather_weighted(acc, y, C, c, active, srcs, my_row, my_w);
+        if (active) partial[(size_t)d * C + c] = pack_bf16x8(acc);
+    }
+}
+
+// Dedup, owner side: out[t] = bf16(residual[t] + sum of the token's partial
+// rows in ascending rank order).
+__global__ void __launch_bounds__(kThreads) owner_sum_kernel(
+    const uint4* __restrict__ partial, const int32_t* __restrict__ pair_dedup_row, int N, int C,
+    int k, int Rd_bound, const uint4* residual, uint4* out) {
+    const int lane = threadIdx.x & 31;
+    const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    if (t >= N) return;
+    const int my_d = lane < k ? clamp_row(pair_dedup_row[(size_t)t * k + lane], Rd_bound) : -1;
+    // distinct rows of the token; their order among themselves is ascending d,
+    // which is ascending rank because dedup rows are stored rank-major
+    bool first = lane < k;
+    int below = 0;
+    for (int jj = 0; jj < k; ++jj) {
+        const int o = __shfl_sync(0xffffffffu, my_d, jj);
+        if (jj < lane && o == my_d) first = false;
+    }
+    const uint32_t firsts = __ballot_sync(0xffffffffu, first);
+    for (int jj = 0; jj < k; ++jj) {
+        const int o = __shfl_sync(0xffffffffu, my_d, jj);
+        if (((firsts >> jj) & 1u) && o < my_d) ++below;
+    }
+    const int nd = __popc(firsts);
+    // lane q receives the q-th smallest distinct row
+    int sorted_d = 0;
+    for (int jj = 0; jj < k; ++jj) {
+        const int b = __shfl_sync(0xffffffffu, below, jj);
+        const int o = __shfl_sync(0xffffffffu, my_d, jj);
+        if (((firsts >> jj) & 1u) && b == lane) sorted_d = o;
+    }
+    const uint32_t srcs = nd >= 32 ? 0xffffffffu : ((1u << nd) - 1u);
+    for (int c0 = 0; c0 < C; c0 += 32) {
+        const int c = c0 + lane;
+        const bool active = c < C;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        gather_weighted(acc, partial, C, c, active, srcs, sorted_d, 1.0f);
+        if (active) {
+            if (residual) add_bf16x8(acc, residual[(size_t)t * C + c]);
+            out[(size_t)t * C + c] = pack_bf16x8(acc);
+        }
+    }
+}
+
+inline int warps_grid(long long n) { return (int)((n + kThreads / 32 - 1) / (kThreads / 32)); }
+
+}  // namespace
+
+cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& L,
+                           const moe_shape& s, uint16_t* partial, const uint16_t* residual,
+                           uint16_t* out, cudaStream_t st) {
+    if (s.N == 0) return cudaSuccess;
+    const int C = s.H / 8;
+    const int R = s.N * s.k;
+    const uint4* res = reinterpret_cast<const uint4*>(residual);
+    if (!s.dedup) {
+        combine_kernel<<<warps_grid(s.N), kThreads, 0, st>>>(
+            reinterpret_cast<const uint4*>(y), w, L.pair_row, s.N, C, s.k, R, res,
+            reinterpret_cast<uint4*>(out));
+        return cudaGetLastError();
+    }
+    const int Rd_max = s.N * (s.k < s.W ? s.k : s.W);
+    rank_reduce_kernel<<<warps_grid(Rd_max), kThreads, 0, st>>>(
+        reinterpret_cast<const uint4*>(y), w, L.pair_row, L.pair_dedup_row, L.dedup_row_token,
+        L.n_dedup_rows, s.N, C, s.k, R, reinterpret_cast<uint4*>(partial));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    owner_sum_kernel<<<warps_grid(s.N), kThreads, 0, st>>>(
+        reinterpret_cast<const uint4*>(partial), L.pair_dedup_row, s.N, C, s.k, Rd_max, res,
+        reinterpret_cast<uint4*>(out));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,594 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// FarSkip-Collective (arXiv 2511.11505) Sec. 2.1: the gated expert MLP; "Kernel
+// fusion for expert parallelism", section "Fusing the layer into one kernel",
+// stages 4-6: the gate/up MatMul, the SwiGLU activation and the down MatMul of
+// every expert over its expert-contiguous rows ("Expert Coupling" Appendix
+// A-A1: dispatch feeds a grouped GEMM).
+//
+// Two launches of one persistent, warp-specialised kernel:
+//   gate/up:  one 128x256 MMA tile holds 128 gate columns and the matching 128
+//             up columns of the same rows, so the epilogue can apply
+//             h = SiLU(g) * u straight out of TMEM and store bf16 h.
+//   down:     a 128x256 tile of y = h Wd^T, stored as bf16.
+// Roles (192 threads): warp 0 issues TMA loads into a 4-stage shared-memory
+// ring (128B swizzle), warp 1 owns TMEM and issues tcgen05.mma from one thread
+// (fp32 accumulators, two 256-column buffers so the epilogue of one tile
+// overlaps the main loop of the next), warps 2-5 read the accumulators back
+// with tcgen05.ld and write the outputs.  Tiles of an expert never cross into
+// the next expert's rows on store: rows past the segment end are masked, so
+// no padding of the expert-major layout is needed.  Every wait is bounded; a
+// wait that runs out of time records MOE_ERR_TIMEOUT, the CTA drains what it
+// has in flight, frees TMEM and returns.
+#include <cudaTypedefs.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = kGemmBM;       // rows per tile (TMEM lanes)
+constexpr int BK = 64;            // bf16 elements per k-block: one 128-byte swizzle row
+constexpr int UMMA_K = 16;        // K of one kind::f16 MMA
+constexpr int kStages = 4;
+constexpr int kMmaN = 256;        // columns per MMA and per accumulator
+constexpr int kAccs = 2;
+constexpr int kTmemCols = kMmaN * kAccs;  // 512: the whole TMEM of the SM
+constexpr int A_BYTES = BM * BK * 2;      // 16 KB
+constexpr int B_BYTES = kMmaN * BK * 2;   // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int kThreads = 192;
+constexpr int kEpilogueWarps = 4;
+constexpr long long kWaitLimit = 2000000000LL;  // ~1 s of SM clock per wait
+
+struct Ctl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull[kAccs];
+    uint64_t tempty[kAccs];
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort;
+    int prefix[kMaxE + 1];
+    int offs[kMaxE];
+    int cnts[kMaxE];
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * STAGE_BYTES + sizeof(Ctl);
+
+// ---- PTX wrappers -------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait.  Gives up when another role has aborted, or after kWaitLimit
+// cycles, in which case it records the timeout and raises the abort flag.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort,
+                                         int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitLimit) {
+            *abort = 1;
+            set_error(err, MOE_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Bounded wait that ignores the abort flag (used only while draining).
+__device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitLimit) return;
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, cta_group::1.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05.mma issued so far by this thread is done.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets row (lane
+// quadrant base + i), columns [col, col + 32).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+//   bits  0-13 start address >> 4      bits 16-29 leading byte offset >> 4 (unused here)
+//   bits 32-45 stride byte offset >> 4 bits 46-48 fixed 0b001
+//   bits 61-63 swizzle mode (2 = 128-byte swizzle)
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits 4-5),
+// bf16 A (bits 7-9) and B (bits 10-12), both K-major, N >> 3 at bits 17-22,
+// M >> 4 at bits 24-28.
+constexpr uint32_t make_idesc(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// tile -> (expert, m-block, n-block).  Tiles are numbered expert by expert;
+// inside an expert the m-blocks vary fastest, so CTAs running side by side
+// share the same weight block through L2.
+__device__ __forceinline__ void decode_tile(const int* prefix, int E, int NB, int tile, int& e,
+                                            int& mb, int& nb) {
+    const int q = tile / NB;
+    int lo = 0, hi = E;  // prefix[lo] <= q < prefix[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= q) lo = mid;
+        else hi = mid;
+    }
+    e = lo;
+    const int MB = prefix[e + 1] - prefix[e];
+    const int local = tile - NB * prefix[e];
+    nb = local / MB;
+    mb = local - nb * MB;
+}
+
+template <bool kSwiGLU>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB0,
+                        const __grid_constant__ CUtensorMap tmB1,
+                        const int32_t* __restrict__ expert_offsets,
+                        const int32_t* __restrict__ expert_counts,
+                        const int32_t* __restrict__ mblk_prefix, int E, int K, int n_out,
+                        __nv_bfloat16* __restrict__ out, int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* tiles = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    const uint32_t tiles_addr = smem_u32(tiles);
+    Ctl* ctl = reinterpret_cast<Ctl*>(tiles + (size_t)kStages * STAGE_BYTES);
+    volatile int* abort_flag = &ctl->abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int BNo = kSwiGLU ? kMmaN / 2 : kMmaN;  // output columns per tile
+    const int NB = (n_out + BNo - 1) / BNo;
+    const int KB = (K + BK - 1) / BK;
+
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) ctl->prefix[i] = mblk_prefix[i];
+    for (int i = threadIdx.x; i < E; i += blockDim.x) {
+        ctl->offs[i] = expert_offsets[i];
+        ctl->cnts[i] = expert_counts[i];
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int a = 0; a < kAccs; ++a) {
+            mbar_init(smem_u32(&ctl->tfull[a]), 1);
+            mbar_init(smem_u32(&ctl->tempty[a]), kEpilogueWarps);
+        }
+        mbar_init(smem_u32(&ctl->done), 1);
+        ctl->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_map(&tmA);
+        prefetch_map(&tmB0);
+        if (kSwiGLU) prefetch_map(&tmB1);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    const int total = ctl->prefix[E] * NB;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0, armed_parity = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+                int e, mb, nb;
+                decode_tile(ctl->prefix, E, NB, tile, e, mb, nb);
+                const int row0 = ctl->offs[e] + mb * BM;
+                const int n0 = nb * BNo;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_bar(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full = smem_u32(&ctl->full[stage]);
+                    const uint32_t a_s = tiles_addr + stage * STAGE_BYTES;
+                    const uint32_t b_s = a_s + A_BYTES;
+                    mbar_expect_tx(full, STAGE_BYTES);
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    tma_load_2d(a_s, &tmA, full, kb * BK, row0);
+                    if (kSwiGLU) {
+                        tma_load_3d(b_s, &tmB0, full, kb * BK, n0, e);
+                        tma_load_3d(b_s + B_BYTES / 2, &tmB1, full, kb * BK, n0, e);
+                    } else {
+                        tma_load_3d(b_s, &tmB0, full, kb * BK, n0, e);
+                    }
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (*abort_flag) {
+                // let every copy still in flight land before the CTA exits
+                for (int s = 0; s < kStages; ++s)
+                    if ((armed >> s) & 1u)
+                        wait_bar_drain(smem_u32(&ctl->full[s]), (armed_parity >> s) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(BM, kMmaN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+                if (!wait_bar(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u, abort_flag, err)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(acc * kMmaN);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_bar(smem_u32(&ctl->full[stage]), phase, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_s = tiles_addr + stage * STAGE_BYTES;
+                    const uint64_t ad = sw128_desc(a_s);
+                    const uint64_t bd = sw128_desc(a_s + A_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        // advance 16 elements = 32 bytes along K inside the swizzle row
+                        umma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
+                                  (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(smem_u32(&ctl->empty[stage]));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(smem_u32(&ctl->tfull[acc]));
+                if (++acc == kAccs) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // every MMA issued by this thread has retired once `done` fires
+            umma_commit(smem_u32(&ctl->done));
+            wait_bar_drain(smem_u32(&ctl->done), 0);
+        }
+    } else {
+        // ---------------- epilogue: TMEM -> registers -> global ----------------
+        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const int r_in_tile = q * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            int e, mb, nb;
+            decode_tile(ctl->prefix, E, NB, tile, e, mb, nb);
+            const int seg_end = ctl->offs[e] + ctl->cnts[e];
+            const int row = ctl->offs[e] + mb * BM + r_in_tile;
+            const bool row_ok = row < seg_end;
+            const int n0 = nb * BNo;
+            int ready = 0;
+            if (lane == 0) ready = wait_bar(smem_u32(&ctl->tfull[acc]), acc_phase, abort_flag, err);
+            ready = __shfl_sync(0xffffffffu, ready, 0);
+            if (!ready) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kMmaN);
+            __nv_bfloat16* orow = out + (size_t)(row_ok ? row : 0) * n_out;
+            if (kSwiGLU) {
+#pragma unroll 1
+                for (int c = 0; c < BNo / 32; ++c) {
+                    uint32_t g[32], u[32];
+                    tmem_ld32(tbase + c * 32, g);
+                    tmem_ld32(tbase + BNo + c * 32, u);
+                    tmem_wait_ld();
+                    if (row_ok) {
+#pragma unroll
+                        for (int grp = 0; grp < 4; ++grp) {
+                            const int col = n0 + c * 32 + grp * 8;
+                            if (col < n_out) {
+                                uint4 o;
+                                uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const int j = grp * 8 + 2 * i;
+                                    const float h0 = silu(__uint_as_float(g[j])) * __uint_as_float(u[j]);
+                                    const float h1 =
+                                        silu(__uint_as_float(g[j + 1])) * __uint_as_float(u[j + 1]);
+                                    op[i] = pack2(h0, h1);
+                                }
+                                *reinterpret_cast<uint4*>(orow + col) = o;
+                            }
+                        }
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BNo / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + c * 32, v);
+                    tmem_wait_ld();
+                    if (row_ok) {
+#pragma unroll
+                        for (int grp = 0; grp < 4; ++grp) {
+                            const int col = n0 + c * 32 + grp * 8;
+                            if (col < n_out) {
+                                uint4 o;
+                                uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const int j = grp * 8 + 2 * i;
+                                    op[i] = pack2(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+                                }
+                                *reinterpret_cast<uint4*>(orow + col) = o;
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+            if (++acc == kAccs) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// m-blocks per expert, exclusive prefix over expert ids: mblk_prefix[E+1].
+__global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* __restrict__ counts, int E,
+                                                        int32_t* __restrict__ mblk_prefix) {
+    __shared__ int warp_sums[32];
+    const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+    const int v = e < E ? (counts[e] + BM - 1) / BM : 0;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int ws = warp_sums[lane];
+        int wi = ws;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, wi, off);
+            if (lane >= off) wi += o;
+        }
+        warp_sums[lane] = wi - ws;
+    }
+    __syncthreads();
+    const int excl = warp_sums[warp] + incl - v;
+    if (e < E) mblk_prefix[e] = excl;
+    if (e == E - 1) mblk_prefix[E] = excl + v;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, cols] matrix; box = 64 columns x box_rows.
+bool map_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 map over [E, rows, cols]; box = 64 columns x box_rows x 1 expert.
+bool map_3d(CUtensorMap* m, const void* ptr, uint64_t E, uint64_t rows, uint64_t cols,
+            uint32_t box_rows) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {cols, rows, E};
+    cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+    cuuint32_t box[3] = {(cuuint32_t)BK, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+moe_status launch_expert_ffn(const uint16_t* xa, const moe_layout& L, const moe_shape& s,
+                             const uint16_t* wg, const uint16_t* wu, const uint16_t* wd,
+                             uint16_t* h, uint16_t* y, void* ws, cudaStream_t st) {
+    const int R = s.N * s.k;
+    if (R == 0) return MOE_OK;
+    const Workspace wl = workspace_layout(s);
+    int* err = ws_ptr<int>(ws, wl.err);
+    int32_t* prefix = ws_ptr<int32_t>(ws, wl.mblk_prefix);
+
+    CUtensorMap a1, bg, bu, a2, bd;
+    if (!map_2d(&a1, xa, R, s.H, BM) || !map_3d(&bg, wg, s.E, s.I, s.H, kMmaN / 2) ||
+        !map_3d(&bu, wu, s.E, s.I, s.H, kMmaN / 2) || !map_2d(&a2, h, R, s.I, BM) ||
+        !map_3d(&bd, wd, s.E, s.H, s.I, kMmaN))
+        return MOE_ERR_UNSUPPORTED;
+
+    schedule_kernel<<<1, 1024, 0, st>>>(L.expert_counts, s.E, prefix);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(grouped_gemm_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess)
+        return MOE_ERR_CUDA;
+
+    // tiles <= NB * (ceil(R / BM) + E): every expert adds at most one ragged m-block
+    const long long mblocks = (R + BM - 1) / BM + s.E;
+    const int sms = sm_count();
+    const long long t1 = mblocks * ((s.I + kMmaN / 2 - 1) / (kMmaN / 2));
+    const long long t2 = mblocks * ((s.H + kMmaN - 1) / kMmaN);
+    const int g1 = (int)(t1 < sms ? t1 : sms);
+    const int g2 = (int)(t2 < sms ? t2 : sms);
+
+    grouped_gemm_kernel<true><<<g1, kThreads, kSmemBytes, st>>>(
+        a1, bg, bu, L.expert_offsets, L.expert_counts, prefix, s.E, s.H, s.I,
+        reinterpret_cast<__nv_bfloat16*>(h), err);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    grouped_gemm_kernel<false><<<g2, kThreads, kSmemBytes, st>>>(
+        a2, bd, bd, L.expert_offsets, L.expert_counts, prefix, s.E, s.I, s.H,
+        reinterpret_cast<__nv_bfloat16*>(y), err);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+}  // namespace moe

@@ -1,0 +1,308 @@
+// Dispatch layout: a stable counting sort of the (token, expert) pairs by the
+// placement slot of the expert, plus the deduplicated (token, rank) rows.
+//
+// "Kernel fusion for expert parallelism", section "Expert parallelism:
+// dispatch and combine" (W ranks of E/W experts; receivers must know their
+// per-sender counts) and "Expert Coupling" (arXiv 2610.09372) Sec. V-A (one row
+// per unique (token, destination rank); a placement is a permutation of global
+// expert IDs) and Appendix A-A2 (the receiver expands rows to expert-major
+// order).
+//
+// Three launches, all deterministic:
+//  1. count:   per block of 256 tokens, one 32-bit mask per (warp, slot) and
+//              per (warp, rank) records which lanes (tokens) hit it; the block
+//              count of a key is the sum of the popcounts.  OR-ing the rank
+//              bits merges a token's experts on one rank for free, which is the
+//              deduplication.
+//  2. scan:    one block turns the per-block counts into exclusive bases
+//              (blocks in token order) and the totals into slot/rank offsets.
+//  3. scatter: each block rebuilds its masks; a pair's row is its warp's base
+//              plus the popcount of the lower lanes' bits, so tokens ascend
+//              inside every segment exactly as in a stable sort.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 32 * kLayoutWarps;
+
+// slot_of[e] = the placement slot holding expert e.  Invalid placements are
+// reported and resolved deterministically (lowest slot wins, unplaced experts
+// fall back to slot 0) so that every block derives the same table.
+__device__ void build_slot_of(int* slot_of, const int32_t* placement, int E, int* err) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) slot_of[e] = 0x7fffffff;
+    __syncthreads();
+    for (int p = threadIdx.x; p < E; p += blockDim.x) {
+        const int e = placement ? placement[p] : p;
+        if (e < 0 || e >= E) {
+            set_error(err, MOE_ERR_INVALID_ARG);
+            continue;
+        }
+        const int old = atomicMin(&slot_of[e], p);
+        if (old != 0x7fffffff) set_error(err, MOE_ERR_INVALID_ARG);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        if (slot_of[e] == 0x7fffffff) {
+            set_error(err, MOE_ERR_INVALID_ARG);
+            slot_of[e] = 0;
+        }
+    }
+    __syncthreads();
+}
+
+struct Smem {
+    int* slot_of;     // [E]
+    uint32_t* mask;   // [kLayoutWarps][E]
+    uint32_t* rmask;  // [kLayoutWarps][W]
+    int* base;        // [kLayoutWarps][E]
+    int* rbase;       // [kLayoutWarps][W]
+};
+
+__device__ Smem carve(uint32_t* sm, int E, int W) {
+    Smem s;
+    s.slot_of = reinterpret_cast<int*>(sm);
+    s.mask = sm + E;
+    s.rmask = s.mask + kLayoutWarps * E;
+    s.base = reinterpret_cast<int*>(s.rmask + kLayoutWarps * W);
+    s.rbase = s.base + kLayoutWarps * E;
+    return s;
+}
+
+// Fill this block's lane masks.  Returns nothing; masks are valid after the
+// trailing __syncthreads.
+__device__ void build_masks(const Smem& s, const int32_t* __restrict__ ids, int N, int E, int k,
+                            int W, int dedup, int* err) {
+    for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x) s.mask[i] = 0;
+    if (dedup)
+        for (int i = threadIdx.x; i < kLayoutWarps * W; i += blockDim.x) s.rmask[i] = 0;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kLayoutTokens + threadIdx.x;
+    const int per_rank = E / W;
+    if (t < N) {
+        const uint32_t bit = 1u << lane;
+        for (int j = 0; j < k; ++j) {
+            int e = ids[(size_t)t * k + j];
+            if (e < 0 || e >= E) {
+                set_error(err, MOE_ERR_INVALID_ARG);
+                e = 0;
+            }
+            const int p = s.slot_of[e];
+            const uint32_t old = atomicOr(&s.mask[warp * E + p], bit);
+            if (old & bit) set_error(err, MOE_ERR_INVALID_ARG);  // expert repeated in a token
+            if (dedup) atomicOr(&s.rmask[warp * W + p / per_rank], bit);
+        }
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads) layout_count_kernel(
+    const int32_t* __restrict__ ids, const int32_t* __restrict__ placement, int N, int E, int k,
+    int W, int dedup, int32_t* __restrict__ blk_counts, int32_t* __restrict__ blk_rcounts,
+    int* err) {
+    extern __shared__ uint32_t sm[];
+    const Smem s = carve(sm, E, W);
+    build_slot_of(s.slot_of, placement, E, err);
+    build_masks(s, ids, N, E, k, W, dedup, err);
+    for (int p = threadIdx.x; p < E; p += blockDim.x) {
+        int c = 0;
+#pragma unroll
+        for (int w = 0; w < kLayoutWarps; ++w) c += __popc(s.mask[w * E + p]);
+        blk_counts[(size_t)blockIdx.x * E + p] = c;
+    }
+    if (dedup) {
+        for (int r = threadIdx.x; r < W; r += blockDim.x) {
+            int c = 0;
+#pragma unroll
+            for (int w = 0; w < kLayoutWarps; ++w) c += __popc(s.rmask[w * W + r]);
+            blk_rcounts[(size_t)blockIdx.x * W + r] = c;
+        }
+    }
+}
+
+// Exclusive scan of one value per thread over a block of up to 1024 threads.
+__device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+        int ws = lane < nw ? warp_sums[lane] : 0;
+        int wi = ws;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, wi, off);
+            if (lane >= off) wi += o;
+        }
+        if (lane < nw) warp_sums[lane] = wi - ws;  // exclusive prefix of the warps
+        if (lane == 31) *total = wi;
+    }
+    __syncthreads();
+    const int r = warp_sums[warp] + incl - v;
+    __syncthreads();
+    return r;
+}
+
+// Exclusive column scan over the layout blocks of column c of a [nb][ncol]
+// table, in place; returns the column total.
+__device__ int column_scan(int32_t* __restrict__ tab, int nb, int ncol, int c) {
+    int run = 0;
+    int b = 0;
+    for (; b + 4 <= nb; b += 4) {
+        const int c0 = tab[(size_t)(b + 0) * ncol + c];
+        const int c1 = tab[(size_t)(b + 1) * ncol + c];
+        const int c2 = tab[(size_t)(b + 2) * ncol + c];
+        const int c3 = tab[(size_t)(b + 3) * ncol + c];
+        tab[(size_t)(b + 0) * ncol + c] = run;
+        tab[(size_t)(b + 1) * ncol + c] = run + c0;
+        tab[(size_t)(b + 2) * ncol + c] = run + c0 + c1;
+        tab[(size_t)(b + 3) * ncol + c] = run + c0 + c1 + c2;
+        run += c0 + c1 + c2 + c3;
+    }
+    for (; b < nb; ++b) {
+        const int c0 = tab[(size_t)b * ncol + c];
+        tab[(size_t)b * ncol + c] = run;
+        run += c0;
+    }
+    return run;
+}
+
+__global__ void __launch_bounds__(1024) layout_scan_kernel(
+    const int32_t* __restrict__ placement, int nb, int E, int W, int dedup,
+    int32_t* __restrict__ blk_counts, int32_t* __restrict__ blk_rcounts,
+    int32_t* __restrict__ slot_start, moe_layout L) {
+    __shared__ int warp_sums[32];
+    __shared__ int total;
+    const int p = threadIdx.x;  // blockDim.x == 1024 >= E >= W
+
+    const int cnt = p < E ? column_scan(blk_counts, nb, E, p) : 0;
+    const int start = block_exclusive_scan(cnt, warp_sums, &total);
+    const int R = total;
+    __syncthreads();
+    if (p < E) {
+        slot_start[p] = start;
+        int e = placement ? placement[p] : p;
+        if (e < 0 || e >= E) e = 0;  // reported by the count kernel
+        L.expert_counts[e] = cnt;
+        L.expert_offsets[e] = start;
+        const int per_rank = E / W;
+        if (p % per_rank == 0) L.rank_offsets[p / per_rank] = start;
+    }
+    if (p == 0) {
+        slot_start[E] = R;
+        L.expert_offsets[E] = R;
+        L.rank_offsets[W] = R;
+    }
+    if (!dedup) return;
+    const int rcnt = p < W ? column_scan(blk_rcounts, nb, W, p) : 0;
+    const int rstart = block_exclusive_scan(rcnt, warp_sums, &total);
+    const int Rd = total;
+    if (p < W) {
+        L.dedup_counts[p] = rcnt;
+        L.dedup_offsets[p] = rstart;
+    }
+    if (p == 0) {
+        L.dedup_offsets[W] = Rd;
+        *L.n_dedup_rows = Rd;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) layout_scatter_kernel(
+    const int32_t* __restrict__ ids, const int32_t* __restrict__ placement, int N, int E, int k,
+    int W, int dedup, const int32_t* __restrict__ blk_counts,
+    const int32_t* __restrict__ blk_rcounts, const int32_t* __restrict__ slot_start, moe_layout L,
+    int* err) {
+    extern __shared__ uint32_t sm[];
+    const Smem s = carve(sm, E, W);
+    build_slot_of(s.slot_of, placement, E, nullptr);  // errors were reported by the count pass
+    build_masks(s, ids, N, E, k, W, dedup, nullptr);
+    for (int p = threadIdx.x; p < E; p += blockDim.x) {
+        int run = slot_start[p] + blk_counts[(size_t)blockIdx.x * E + p];
+#pragma unroll
+        for (int w = 0; w < kLayoutWarps; ++w) {
+            s.base[w * E + p] = run;
+            run += __popc(s.mask[w * E + p]);
+        }
+    }
+    if (dedup) {
+        for (int r = threadIdx.x; r < W; r += blockDim.x) {
+            int run = L.dedup_offsets[r] + blk_rcounts[(size_t)blockIdx.x * W + r];
+#pragma unroll
+            for (int w = 0; w < kLayoutWarps; ++w) {
+                s.rbase[w * W + r] = run;
+                run += __popc(s.rmask[w * W + r]);
+            }
+        }
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kLayoutTokens + threadIdx.x;
+    if (t >= N) return;
+    const uint32_t lower = (1u << lane) - 1u;
+    const int per_rank = E / W;
+    for (int j = 0; j < k; ++j) {
+        int e = ids[(size_t)t * k + j];
+        if (e < 0 || e >= E) e = 0;
+        const int p = s.slot_of[e];
+        const int row = s.base[warp * E + p] + __popc(s.mask[warp * E + p] & lower);
+        L.row_token[row] = t;
+        L.pair_row[(size_t)t * k + j] = row;
+        if (dedup) {
+            const int r = p / per_rank;
+            const int d = s.rbase[warp * W + r] + __popc(s.rmask[warp * W + r] & lower);
+            L.pair_dedup_row[(size_t)t * k + j] = d;
+            L.dedup_row_token[d] = t;
+            L.expand_src[row] = d;
+        }
+    }
+}
+
+inline size_t smem_bytes(int E, int W) {
+    return sizeof(uint32_t) * ((size_t)E + 2 * (size_t)kLayoutWarps * (E + W));
+}
+
+}  // namespace
+
+cudaError_t launch_layout(const int32_t* ids, const int32_t* placement, const moe_shape& s,
+                          const moe_layout& L, void* ws, cudaStream_t st) {
+    const Workspace wl = workspace_layout(s);
+    int* err = ws_ptr<int>(ws, wl.err);
+    int32_t* blk_counts = ws_ptr<int32_t>(ws, wl.blk_counts);
+    int32_t* blk_rcounts = ws_ptr<int32_t>(ws, wl.blk_rcounts);
+    int32_t* slot_start = ws_ptr<int32_t>(ws, wl.slot_start);
+    const int nb = layout_blocks(s.N);
+    const size_t smem = smem_bytes(s.E, s.W);
+    cudaError_t e;
+    if (smem > 48 * 1024) {
+        e = cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(layout_scatter_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    if (nb > 0) {
+        layout_count_kernel<<<nb, kThreads, smem, st>>>(ids, placement, s.N, s.E, s.k, s.W,
+                                                        s.dedup, blk_counts, blk_rcounts, err);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    layout_scan_kernel<<<1, 1024, 0, st>>>(placement, nb, s.E, s.W, s.dedup, blk_counts,
+                                            blk_rcounts, slot_start, L);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (nb > 0) {
+        layout_scatter_kernel<<<nb, kThreads, smem, st>>>(ids, placement, s.N, s.E, s.k, s.W,
+                                                          s.dedup, blk_counts, blk_rcounts,
+                                                          slot_start, L, err);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace moe

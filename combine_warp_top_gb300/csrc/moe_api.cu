@@ -1,0 +1,183 @@
+// C ABI entry points of libmoe: argument checks, workspace sizing, and the
+// chaining of the kernels of the other files on the caller's stream.
+// Declarations and the contract of every call are in include/moe.h.
+#include <stdio.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 1;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
+namespace {
+
+moe_status check_shape(const moe_shape* s) {
+    if (!s) return MOE_ERR_INVALID_ARG;
+    if (s->N < 0 || s->H <= 0 || s->E <= 0 || s->k <= 0 || s->W <= 0 || s->I <= 0)
+        return MOE_ERR_INVALID_ARG;
+    if (s->k > s->E || s->E % s->W != 0) return MOE_ERR_INVALID_ARG;
+    if (s->E > kMaxE || s->k > kMaxK) return MOE_ERR_UNSUPPORTED;
+    if (s->H % 8 != 0 || s->I % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if ((long long)s->N * s->k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status check_layout(const moe_layout* L, const moe_shape* s) {
+    if (!L) return MOE_ERR_INVALID_ARG;
+    if (!L->expert_counts || !L->expert_offsets || !L->rank_offsets || !L->row_token ||
+        !L->pair_row)
+        return MOE_ERR_INVALID_ARG;
+    if (s->dedup && (!L->dedup_counts || !L->dedup_offsets || !L->dedup_row_token ||
+                     !L->pair_dedup_row || !L->expand_src || !L->n_dedup_rows))
+        return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status check_ws(const moe_shape* s, void* ws, size_t ws_bytes) {
+    if (!ws || ws_bytes < workspace_layout(*s).total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+inline cudaStream_t as_stream(void* p) { return reinterpret_cast<cudaStream_t>(p); }
+
+#define MOE_TRY(expr)                     \
+    do {                                  \
+        const moe_status _st = (expr);    \
+        if (_st != MOE_OK) return _st;    \
+    } while (0)
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_shape* shape) {
+    if (check_shape(shape) != MOE_OK) return 0;
+    return workspace_layout(*shape).total;
+}
+
+moe_status moe_route(const float* logits, const moe_shape* shape, int32_t* topk_ids,
+                     float* topk_w, void* stream) {
+    MOE_TRY(check_shape(shape));
+    if (shape->N == 0) return MOE_OK;
+    if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+    return cuda_status(
+        launch_route(logits, shape->N, shape->E, shape->k, topk_ids, topk_w, as_stream(stream)));
+}
+
+moe_status moe_dispatch_layout(const int32_t* topk_ids, const int32_t* placement,
+                               const moe_shape* shape, const moe_layout* layout, void* ws,
+                               size_t ws_bytes, void* stream) {
+    MOE_TRY(check_shape(shape));
+    MOE_TRY(check_layout(layout, shape));
+    MOE_TRY(check_ws(shape, ws, ws_bytes));
+    if (shape->N > 0 && !topk_ids) return MOE_ERR_INVALID_ARG;
+    return cuda_status(
+        launch_layout(topk_ids, placement, *shape, *layout, ws, as_stream(stream)));
+}
+
+moe_status moe_dispatch(const uint16_t* x, const moe_layout* layout, const moe_shape* shape,
+                        uint16_t* xd, void* stream) {
+    MOE_TRY(check_shape(shape));
+    MOE_TRY(check_layout(layout, shape));
+    if (shape->N == 0) return MOE_OK;
+    if (!x || !xd) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_dispatch(x, *layout, *shape, xd, as_stream(stream)));
+}
+
+moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const moe_shape* shape,
+                          const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                          uint16_t* xe, uint16_t* h, uint16_t* y, void* ws, size_t ws_bytes,
+                          void* stream) {
+    MOE_TRY(check_shape(shape));
+    MOE_TRY(check_layout(layout, shape));
+    MOE_TRY(check_ws(shape, ws, ws_bytes));
+    if (shape->N == 0) return MOE_OK;
+    if (!xd || !w_gate || !w_up || !w_down || !h || !y) return MOE_ERR_INVALID_ARG;
+    if (shape->dedup && !xe) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = as_stream(stream);
+    const uint16_t* a = xd;
+    if (shape->dedup) {
+        MOE_TRY(cuda_status(launch_expand(xd, *layout, *shape, xe, st)));
+        a = xe;
+    }
+    return launch_expert_ffn(a, *layout, *shape, w_gate, w_up, w_down, h, y, ws, st);
+}
+
+moe_status moe_combine(const uint16_t* y, const float* topk_w, const moe_layout* layout,
+                       const moe_shape* shape, uint16_t* partial, const uint16_t* residual,
+                       uint16_t* out, void* stream) {
+    MOE_TRY(check_shape(shape));
+    MOE_TRY(check_layout(layout, shape));
+    if (shape->N == 0) return MOE_OK;
+    if (!y || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+    if (shape->dedup && !partial) return MOE_ERR_INVALID_ARG;
+    return cuda_status(
+        launch_combine(y, topk_w, *layout, *shape, partial, residual, out, as_stream(stream)));
+}
+
+moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32_t* placement,
+                             const uint16_t* w_gate, const uint16_t* w_up,
+                             const uint16_t* w_down, const uint16_t* residual,
+                             const moe_shape* shape, int32_t* topk_ids, float* topk_w,
+                             const moe_layout* layout, uint16_t* xd, uint16_t* xe, uint16_t* h,
+                             uint16_t* y, uint16_t* partial, uint16_t* out, void* ws,
+                             size_t ws_bytes, void* stream) {
+    MOE_TRY(check_shape(shape));
+    MOE_TRY(check_layout(layout, shape));
+    MOE_TRY(check_ws(shape, ws, ws_bytes));
+    if (shape->N == 0) return MOE_OK;
+    if (!logits || !x || !w_gate || !w_up || !w_down || !topk_ids || !topk_w || !xd || !h ||
+        !y || !out)
+        return MOE_ERR_INVALID_ARG;
+    if (shape->dedup && (!xe || !partial)) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(moe_route(logits, shape, topk_ids, topk_w, stream));
+    MOE_TRY(moe_dispatch_layout(topk_ids, placement, shape, layout, ws, ws_bytes, stream));
+    MOE_TRY(moe_dispatch(x, layout, shape, xd, stream));
+    MOE_TRY(moe_expert_ffn(xd, layout, shape, w_gate, w_up, w_down, xe, h, y, ws, ws_bytes,
+                           stream));
+    return moe_combine(y, topk_w, layout, shape, partial, residual, out, stream);
+}
+
+moe_status moe_get_error(void* ws, void* stream) {
+    if (!ws) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = as_stream(stream);
+    int code = 0;
+    if (cudaMemcpyAsync(&code, ws, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (code != 0) {
+        if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return (moe_status)code;
+}
+
+const char* moe_status_str(moe_status status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+        case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+        case MOE_ERR_CUDA: return "CUDA runtime error";
+        case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+        case MOE_ERR_DEVICE_ASSERT: return "device-side check failed";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

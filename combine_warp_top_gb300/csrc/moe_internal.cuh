@@ -1,0 +1,82 @@
+// Internal declarations of libmoe: workspace layout, launch helpers shared by
+// the kernel files, and the inline-PTX wrappers (mbarrier, TMA, tcgen05) used
+// by the grouped GEMM.  Not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+constexpr int kLayoutWarps = 8;                  // warps per layout block
+constexpr int kLayoutTokens = 32 * kLayoutWarps;  // tokens per layout block
+constexpr int kGemmBM = 128;                      // rows per GEMM tile
+
+// Workspace layout (byte offsets, each 256-aligned).
+struct Workspace {
+    size_t err;          // int32 error word
+    size_t blk_counts;   // int32 [nblk][E]  per-block counts by placement slot
+    size_t blk_rcounts;  // int32 [nblk][W]  per-block dedup counts by rank
+    size_t slot_start;   // int32 [E+1]      first row of each slot
+    size_t mblk_prefix;  // int32 [E+1]      GEMM m-blocks before expert e
+    size_t total;
+};
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+inline int layout_blocks(int N) { return (N + kLayoutTokens - 1) / kLayoutTokens; }
+
+inline Workspace workspace_layout(const moe_shape& s) {
+    Workspace w;
+    size_t nb = (size_t)layout_blocks(s.N);
+    size_t o = 0;
+    w.err = o;         o += 256;
+    w.blk_counts = o;  o = align256(o + nb * s.E * 4);
+    w.blk_rcounts = o; o = align256(o + nb * s.W * 4);
+    w.slot_start = o;  o = align256(o + (size_t)(s.E + 1) * 4);
+    w.mblk_prefix = o; o = align256(o + (size_t)(s.E + 1) * 4);
+    w.total = o;
+    return w;
+}
+
+template <typename T>
+inline T* ws_ptr(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+// Device-side status recording: the first error sticks.
+__device__ __forceinline__ void set_error(int* err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// ---- kernel launchers (one per .cu file) -------------------------------------------
+
+cudaError_t launch_route(const float* logits, int N, int E, int k, int32_t* ids, float* w,
+                         cudaStream_t st);
+
+cudaError_t launch_layout(const int32_t* ids, const int32_t* placement, const moe_shape& s,
+                          const moe_layout& L, void* ws, cudaStream_t st);
+
+cudaError_t launch_dispatch(const uint16_t* x, const moe_layout& L, const moe_shape& s,
+                            uint16_t* xd, cudaStream_t st);
+
+cudaError_t launch_expand(const uint16_t* xd, const moe_layout& L, const moe_shape& s,
+                          uint16_t* xe, cudaStream_t st);
+
+cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& L,
+                           const moe_shape& s, uint16_t* partial, const uint16_t* residual,
+                           uint16_t* out, cudaStream_t st);
+
+// Returns MOE_OK, or an error status when a host-side step (tensor-map
+// encoding, launch) failed.
+moe_status launch_expert_ffn(const uint16_t* xa, const moe_layout& L, const moe_shape& s,
+                             const uint16_t* wg, const uint16_t* wu, const uint16_t* wd,
+                             uint16_t* h, uint16_t* y, void* ws, cudaStream_t st);
+
+int sm_count();
+
+}  // namespace moe

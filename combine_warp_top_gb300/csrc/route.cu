@@ -1,0 +1,113 @@
+// Router: top-k over fp32 logits, then a softmax over the k selected logits.
+//
+// "Expert Coupling" (arXiv 2610.09372), Appendix A-A1, Table II: the router is
+// an FP32 linear gate whose top-k experts carry the selected probabilities;
+// FarSkip-Collective (arXiv 2511.11505) Sec. 2.1: G(A) is a sparse top-k
+// selection.  The weights are renormalised over the k selected experts.
+//
+// One warp per token.  Lane l holds logits l, l+32, l+64, ... (coalesced
+// 128-byte loads).  k rounds of a warp arg-max pick the experts in descending
+// order; ties go to the lower expert index.  Lane j keeps the j-th pick, so
+// the k results are written with one coalesced store per array.
+#include <math.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+// a beats b: larger value, or equal value and lower index (idx < 0 = empty).
+__device__ __forceinline__ bool beats(float av, int ai, float bv, int bi) {
+    if (ai < 0) return false;
+    if (bi < 0) return true;
+    return av > bv || (av == bv && ai < bi);
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int N, int E,
+                                                    int k, int32_t* __restrict__ ids,
+                                                    float* __restrict__ w) {
+    const int lane = threadIdx.x & 31;
+    const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    if (t >= N) return;
+    const float* row = logits + (size_t)t * E;
+
+    float v[VPL];
+    uint32_t taken = 0;  // bit i: slot i of this lane is used up or past E
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int e = i * 32 + lane;
+        if (e < E) {
+            v[i] = __ldg(row + e);
+        } else {
+            v[i] = 0.f;
+            taken |= 1u << i;
+        }
+    }
+
+    int my_id = -1;
+    float my_val = 0.f;
+    for (int j = 0; j < k; ++j) {
+        float bv = 0.f;
+        int bi = -1;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            // slots are visited in ascending expert index, so a strict '>' keeps
+            // the lower index on ties
+            if (!((taken >> i) & 1u) && (bi < 0 || v[i] > bv)) {
+                bv = v[i];
+                bi = i * 32 + lane;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (beats(ov, oi, bv, bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        // k <= E guarantees bi >= 0 here
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == j) {
+            my_id = bi;
+            my_val = bv;
+        }
+    }
+
+    // softmax over the selected k; the first pick holds the maximum
+    const float m = __shfl_sync(0xffffffffu, my_val, 0);
+    const float z = lane < k ? expf(my_val - m) : 0.f;
+    float s = z;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane < k) {
+        ids[(size_t)t * k + lane] = my_id;
+        w[(size_t)t * k + lane] = z / s;
+    }
+}
+
+template <int VPL>
+cudaError_t go(const float* logits, int N, int E, int k, int32_t* ids, float* w, cudaStream_t st) {
+    const int threads = 256;
+    const int tokens_per_block = threads / 32;
+    const int blocks = (N + tokens_per_block - 1) / tokens_per_block;
+    route_kernel<VPL><<<blocks, threads, 0, st>>>(logits, N, E, k, ids, w);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_route(const float* logits, int N, int E, int k, int32_t* ids, float* w,
+                         cudaStream_t st) {
+    if (N == 0) return cudaSuccess;
+    if (E <= 32) return go<1>(logits, N, E, k, ids, w, st);
+    if (E <= 64) return go<2>(logits, N, E, k, ids, w, st);
+    if (E <= 128) return go<4>(logits, N, E, k, ids, w, st);
+    if (E <= 256) return go<8>(logits, N, E, k, ids, w, st);
+    if (E <= 512) return go<16>(logits, N, E, k, ids, w, st);
+    return go<32>(logits, N, E, k, ids, w, st);
+}
+
+}  // namespace moe

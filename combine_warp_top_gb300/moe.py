@@ -1,0 +1,242 @@
+"""Python binding of libmoe (include/moe.h): argument marshalling only.
+
+Every function below has the name of the C entry point it calls and takes
+torch CUDA tensors in place of device pointers.  All arithmetic runs in the
+library's kernels; if libmoe.so cannot be loaded the binding raises -- there
+is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+SHAPE_FIELDS = ("N", "H", "E", "k", "W", "I", "dedup")
+LAYOUT_FIELDS = ("expert_counts", "expert_offsets", "rank_offsets", "row_token", "pair_row",
+                 "dedup_counts", "dedup_offsets", "dedup_row_token", "pair_dedup_row",
+                 "expand_src", "n_dedup_rows")
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+          4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE_ASSERT"}
+
+
+class MoeShape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in SHAPE_FIELDS]
+
+
+class MoeLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in LAYOUT_FIELDS]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({_lib_status_str(status)})")
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmoe.so (built by __graft_entry__.build()).  Raises if missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"libmoe.so not built at {path}; run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P, S, I32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    shp, lay = ctypes.POINTER(MoeShape), ctypes.POINTER(MoeLayout)
+    sigs = {
+        "moe_workspace_bytes": (S, [shp]),
+        "moe_route": (I32, [P, shp, P, P, P]),
+        "moe_dispatch_layout": (I32, [P, P, shp, lay, P, S, P]),
+        "moe_dispatch": (I32, [P, lay, shp, P, P]),
+        "moe_expert_ffn": (I32, [P, lay, shp, P, P, P, P, P, P, P, S, P]),
+        "moe_combine": (I32, [P, P, lay, shp, P, P, P, P]),
+        "moe_layer_forward": (I32, [P, P, P, P, P, P, P, shp, P, P, lay, P, P, P, P, P, P, P, S,
+                                    P]),
+        "moe_get_error": (I32, [P, P]),
+        "moe_status_str": (ctypes.c_char_p, [I32]),
+    }
+    for name, (res, args) in sigs.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _lib_status_str(status: int) -> str:
+    try:
+        return load().moe_status_str(int(status)).decode()
+    except Exception:
+        return "?"
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise MoeError(status, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch tensor")
+    if not t.is_cuda:
+        raise ValueError("libmoe takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ---- shapes, layouts, buffers ----------------------------------------------------------
+
+@dataclass(frozen=True)
+class Shape:
+    N: int
+    H: int
+    E: int
+    k: int
+    W: int
+    I: int
+    dedup: bool = False
+
+    def c(self) -> MoeShape:
+        return MoeShape(self.N, self.H, self.E, self.k, self.W, self.I, int(bool(self.dedup)))
+
+    @property
+    def R(self) -> int:
+        return self.N * self.k
+
+    @property
+    def R_d_max(self) -> int:
+        return self.N * min(self.k, self.W)
+
+
+class Layout:
+    """Device arrays of one dispatch layout (see moe_layout in include/moe.h)."""
+
+    def __init__(self, shape: Shape, device="cuda"):
+        N, E, k, W = shape.N, shape.E, shape.k, shape.W
+        i32 = dict(dtype=torch.int32, device=device)
+        sizes = dict(expert_counts=E, expert_offsets=E + 1, rank_offsets=W + 1,
+                     row_token=N * k, pair_row=N * k)
+        if shape.dedup:
+            sizes.update(dedup_counts=W, dedup_offsets=W + 1, dedup_row_token=N * min(k, W),
+                         pair_dedup_row=N * k, expand_src=N * k, n_dedup_rows=1)
+        self.tensors = {n: torch.zeros(max(s, 1), **i32) for n, s in sizes.items()}
+        self.c = MoeLayout(*[ctypes.c_void_p(self.tensors[n].data_ptr()) if n in self.tensors
+                             else None for n in LAYOUT_FIELDS])
+
+    def __getitem__(self, name):
+        return self.tensors[name]
+
+
+def moe_workspace_bytes(shape: Shape) -> int:
+    return int(load().moe_workspace_bytes(ctypes.byref(shape.c())))
+
+
+def workspace(shape: Shape, device="cuda") -> torch.Tensor:
+    n = moe_workspace_bytes(shape)
+    if n == 0:
+        raise MoeError(1, "moe_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+# ---- the C entry points ----------------------------------------------------------------
+
+def moe_route(logits, shape: Shape, topk_ids, topk_w, stream=None):
+    _check(load().moe_route(_ptr(logits), ctypes.byref(shape.c()), _ptr(topk_ids), _ptr(topk_w),
+                            _stream(stream)), "moe_route")
+
+
+def moe_dispatch_layout(topk_ids, placement, shape: Shape, layout: Layout, ws, stream=None):
+    _check(load().moe_dispatch_layout(_ptr(topk_ids), _ptr(placement), ctypes.byref(shape.c()),
+                                      ctypes.byref(layout.c), _ptr(ws), ws.numel(),
+                                      _stream(stream)), "moe_dispatch_layout")
+
+
+def moe_dispatch(x, layout: Layout, shape: Shape, xd, stream=None):
+    _check(load().moe_dispatch(_ptr(x), ctypes.byref(layout.c), ctypes.byref(shape.c()), _ptr(xd),
+                               _stream(stream)), "moe_dispatch")
+
+
+def moe_expert_ffn(xd, layout: Layout, shape: Shape, w_gate, w_up, w_down, xe, h, y, ws,
+                   stream=None):
+    _check(load().moe_expert_ffn(_ptr(xd), ctypes.byref(layout.c), ctypes.byref(shape.c()),
+                                 _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(xe), _ptr(h), _ptr(y),
+                                 _ptr(ws), ws.numel(), _stream(stream)), "moe_expert_ffn")
+
+
+def moe_combine(y, topk_w, layout: Layout, shape: Shape, partial, residual, out, stream=None):
+    _check(load().moe_combine(_ptr(y), _ptr(topk_w), ctypes.byref(layout.c),
+                              ctypes.byref(shape.c()), _ptr(partial), _ptr(residual), _ptr(out),
+                              _stream(stream)), "moe_combine")
+
+
+def moe_layer_forward(logits, x, placement, w_gate, w_up, w_down, residual, shape: Shape,
+                      topk_ids, topk_w, layout: Layout, xd, xe, h, y, partial, out, ws,
+                      stream=None):
+    _check(load().moe_layer_forward(
+        _ptr(logits), _ptr(x), _ptr(placement), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+        _ptr(residual), ctypes.byref(shape.c()), _ptr(topk_ids), _ptr(topk_w),
+        ctypes.byref(layout.c), _ptr(xd), _ptr(xe), _ptr(h), _ptr(y), _ptr(partial), _ptr(out),
+        _ptr(ws), ws.numel(), _stream(stream)), "moe_layer_forward")
+
+
+def moe_get_error(ws, stream=None) -> int:
+    return int(load().moe_get_error(_ptr(ws), _stream(stream)))
+
+
+def moe_status_str(status: int) -> str:
+    return _lib_status_str(status)
+
+
+# ---- a layer with its buffers ----------------------------------------------------------
+
+class MoELayer:
+    """Owns the device buffers of one layer shape (all allocated by torch) and
+    runs moe_layer_forward on them.  Weights are bf16 tensors [E, I, H] (gate,
+    up) and [E, H, I] (down); placement int32 [E] or None."""
+
+    def __init__(self, shape: Shape, w_gate, w_up, w_down, placement=None, device="cuda"):
+        self.shape = shape
+        self.w_gate, self.w_up, self.w_down = w_gate, w_up, w_down
+        self.placement = placement
+        N, H, I, k = shape.N, shape.H, shape.I, shape.k
+        bf = dict(dtype=torch.bfloat16, device=device)
+        self.topk_ids = torch.empty(max(N * k, 1), dtype=torch.int32, device=device)
+        self.topk_w = torch.empty(max(N * k, 1), dtype=torch.float32, device=device)
+        self.layout = Layout(shape, device)
+        rows_d = shape.R_d_max if shape.dedup else shape.R
+        self.xd = torch.empty(max(rows_d, 1), H, **bf)
+        self.xe = torch.empty(max(shape.R, 1), H, **bf) if shape.dedup else None
+        self.h = torch.empty(max(shape.R, 1), I, **bf)
+        self.y = torch.empty(max(shape.R, 1), H, **bf)
+        self.partial = torch.empty(max(shape.R_d_max, 1), H, **bf) if shape.dedup else None
+        self.out = torch.empty(max(N, 1), H, **bf)
+        self.ws = workspace(shape, device)
+
+    def forward(self, logits, x, residual=None, out=None, stream=None):
+        out = self.out if out is None else out
+        moe_layer_forward(logits, x, self.placement, self.w_gate, self.w_up, self.w_down,
+                          residual, self.shape, self.topk_ids, self.topk_w, self.layout,
+                          self.xd, self.xe, self.h, self.y, self.partial, out, self.ws, stream)
+        return out
+
+    def check_device_errors(self, stream=None):
+        st = moe_get_error(self.ws, stream)
+        if st != 0:
+            raise MoeError(st, "device")

@@ -46,6 +46,49 @@ def build_lib(force: bool = False) -> str:
     return _LIB
 
 
+_GPU_SRC = os.path.join(_HERE, "synth_gpu.cu")
+_GPU_LIB = os.path.join(_HERE, "libsynth_gpu.so")
+_gpu_lib = None
+
+
+def build_gpu_lib(force: bool = False) -> str:
+    """Compile the device-side twin of the normal_bf16 stream (sm_103a)."""
+    if force or not os.path.exists(_GPU_LIB) or os.path.getmtime(_GPU_LIB) < os.path.getmtime(_GPU_SRC):
+        tmp = _GPU_LIB + f".tmp{os.getpid()}"
+        nvcc = "nvcc" if subprocess.run(["which", "nvcc"], capture_output=True).returncode == 0 \
+            else "/usr/local/cuda/bin/nvcc"
+        subprocess.check_call([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3",
+                               "-shared", "-Xcompiler", "-fPIC", "-o", tmp, _GPU_SRC,
+                               "-cudart", "static"])
+        os.replace(tmp, _GPU_LIB)
+    return _GPU_LIB
+
+
+def _get_gpu():
+    global _gpu_lib
+    with _lock:
+        if _gpu_lib is None:
+            lib = ctypes.CDLL(build_gpu_lib())
+            lib.synth_normal_bf16_device.argtypes = [ctypes.c_uint64, ctypes.c_uint64,
+                                                     ctypes.c_uint64, ctypes.c_int64,
+                                                     ctypes.c_double, ctypes.c_double,
+                                                     ctypes.c_void_p, ctypes.c_void_p]
+            lib.synth_normal_bf16_device.restype = ctypes.c_int
+            _gpu_lib = lib
+    return _gpu_lib
+
+
+def normal_bf16_device(out, seed, stream, mean=0.0, std=1.0, offset=0):
+    """Fill a torch bf16 CUDA tensor with the normal_bf16 stream (device twin)."""
+    import torch
+    assert out.is_cuda and out.dtype == torch.bfloat16 and out.is_contiguous()
+    rc = _get_gpu().synth_normal_bf16_device(seed, stream, offset, out.numel(), mean, std,
+                                             out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    if rc != 0:
+        raise RuntimeError(f"device generator launch failed ({rc})")
+    return out
+
+
 def _get():
     global _lib
     with _lock:
@@ -246,6 +289,15 @@ def make_weight(wl: Workload, which: str, seed=0, experts=None):
     for i, e in enumerate(experts):
         normal_bf16(seed, stream, (rows, cols), std=0.02, offset=int(e) * per, out=out[i])
     return out
+
+
+def make_weight_device(wl: Workload, which: str, seed=0):
+    """Same tensor as make_weight, generated directly in device memory."""
+    import torch
+    stream = {"gate": STREAM_WG, "up": STREAM_WU, "down": STREAM_WD}[which]
+    rows, cols = (wl.I, wl.H) if which in ("gate", "up") else (wl.H, wl.I)
+    out = torch.empty(wl.E, rows, cols, dtype=torch.bfloat16, device="cuda")
+    return normal_bf16_device(out, seed, stream, std=0.02)
 
 
 def bf16_to_f64(a):

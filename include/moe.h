@@ -1,0 +1,177 @@
+/*
+ * moe.h -- C ABI of libmoe: the single-GPU forward pass of an expert-parallel
+ * Mixture-of-Experts layer on GB300 (sm_103a).
+ *
+ * The problem statement follows "Kernel fusion for expert parallelism"
+ * (brunomaga.github.io), section "Expert parallelism: dispatch and combine":
+ * N tokens of width H, E experts of which every token selects its top k, and
+ * W ranks holding E/W experts each.  Here the W ranks are partitions of one
+ * GPU's memory: rank r owns the rows of the experts in placement slots
+ * [r*E/W, (r+1)*E/W).  The placement permutation follows "Expert Coupling"
+ * (arXiv 2610.09372), Sec. V-A: slot p holds global expert placement[p].
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates and frees nothing and keeps no global state besides cached
+ *    device attributes.  bf16 tensors are passed as uint16_t (bit patterns).
+ *    Every tensor is dense, row-major, and 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *    asynchronous on it, except moe_get_error.
+ *  - Argument checks run on the host before any launch and return
+ *    MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_WORKSPACE with nothing
+ *    launched.  A failed launch returns MOE_ERR_CUDA.  Problems that only the
+ *    device can see (an expert id out of range, a placement that is not a
+ *    permutation, a wait that ran out of time) write a status code into the
+ *    workspace's error word; kernels then keep every access in bounds and never
+ *    trap.  moe_get_error reads and clears that word.
+ *  - Sizes: 1 <= k <= min(E, 32), 1 <= E <= 1024, 1 <= W, E % W == 0,
+ *    H % 8 == 0, I % 8 == 0, N >= 0 and N * k < 2^31.  N == 0 is a no-op.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* bad pointer, size or shape (host), bad ids/placement (device) */
+    MOE_ERR_UNSUPPORTED = 2,   /* shape outside the supported limits listed above */
+    MOE_ERR_WORKSPACE = 3,     /* workspace missing or smaller than moe_workspace_bytes() */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    MOE_ERR_TIMEOUT = 5,       /* a device-side wait gave up (the kernel returned early) */
+    MOE_ERR_DEVICE_ASSERT = 6  /* a device-side consistency check failed */
+} moe_status;
+
+/* N tokens of width H; E experts, top-k; W ranks; SwiGLU intermediate width I;
+ * dedup != 0 selects the deduplicating dispatcher ("Expert Coupling" Sec. V-A):
+ * one row per distinct (token, rank) instead of one per (token, expert). */
+typedef struct {
+    int32_t N, H, E, k, W, I;
+    int32_t dedup;
+} moe_shape;
+
+/* Dispatch layout: caller-owned device arrays of int32, written by
+ * moe_dispatch_layout.  R = N*k plain rows; R_d dedup rows.
+ *  expert_counts[E]       rows of expert e
+ *  expert_offsets[E+1]    first row of expert e's segment; [E] = R.  Segments
+ *                         are stored in placement-slot order.
+ *  rank_offsets[W+1]      first plain row of rank r; [W] = R
+ *  row_token[N*k]         token of every plain row (ascending inside a segment)
+ *  pair_row[N*k]          plain row of pair (t, j), at t*k + j
+ *  dedup_counts[W]        dedup rows received by rank r
+ *  dedup_offsets[W+1]     first dedup row of rank r; [W] = R_d
+ *  dedup_row_token[N*min(k,W)]  token of every dedup row (rank-major,
+ *                         ascending tokens inside a rank)
+ *  pair_dedup_row[N*k]    dedup row that carries pair (t, j)
+ *  expand_src[N*k]        dedup row that plain row i is expanded from
+ *  n_dedup_rows[1]        R_d
+ * The dedup arrays are written only when shape->dedup != 0 and may then be
+ * NULL otherwise. */
+typedef struct {
+    int32_t* expert_counts;
+    int32_t* expert_offsets;
+    int32_t* rank_offsets;
+    int32_t* row_token;
+    int32_t* pair_row;
+    int32_t* dedup_counts;
+    int32_t* dedup_offsets;
+    int32_t* dedup_row_token;
+    int32_t* pair_dedup_row;
+    int32_t* expand_src;
+    int32_t* n_dedup_rows;
+} moe_layout;
+
+/* Bytes of device workspace that the calls taking `ws` need for this shape
+ * (error word, per-block counts, tile schedule).  0 if the shape is invalid.
+ * The caller zero-fills the workspace once after allocating it (the first
+ * int32 is the error word); the calls keep it valid afterwards.  One workspace
+ * must not be shared by calls running concurrently. */
+size_t moe_workspace_bytes(const moe_shape* shape);
+
+/* Top-k routing ("Expert Coupling" Appendix A-A1, Table II: fp32 gate, top-k
+ * of E; FarSkip-Collective Sec. 2.1: G is a sparse top-k selection).
+ * logits   fp32 [N, E]
+ * topk_ids int32 [N, k]: the k largest logits of token t, descending, ties to
+ *          the lower expert index
+ * topk_w   fp32 [N, k]: softmax over the k selected logits (sums to one).
+ * Non-finite logits are outside the contract. */
+moe_status moe_route(const float* logits, const moe_shape* shape, int32_t* topk_ids,
+                     float* topk_w, void* stream);
+
+/* Dispatch layout (kernel-fusion page, "Expert parallelism: dispatch and
+ * combine" and "Fusing the layer into one kernel" stage 3 "group"; "Expert
+ * Coupling" Sec. V-A and Appendix A-A2).  Stable counting sort of the (t, j)
+ * pairs by placement slot of topk_ids[t, j]; with dedup, also the distinct
+ * (token, rank) rows and the expansion map.  Bit-exact and deterministic.
+ * placement int32 [E] or NULL (identity = contiguous placement). */
+moe_status moe_dispatch_layout(const int32_t* topk_ids, const int32_t* placement,
+                               const moe_shape* shape, const moe_layout* layout, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/* Dispatch (the all-to-all of the pages, here a copy between HBM partitions).
+ * Plain:  xd[i, :] = x[row_token[i], :], xd bf16 [N*k, H].
+ * Dedup:  xd[d, :] = x[dedup_row_token[d], :], xd bf16 [N*min(k,W), H]; only
+ *         the first R_d rows are written.
+ * x bf16 [N, H].  Every row is a bit-exact copy. */
+moe_status moe_dispatch(const uint16_t* x, const moe_layout* layout, const moe_shape* shape,
+                        uint16_t* xd, void* stream);
+
+/* Grouped SwiGLU expert FFN (FarSkip-Collective Sec. 2.1; kernel-fusion page
+ * stages 4-6).  For every plain row i of expert e:
+ *   h[i, :] = bf16( SiLU(x_i Wg[e]^T) * (x_i Wu[e]^T) )      bf16 [N*k, I]
+ *   y[i, :] = bf16( h[i, :] Wd[e]^T )                          bf16 [N*k, H]
+ * with fp32 accumulation on the tensor cores.  Weights in nn.Linear layout:
+ * w_gate, w_up bf16 [E, I, H]; w_down bf16 [E, H, I].
+ * Plain: xd holds the expert-major rows [N*k, H] and xe is ignored (may be NULL).
+ * Dedup: xd holds the dedup rows; they are first expanded into expert-major
+ *        order in xe bf16 [N*k, H] (the receiver's "group" step).
+ * ws: workspace of moe_workspace_bytes(shape) bytes. */
+moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const moe_shape* shape,
+                          const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                          uint16_t* xe, uint16_t* h, uint16_t* y, void* ws, size_t ws_bytes,
+                          void* stream);
+
+/* Combine (kernel-fusion page, "Expert parallelism: dispatch and combine" and
+ * stage 7 "reduce"; residual add of FarSkip-Collective Sec. 3).
+ * Plain: out[t, :] = bf16( residual[t, :] + sum_j topk_w[t, j] * y[pair_row[t, j], :] ),
+ *        fp32 sum in j order.
+ * Dedup: the rank holding the experts first forms one partial row per
+ *        (token, rank), partial[d, :] = bf16( sum over the token's j carried by
+ *        row d of topk_w[t, j] * y[pair_row[t, j], :] ) (j order), bf16
+ *        [N*min(k,W), H]; the owner then sums the token's partials in ascending
+ *        rank order and adds the residual.
+ * residual may be NULL (out is then the MoE output alone) and out may equal
+ * residual (in-place add into the residual stream).  partial is ignored when
+ * dedup == 0. */
+moe_status moe_combine(const uint16_t* y, const float* topk_w, const moe_layout* layout,
+                       const moe_shape* shape, uint16_t* partial, const uint16_t* residual,
+                       uint16_t* out, void* stream);
+
+/* The whole layer in order on one stream: moe_route, moe_dispatch_layout,
+ * moe_dispatch, moe_expert_ffn, moe_combine, with the buffers documented for
+ * each of them. */
+moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32_t* placement,
+                             const uint16_t* w_gate, const uint16_t* w_up,
+                             const uint16_t* w_down, const uint16_t* residual,
+                             const moe_shape* shape, int32_t* topk_ids, float* topk_w,
+                             const moe_layout* layout, uint16_t* xd, uint16_t* xe, uint16_t* h,
+                             uint16_t* y, uint16_t* partial, uint16_t* out, void* ws,
+                             size_t ws_bytes, void* stream);
+
+/* Synchronizes `stream`, reads the workspace error word, clears it, and
+ * returns it (MOE_OK if no device-side problem was recorded). */
+moe_status moe_get_error(void* ws, void* stream);
+
+/* Static description of a status code. */
+const char* moe_status_str(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

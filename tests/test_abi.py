@@ -1,0 +1,62 @@
+"""The C ABI library loads on a host without a GPU and exports every entry point
+that include/moe.h declares; its host-side argument checks answer without
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from combine_warp_top_gb300 import build as libbuild
+from combine_warp_top_gb300 import moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return moe.load()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(moe_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("moe_route", "moe_dispatch_layout", "moe_dispatch", "moe_expert_ffn",
+                     "moe_combine", "moe_layer_forward", "moe_workspace_bytes", "moe_get_error",
+                     "moe_status_str"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_host_side_checks_without_gpu(lib):
+    shape = moe.Shape(4096, 7168, 256, 8, 8, 2048)
+    assert moe.moe_workspace_bytes(shape) > 0
+    assert moe.moe_workspace_bytes(moe.Shape(4096, 7168, 256, 8, 7, 2048)) == 0  # E % W
+    assert moe.moe_workspace_bytes(moe.Shape(16, 8, 4, 5, 1, 8)) == 0           # k > E
+    assert moe.moe_workspace_bytes(moe.Shape(16, 12, 4, 2, 1, 8)) == 0          # H % 8
+    # a NULL logits pointer is refused before any CUDA call
+    assert lib.moe_route(None, ctypes.byref(shape.c()), None, None, None) == 1
+    assert lib.moe_dispatch(None, None, ctypes.byref(shape.c()), None, None) == 1
+    assert lib.moe_get_error(None, None) == 3
+    assert lib.moe_status_str(0) == b"ok"
+    assert lib.moe_status_str(5) == b"device-side wait timed out"
+
+
+def test_workspace_grows_with_tokens(lib):
+    small = moe.moe_workspace_bytes(moe.Shape(256, 64, 8, 2, 2, 64))
+    large = moe.moe_workspace_bytes(moe.Shape(256 * 64, 64, 8, 2, 2, 64))
+    assert large > small

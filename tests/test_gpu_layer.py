@@ -1,0 +1,131 @@
+"""End-to-end parity of moe_layer_forward (one call through the C ABI) against
+the oracle, with and without dedup and residual, and the C ABI's error paths."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from cases import SMALL
+from combine_warp_top_gb300 import moe, synth
+from gpu_util import assert_close, dev_bf16, dev_i32, host_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def build_layer(wl, dedup, placement=None, N=None):
+    N = wl.N if N is None else N
+    wg, wu, wd = (synth.make_weight(wl, w) for w in ("gate", "up", "down"))
+    shape = moe.Shape(N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=dedup)
+    layer = moe.MoELayer(shape, dev_bf16(wg), dev_bf16(wu), dev_bf16(wd),
+                         None if placement is None else dev_i32(placement))
+    return layer, (wg, wu, wd)
+
+
+def check_layer(wl, dedup, placement=None, N=None):
+    N = wl.N if N is None else N
+    layer, (wg, wu, wd) = build_layer(wl, dedup, placement, N)
+    L = synth.make_logits(wl, N=N)
+    x, res = synth.make_x(wl, N=N), synth.make_residual(wl, N=N)
+    out = layer.forward(torch.from_numpy(L).cuda(), dev_bf16(x), dev_bf16(res))
+    torch.cuda.synchronize()
+    layer.check_device_errors()
+    got = host_f64(out)
+    ids = layer.topk_ids.view(N, wl.k).cpu().numpy()
+    ref = oracle.layer_forward(L, x, wg, wu, wd, wl.k, wl.W, placement=placement, residual=res,
+                               dedup=dedup)
+    assert np.array_equal(ids, ref["topk_ids"])
+    assert np.array_equal(layer.layout["expert_counts"].cpu().numpy(),
+                          ref["layout"]["expert_counts"])
+    if dedup:
+        assert int(layer.layout["n_dedup_rows"].item()) == ref["layout"]["n_dedup_rows"]
+    assert_close(got, ref["out"], "out")
+    # the MoE delta alone: residual NULL
+    out2 = layer.forward(torch.from_numpy(L).cuda(), dev_bf16(x), None)
+    torch.cuda.synchronize()
+    delta = ref["out"] - oracle.widen_bf16(res)
+    assert_close(host_f64(out2), delta, "MoE delta")
+
+
+@pytest.mark.parametrize("dedup", [False, True])
+@pytest.mark.parametrize("name", list(SMALL))
+def test_layer_small(name, dedup):
+    check_layer(SMALL[name], dedup)
+
+
+@pytest.mark.parametrize("name", ["correlated_contiguous", "correlated_placed"])
+def test_layer_correlated_reduced(name):
+    wl = synth.WORKLOADS[name]
+    check_layer(wl, True, synth.make_placement(wl), N=512)
+
+
+def test_layer_skewed_reduced():
+    wl = synth.WORKLOADS["skewed"]
+    small = synth.Workload("skewed_small", 1024, 256, wl.E, wl.k, 256, wl.W, logits="zipf",
+                           zipf_alpha=1.2)
+    check_layer(small, False)
+
+
+def test_layer_empty_batch_is_noop():
+    wl = SMALL["tiny"]
+    layer, _ = build_layer(wl, False, N=0)
+    empty = torch.empty(0, wl.E, dtype=torch.float32, device="cuda")
+    layer.forward(empty, torch.empty(0, wl.H, dtype=torch.bfloat16, device="cuda"), None)
+    torch.cuda.synchronize()
+    layer.check_device_errors()
+
+
+def test_repeated_calls_are_bitwise_stable():
+    wl = SMALL["ragged"]
+    layer, _ = build_layer(wl, True)
+    L = torch.from_numpy(synth.make_logits(wl)).cuda()
+    x, res = dev_bf16(synth.make_x(wl)), dev_bf16(synth.make_residual(wl))
+    first = layer.forward(L, x, res).clone()
+    for _ in range(3):
+        again = layer.forward(L, x, res)
+        torch.cuda.synchronize()
+        assert torch.equal(first.view(torch.int16), again.view(torch.int16))
+
+
+# ---- error paths: checked on the host, nothing launched ---------------------------------
+
+def test_invalid_arguments_are_rejected():
+    lib = moe.load()
+    wl = SMALL["tiny"]
+    good = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I)
+    assert moe.moe_workspace_bytes(good) > 0
+    for bad in (moe.Shape(64, 128, 8, 9, 2, 256), moe.Shape(64, 128, 8, 2, 3, 256),
+                moe.Shape(-1, 128, 8, 2, 2, 256), moe.Shape(64, 128, 8, 0, 2, 256)):
+        assert moe.moe_workspace_bytes(bad) == 0
+    assert lib.moe_workspace_bytes(moe.MoeShape(64, 130, 8, 2, 2, 256)) == 0  # H % 8
+    assert lib.moe_workspace_bytes(moe.MoeShape(64, 128, 2048, 2, 2, 256)) == 0  # E too large
+    ids = torch.zeros(wl.N * wl.k, dtype=torch.int32, device="cuda")
+    w = torch.zeros(wl.N * wl.k, dtype=torch.float32, device="cuda")
+    st = lib.moe_route(None, ctypes.byref(good.c()), ids.data_ptr(), w.data_ptr(), None)
+    assert st == 1
+    lay = moe.Layout(good)
+    small_ws = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_dispatch_layout(ids, None, good, lay, small_ws)
+    assert e.value.status == 3
+    with pytest.raises(moe.MoeError):
+        moe.moe_dispatch_layout(ids, None, moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, True),
+                                lay, moe.workspace(good))  # dedup arrays missing
+
+
+def test_bad_placement_is_reported_by_the_device():
+    """A placement that is not a permutation is flagged in the workspace error
+    word; the kernels stay in bounds."""
+    wl = SMALL["tiny"]
+    shape = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=True)
+    ids, _ = oracle.route(synth.make_logits(wl), wl.k)
+    lay = moe.Layout(shape)
+    ws = moe.workspace(shape)
+    bad = np.arange(wl.E, dtype=np.int32)
+    bad[3] = 2
+    moe.moe_dispatch_layout(dev_i32(ids), dev_i32(bad), shape, lay, ws)
+    assert moe.moe_get_error(ws) == 1
+    assert moe.moe_get_error(ws) == 0  # cleared by the read
+    moe.moe_dispatch_layout(dev_i32(ids), None, shape, lay, ws)
+    assert moe.moe_get_error(ws) == 0
