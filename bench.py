@@ -1,0 +1,476 @@
+#!/usr/bin/env python
+"""Throughput of the MoE layer forward pass on GB300.
+
+One step = one pass of the whole path (route, dispatch layout, dispatch,
+[dedup expansion], gate/up GEMM + SwiGLU, down GEMM, combine + residual) over
+one batch of synthetic tokens, with inputs and expert weights resident in HBM.
+The default workload is the DeepSeek-V3-shaped layer (N=4096 tokens, H=7168,
+E=256 experts, top-8, SwiGLU width 2048, W=8 ranks); its 22.5 GB of expert
+weights are read every step, far more than the 129 MB L2, so no L2 flush is
+needed between steps.
+
+Prints one JSON line.  --impl reference times the CPU oracle instead (the
+plain float64 restatement of the layer) on a bounded sample of the same
+workload.  Under torchrun (N > 1) every rank runs its own replica of the layer
+on its own tokens (weak scaling, no collective on the data path); the reported
+time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as dt
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (1 GB300); dispatch/combine HBM GB/s; grouped-GEMM TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="deepseek_v3")
+    p.add_argument("--tokens", type=int, default=None, help="override N (profiling cases)")
+    p.add_argument("--experts", type=int, default=None, help="override E (profiling cases)")
+    p.add_argument("--dedup", choices=["auto", "on", "off"], default="auto")
+    p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------- workload
+
+def workload(args):
+    from combine_warp_top_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    changes = {}
+    if args.tokens is not None:
+        changes["N"] = args.tokens
+    if args.experts is not None:
+        changes["E"] = args.experts
+        changes["W"] = min(wl.W, args.experts)
+    if args.dedup != "auto":
+        changes["dedup"] = args.dedup == "on"
+    if changes:
+        import dataclasses
+        wl = dataclasses.replace(wl, name=wl.name + "_" + "_".join(f"{k}{v}" for k, v in changes.items()),
+                                 **changes)
+    return wl
+
+
+def algorithmic(wl, R_d):
+    """Bytes each stage must move and flops it must do (bf16 activations and
+    weights, fp32 logits and weights of the router)."""
+    N, H, E, k, I, W = wl.N, wl.H, wl.E, wl.k, wl.I, wl.W
+    R = N * k
+    rows_d = R_d if wl.dedup else R
+    st = {
+        "route": dict(bytes=N * E * 4 + R * 8),
+        "layout": dict(bytes=2 * R * 4 + (5 if wl.dedup else 2) * R * 4),
+        "dispatch": dict(bytes=N * H * 2 + rows_d * H * 2),
+        "gate_up": dict(bytes=2 * E * I * H * 2 + R * H * 2 + R * I * 2, flops=4 * R * H * I),
+        "down": dict(bytes=E * H * I * 2 + R * I * 2 + R * H * 2, flops=2 * R * H * I),
+        "combine": dict(bytes=R * H * 2 + 2 * N * H * 2 + R * 8 +
+                        (2 * R_d * H * 2 if wl.dedup else 0)),
+    }
+    if wl.dedup:
+        st["expand"] = dict(bytes=R_d * H * 2 + R * H * 2)
+    return st
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ["timestamp", "index", "clocks.sm", "clocks.max.sm", "power.draw",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(1.0)  # nvidia-smi needs a moment before its first sample
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                ts = dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t0 <= r[0] <= self.t1]
+        window = "timed region"
+        if len(inside) < 3:
+            inside = [r for r in rows if self.t0 - 0.5 <= r[0] <= self.t1 + 0.5]
+            window = "timed region +-0.5 s"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median([r[1] for r in inside]) if inside else None,
+                "sm_max_mhz": max((r[2] for r in inside), default=None),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ---------------------------------------------------------------------------- oracle timing
+
+def oracle_worker(spec):
+    """Times the CPU oracle (route + the layer output straight from the MoE
+    definition) on routed (token, expert) pairs of the workload.  Runs in its
+    own single-threaded process.  spec: argv of the workload, number of steps,
+    seconds of oracle time per step (at least one pair per step)."""
+    import numpy as np  # noqa: F401
+
+    import oracle
+    from combine_warp_top_gb300 import synth
+    args = parse_args(spec["argv"])
+    wl = workload(args)
+    n_tok = min(wl.N, 4096)
+    L = synth.make_logits(wl, N=n_tok)
+    x = synth.make_x(wl, N=n_tok)
+    res = synth.make_residual(wl, N=n_tok)
+    weights = {}
+
+    def expert(e):  # input generation, not timed
+        if e not in weights:
+            if len(weights) > 16:
+                weights.clear()
+            weights[e] = tuple(synth.make_weight(wl, w, experts=[e])[0]
+                               for w in ("gate", "up", "down"))
+        return weights[e]
+
+    steps = []
+    t = 0
+    j = 0
+    ids = w = None
+    for _ in range(spec["steps"]):
+        t_oracle, pairs = 0.0, 0
+        while pairs == 0 or t_oracle < spec["seconds"]:
+            tt = t % n_tok
+            if j == 0:
+                c0 = time.perf_counter()
+                ids, w = oracle.route(L[tt:tt + 1], wl.k)
+                t_oracle += time.perf_counter() - c0
+            wg, wu, wd = expert(int(ids[0, j]))
+            c0 = time.perf_counter()
+            oracle.token_outputs(x[tt:tt + 1], ids[:, j:j + 1], w[:, j:j + 1],
+                                 lambda _e: (wg, wu, wd), res[tt:tt + 1] if j == 0 else None)
+            t_oracle += time.perf_counter() - c0
+            pairs += 1
+            j += 1
+            if j == wl.k:
+                j = 0
+                t += 1
+        steps.append({"pairs": pairs, "tokens": pairs / wl.k, "seconds": t_oracle})
+    return {"steps": steps, "k": wl.k}
+
+
+def run_oracle(argv, seconds, steps=1):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    spec = json.dumps({"argv": argv, "seconds": seconds, "steps": steps})
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-worker", spec],
+                       capture_output=True, text=True, env=env, cwd=ROOT)
+    if r.returncode != 0:
+        raise RuntimeError("oracle worker failed:\n" + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def strip_args(argv):
+    keep, skip = [], False
+    for a in argv:
+        if skip:
+            skip = False
+            continue
+        if a in ("--impl", "--gpus", "--steps", "--warmup", "--e2e-steps", "--cpu-seconds"):
+            skip = True
+            continue
+        if a.startswith("--impl=") or a == "--no-cpu-baseline":
+            continue
+        keep.append(a)
+    return keep
+
+
+# ---------------------------------------------------------------------------- distributed
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, local):
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return dist
+
+
+def max_over_ranks(value, world):
+    import torch
+    import torch.distributed as dist
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    import torch.distributed as dist
+    if world > 1:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from combine_warp_top_gb300 import moe, synth
+
+    world, rank, local = dist_info()
+    dist_init(world, local)
+    torch.cuda.set_device(local)
+    wl = workload(args)
+    seed = rank  # every rank has its own tokens; weights are the same layer
+    shape = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=wl.dedup)
+
+    w_gate = synth.make_weight_device(wl, "gate")
+    w_up = synth.make_weight_device(wl, "up")
+    w_down = synth.make_weight_device(wl, "down")
+    placement = synth.make_placement(wl)
+    placement_d = None if wl.placement == "contiguous" else torch.from_numpy(placement).cuda()
+    layer = moe.MoELayer(shape, w_gate, w_up, w_down, placement_d)
+
+    L_h = torch.from_numpy(synth.make_logits(wl, seed)).pin_memory()
+    x_h = torch.from_numpy(synth.make_x(wl, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
+    r_h = torch.from_numpy(synth.make_residual(wl, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_h = torch.empty(wl.N, wl.H, dtype=torch.bfloat16).pin_memory()
+    L_d, x_d, r_d = L_h.cuda(), x_h.cuda(), r_h.cuda()
+    torch.cuda.synchronize()
+
+    # rows a dedup dispatcher would send for this routing (reported, not timed)
+    dshape = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=True)
+    dlay, dws = moe.Layout(dshape), moe.workspace(dshape)
+    moe.moe_route(L_d, shape, layer.topk_ids, layer.topk_w)
+    moe.moe_dispatch_layout(layer.topk_ids, placement_d, dshape, dlay, dws)
+    torch.cuda.synchronize()
+    R_d = int(dlay["n_dedup_rows"].item())
+    counts = dlay["expert_counts"].cpu().numpy()
+    del dlay, dws
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        layer.forward_stages(L_d, x_d, r_d)
+    torch.cuda.synchronize()
+    layer.check_device_errors()
+
+    stages = [s for s in moe.MoELayer.STAGES if s != "expand" or wl.dedup]
+    ev = [{s: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for s in stages} for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t0")
+    t_start.record(stream)
+    for i in range(args.steps):
+        layer.forward_stages(L_d, x_d, r_d, events=ev[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t1")
+    barrier(world)
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    clocks = sampler.stop() if sampler else None
+    layer.check_device_errors()
+    stage_ms = {s: statistics.mean(e[s][0].elapsed_time(e[s][1]) for e in ev) for s in stages}
+
+    # end to end through the public call with host buffers
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 50))
+    dev_in = (L_d, x_d, r_d)
+    for _ in range(2):
+        layer.forward_host(L_h, x_h, r_h, out_h, dev_in)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        layer.forward_host(L_h, x_h, r_h, out_h, dev_in)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    layer.check_device_errors()
+
+    if rank != 0:
+        return None
+
+    pk, pk_src = peaks()
+    alg = algorithmic(wl, R_d)
+    ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    stage_report = {}
+    for s in stages:
+        ms = stage_ms[s]
+        d = {"ms": round(ms, 4), "GB/s": round(alg[s]["bytes"] / ms / 1e6, 1)}
+        d["hbm_frac"] = round(d["GB/s"] / pk["hbm_gbs"], 3)
+        if "flops" in alg[s]:
+            d["TFLOP/s"] = round(alg[s]["flops"] / ms / 1e9, 1)
+            d["tensor_frac"] = round(d["TFLOP/s"] / pk["bf16_tflops_sustained"], 3)
+            d["bound"] = "tensor" if alg[s]["flops"] / alg[s]["bytes"] > ridge else "hbm"
+        stage_report[s] = d
+
+    dom = "gate_up"
+    a = alg[dom]
+    intensity = a["flops"] / a["bytes"]
+    if intensity > ridge:
+        achieved = a["flops"] / stage_ms[dom] / 1e9
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops_sustained"],
+                "unit": "TFLOP/s"}
+    else:
+        achieved = a["bytes"] / stage_ms[dom] / 1e6
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 3)
+    roof["traffic"] = None
+    roof["kernel"] = "grouped_gemm_kernel<SwiGLU> (moe_ffn_gate_up)"
+    roof["peak_source"] = f"{pk_src} ({'bf16_tflops_sustained' if roof['unit'] == 'TFLOP/s' else 'hbm_gbs'})"
+    roof["algorithmic_per_launch"] = {"bytes": a["bytes"], "flops": a["flops"]}
+
+    tokens = wl.N * args.steps * world
+    value = tokens / (elapsed_ms / 1e3)
+    e2e_value = wl.N * e2e_steps * world / (e2e_ms / 1e3)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64/Box-Muller; random-init expert weights)",
+        "config": {"workload": wl.name, "N": wl.N, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
+                   "W": wl.W, "dedup": wl.dedup, "placement": wl.placement,
+                   "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU",
+                   "l2": f"no flush: {3 * wl.E * wl.H * wl.I * 2 / 1e9:.2f} GB of expert weights "
+                         "read per step, larger than the 129 MB L2"},
+        "roofline": roof,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": wl.N * wl.E * 4 + 2 * wl.N * wl.H * 2,
+                "d2h_bytes_per_step": wl.N * wl.H * 2},
+        "gpu_launches": layer.kernel_launches_per_step() * args.steps,
+        "clocks": clocks,
+        "stages": stage_report,
+        "dispatch_rows": {"plain": wl.N * wl.k, "dedup": R_d,
+                          "dedup_reduction": round(1 - R_d / (wl.N * wl.k), 4),
+                          "max_over_mean_expert_load": round(float(counts.max() / counts.mean()), 3)},
+    }
+    if not args.no_cpu_baseline and world == 1:
+        cb = run_oracle(strip_args(sys.argv[1:]), args.cpu_seconds)["steps"][0]
+        line["cpu_baseline"] = {
+            "value": round(cb["tokens"] / cb["seconds"], 4), "unit": "tokens/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{cb['pairs']} routed (token, expert) pairs = {cb['tokens']:.3g} tokens of "
+                      f"the {wl.name} workload (route + SwiGLU expert + weighted sum + residual, "
+                      f"float64 numpy, one thread), {cb['seconds']:.1f} s of oracle time"}
+    return line
+
+
+# ---------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return None
+    wl = workload(args)
+    argv = strip_args(sys.argv[1:])
+    steps_total = args.steps + args.warmup
+    # each step gets an equal share of about two minutes of oracle time
+    per_step = 120.0 / steps_total
+    r = run_oracle(argv, per_step, steps=steps_total)["steps"][args.warmup:]
+    tokens = sum(s["tokens"] for s in r)
+    secs = sum(s["seconds"] for s in r)
+    value = tokens / secs if secs > 0 else 0.0
+    return {
+        "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / len(r) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": wl.name, "N": wl.N, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
+                   "W": wl.W, "dedup": wl.dedup, "placement": wl.placement},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: routed (token, expert) pairs of the {wl.name} "
+                                   f"workload for ~{per_step:.2f} s of oracle time, at least one "
+                                   f"pair ({tokens:.3g} tokens over {len(r)} timed steps)"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    if args.oracle_worker:
+        print(json.dumps(oracle_worker(json.loads(args.oracle_worker))))
+        return
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -547,48 +547,75 @@ bool map_3d(CUtensorMap* m, const void* ptr, uint64_t E, uint64_t rows, uint64_t
 
 }  // namespace
 
-moe_status launch_expert_ffn(const uint16_t* xa, const moe_layout& L, const moe_shape& s,
-                             const uint16_t* wg, const uint16_t* wu, const uint16_t* wd,
-                             uint16_t* h, uint16_t* y, void* ws, cudaStream_t st) {
-    const int R = s.N * s.k;
-    if (R == 0) return MOE_OK;
+namespace {
+
+bool set_smem_attr() {
+    return cudaFuncSetAttribute(grouped_gemm_kernel<true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kSmemBytes) == cudaSuccess &&
+           cudaFuncSetAttribute(grouped_gemm_kernel<false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kSmemBytes) == cudaSuccess;
+}
+
+// Writes the m-block prefix of the tile schedule into the workspace and
+// returns the persistent grid size for a GEMM with `n_tiles_per_mblock`
+// n-blocks: never more CTAs than tiles, never more than one per SM.
+moe_status schedule(const moe_layout& L, const moe_shape& s, void* ws, cudaStream_t st,
+                    long long n_blocks, int32_t** prefix_out, int* grid) {
     const Workspace wl = workspace_layout(s);
-    int* err = ws_ptr<int>(ws, wl.err);
     int32_t* prefix = ws_ptr<int32_t>(ws, wl.mblk_prefix);
-
-    CUtensorMap a1, bg, bu, a2, bd;
-    if (!map_2d(&a1, xa, R, s.H, BM) || !map_3d(&bg, wg, s.E, s.I, s.H, kMmaN / 2) ||
-        !map_3d(&bu, wu, s.E, s.I, s.H, kMmaN / 2) || !map_2d(&a2, h, R, s.I, BM) ||
-        !map_3d(&bd, wd, s.E, s.H, s.I, kMmaN))
-        return MOE_ERR_UNSUPPORTED;
-
     schedule_kernel<<<1, 1024, 0, st>>>(L.expert_counts, s.E, prefix);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(grouped_gemm_kernel<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
-        return MOE_ERR_CUDA;
-
-    // tiles <= NB * (ceil(R / BM) + E): every expert adds at most one ragged m-block
-    const long long mblocks = (R + BM - 1) / BM + s.E;
+    // tiles <= n_blocks * (ceil(R / BM) + E): each expert adds at most one ragged m-block
+    const long long R = (long long)s.N * s.k;
+    const long long tiles = n_blocks * ((R + BM - 1) / BM + s.E);
     const int sms = sm_count();
-    const long long t1 = mblocks * ((s.I + kMmaN / 2 - 1) / (kMmaN / 2));
-    const long long t2 = mblocks * ((s.H + kMmaN - 1) / kMmaN);
-    const int g1 = (int)(t1 < sms ? t1 : sms);
-    const int g2 = (int)(t2 < sms ? t2 : sms);
-
-    grouped_gemm_kernel<true><<<g1, kThreads, kSmemBytes, st>>>(
-        a1, bg, bu, L.expert_offsets, L.expert_counts, prefix, s.E, s.H, s.I,
-        reinterpret_cast<__nv_bfloat16*>(h), err);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-    grouped_gemm_kernel<false><<<g2, kThreads, kSmemBytes, st>>>(
-        a2, bd, bd, L.expert_offsets, L.expert_counts, prefix, s.E, s.I, s.H,
-        reinterpret_cast<__nv_bfloat16*>(y), err);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    *grid = (int)(tiles < sms ? tiles : sms);
+    *prefix_out = prefix;
     return MOE_OK;
+}
+
+}  // namespace
+
+moe_status launch_gate_up(const uint16_t* rows, const moe_layout& L, const moe_shape& s,
+                          const uint16_t* wg, const uint16_t* wu, uint16_t* h, void* ws,
+                          cudaStream_t st) {
+    const int R = s.N * s.k;
+    if (R == 0) return MOE_OK;
+    CUtensorMap a, bg, bu;
+    if (!map_2d(&a, rows, R, s.H, BM) || !map_3d(&bg, wg, s.E, s.I, s.H, kMmaN / 2) ||
+        !map_3d(&bu, wu, s.E, s.I, s.H, kMmaN / 2))
+        return MOE_ERR_UNSUPPORTED;
+    if (!set_smem_attr()) return MOE_ERR_CUDA;
+    int32_t* prefix;
+    int grid;
+    const moe_status ss = schedule(L, s, ws, st, (s.I + kMmaN / 2 - 1) / (kMmaN / 2), &prefix, &grid);
+    if (ss != MOE_OK) return ss;
+    int* err = ws_ptr<int>(ws, workspace_layout(s).err);
+    grouped_gemm_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(
+        a, bg, bu, L.expert_offsets, L.expert_counts, prefix, s.E, s.H, s.I,
+        reinterpret_cast<__nv_bfloat16*>(h), err);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status launch_down(const uint16_t* h, const moe_layout& L, const moe_shape& s,
+                       const uint16_t* wd, uint16_t* y, void* ws, cudaStream_t st) {
+    const int R = s.N * s.k;
+    if (R == 0) return MOE_OK;
+    CUtensorMap a, bd;
+    if (!map_2d(&a, h, R, s.I, BM) || !map_3d(&bd, wd, s.E, s.H, s.I, kMmaN))
+        return MOE_ERR_UNSUPPORTED;
+    if (!set_smem_attr()) return MOE_ERR_CUDA;
+    int32_t* prefix;
+    int grid;
+    const moe_status ss = schedule(L, s, ws, st, (s.H + kMmaN - 1) / kMmaN, &prefix, &grid);
+    if (ss != MOE_OK) return ss;
+    int* err = ws_ptr<int>(ws, workspace_layout(s).err);
+    grouped_gemm_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(
+        a, bd, bd, L.expert_offsets, L.expert_counts, prefix, s.E, s.I, s.H,
+        reinterpret_cast<__nv_bfloat16*>(y), err);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace moe

@@ -99,6 +99,38 @@ moe_status moe_dispatch(const uint16_t* x, const moe_layout* layout, const moe_s
     return cuda_status(launch_dispatch(x, *layout, *shape, xd, as_stream(stream)));
 }
 
+moe_status moe_expand(const uint16_t* xd, const moe_layout* layout, const moe_shape* shape,
+                      uint16_t* xe, void* stream) {
+    MOE_TRY(check_shape(shape));
+    MOE_TRY(check_layout(layout, shape));
+    if (!shape->dedup) return MOE_ERR_INVALID_ARG;
+    if (shape->N == 0) return MOE_OK;
+    if (!xd || !xe) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_expand(xd, *layout, *shape, xe, as_stream(stream)));
+}
+
+moe_status moe_ffn_gate_up(const uint16_t* rows, const moe_layout* layout, const moe_shape* shape,
+                           const uint16_t* w_gate, const uint16_t* w_up, uint16_t* h, void* ws,
+                           size_t ws_bytes, void* stream) {
+    MOE_TRY(check_shape(shape));
+    MOE_TRY(check_layout(layout, shape));
+    MOE_TRY(check_ws(shape, ws, ws_bytes));
+    if (shape->N == 0) return MOE_OK;
+    if (!rows || !w_gate || !w_up || !h) return MOE_ERR_INVALID_ARG;
+    return launch_gate_up(rows, *layout, *shape, w_gate, w_up, h, ws, as_stream(stream));
+}
+
+moe_status moe_ffn_down(const uint16_t* h, const moe_layout* layout, const moe_shape* shape,
+                        const uint16_t* w_down, uint16_t* y, void* ws, size_t ws_bytes,
+                        void* stream) {
+    MOE_TRY(check_shape(shape));
+    MOE_TRY(check_layout(layout, shape));
+    MOE_TRY(check_ws(shape, ws, ws_bytes));
+    if (shape->N == 0) return MOE_OK;
+    if (!h || !w_down || !y) return MOE_ERR_INVALID_ARG;
+    return launch_down(h, *layout, *shape, w_down, y, ws, as_stream(stream));
+}
+
 moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const moe_shape* shape,
                           const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
                           uint16_t* xe, uint16_t* h, uint16_t* y, void* ws, size_t ws_bytes,
@@ -109,13 +141,13 @@ moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const mo
     if (shape->N == 0) return MOE_OK;
     if (!xd || !w_gate || !w_up || !w_down || !h || !y) return MOE_ERR_INVALID_ARG;
     if (shape->dedup && !xe) return MOE_ERR_INVALID_ARG;
-    cudaStream_t st = as_stream(stream);
-    const uint16_t* a = xd;
+    const uint16_t* rows = xd;
     if (shape->dedup) {
-        MOE_TRY(cuda_status(launch_expand(xd, *layout, *shape, xe, st)));
-        a = xe;
+        MOE_TRY(moe_expand(xd, layout, shape, xe, stream));
+        rows = xe;
     }
-    return launch_expert_ffn(a, *layout, *shape, w_gate, w_up, w_down, h, y, ws, st);
+    MOE_TRY(moe_ffn_gate_up(rows, layout, shape, w_gate, w_up, h, ws, ws_bytes, stream));
+    return moe_ffn_down(h, layout, shape, w_down, y, ws, ws_bytes, stream);
 }
 
 moe_status moe_combine(const uint16_t* y, const float* topk_w, const moe_layout* layout,

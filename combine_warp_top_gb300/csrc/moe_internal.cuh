@@ -71,11 +71,13 @@ cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& 
                            const moe_shape& s, uint16_t* partial, const uint16_t* residual,
                            uint16_t* out, cudaStream_t st);
 
-// Returns MOE_OK, or an error status when a host-side step (tensor-map
+// Return MOE_OK, or an error status when a host-side step (tensor-map
 // encoding, launch) failed.
-moe_status launch_expert_ffn(const uint16_t* xa, const moe_layout& L, const moe_shape& s,
-                             const uint16_t* wg, const uint16_t* wu, const uint16_t* wd,
-                             uint16_t* h, uint16_t* y, void* ws, cudaStream_t st);
+moe_status launch_gate_up(const uint16_t* rows, const moe_layout& L, const moe_shape& s,
+                          const uint16_t* wg, const uint16_t* wu, uint16_t* h, void* ws,
+                          cudaStream_t st);
+moe_status launch_down(const uint16_t* h, const moe_layout& L, const moe_shape& s,
+                       const uint16_t* wd, uint16_t* y, void* ws, cudaStream_t st);
 
 int sm_count();
 

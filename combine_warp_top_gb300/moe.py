@@ -57,6 +57,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_dispatch_layout": (I32, [P, P, shp, lay, P, S, P]),
         "moe_dispatch": (I32, [P, lay, shp, P, P]),
         "moe_expert_ffn": (I32, [P, lay, shp, P, P, P, P, P, P, P, S, P]),
+        "moe_expand": (I32, [P, lay, shp, P, P]),
+        "moe_ffn_gate_up": (I32, [P, lay, shp, P, P, P, P, S, P]),
+        "moe_ffn_down": (I32, [P, lay, shp, P, P, P, S, P]),
         "moe_combine": (I32, [P, P, lay, shp, P, P, P, P]),
         "moe_layer_forward": (I32, [P, P, P, P, P, P, P, shp, P, P, lay, P, P, P, P, P, P, P, S,
                                     P]),
@@ -180,6 +183,23 @@ def moe_expert_ffn(xd, layout: Layout, shape: Shape, w_gate, w_up, w_down, xe, h
                                  _ptr(ws), ws.numel(), _stream(stream)), "moe_expert_ffn")
 
 
+def moe_expand(xd, layout: Layout, shape: Shape, xe, stream=None):
+    _check(load().moe_expand(_ptr(xd), ctypes.byref(layout.c), ctypes.byref(shape.c()), _ptr(xe),
+                             _stream(stream)), "moe_expand")
+
+
+def moe_ffn_gate_up(rows, layout: Layout, shape: Shape, w_gate, w_up, h, ws, stream=None):
+    _check(load().moe_ffn_gate_up(_ptr(rows), ctypes.byref(layout.c), ctypes.byref(shape.c()),
+                                  _ptr(w_gate), _ptr(w_up), _ptr(h), _ptr(ws), ws.numel(),
+                                  _stream(stream)), "moe_ffn_gate_up")
+
+
+def moe_ffn_down(h, layout: Layout, shape: Shape, w_down, y, ws, stream=None):
+    _check(load().moe_ffn_down(_ptr(h), ctypes.byref(layout.c), ctypes.byref(shape.c()),
+                               _ptr(w_down), _ptr(y), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_ffn_down")
+
+
 def moe_combine(y, topk_w, layout: Layout, shape: Shape, partial, residual, out, stream=None):
     _check(load().moe_combine(_ptr(y), _ptr(topk_w), ctypes.byref(layout.c),
                               ctypes.byref(shape.c()), _ptr(partial), _ptr(residual), _ptr(out),
@@ -235,6 +255,74 @@ class MoELayer:
                           residual, self.shape, self.topk_ids, self.topk_w, self.layout,
                           self.xd, self.xe, self.h, self.y, self.partial, out, self.ws, stream)
         return out
+
+    STAGES = ("route", "layout", "dispatch", "expand", "gate_up", "down", "combine")
+
+    def forward_stages(self, logits, x, residual=None, out=None, stream=None, events=None):
+        """The same kernels as forward(), one C call per stage of the pages'
+        pipeline.  If ``events`` maps stage names to (start, end) CUDA events,
+        they are recorded around each stage on the stream."""
+        out = self.out if out is None else out
+        st = torch.cuda.current_stream() if stream is None else stream
+        s = self.shape
+
+        def rec(name, i):
+            if events is not None and name in events:
+                events[name][i].record(st)
+
+        rec("route", 0)
+        moe_route(logits, s, self.topk_ids, self.topk_w, st)
+        rec("route", 1)
+        rec("layout", 0)
+        moe_dispatch_layout(self.topk_ids, self.placement, s, self.layout, self.ws, st)
+        rec("layout", 1)
+        rec("dispatch", 0)
+        moe_dispatch(x, self.layout, s, self.xd, st)
+        rec("dispatch", 1)
+        rows = self.xd
+        if s.dedup:
+            rec("expand", 0)
+            moe_expand(self.xd, self.layout, s, self.xe, st)
+            rec("expand", 1)
+            rows = self.xe
+        rec("gate_up", 0)
+        moe_ffn_gate_up(rows, self.layout, s, self.w_gate, self.w_up, self.h, self.ws, st)
+        rec("gate_up", 1)
+        rec("down", 0)
+        moe_ffn_down(self.h, self.layout, s, self.w_down, self.y, self.ws, st)
+        rec("down", 1)
+        rec("combine", 0)
+        moe_combine(self.y, self.topk_w, self.layout, s, self.partial, residual, out, st)
+        rec("combine", 1)
+        return out
+
+    def kernel_launches_per_step(self) -> int:
+        """Kernels of this library launched by one forward (route 1, layout 3,
+        dispatch 1, expand 1 with dedup, each GEMM 2 with its schedule, combine
+        1 or 2 with dedup)."""
+        s = self.shape
+        if s.N == 0:
+            return 0
+        return 1 + 3 + 1 + (1 if s.dedup else 0) + 2 + 2 + (2 if s.dedup else 1)
+
+    def forward_host(self, logits_h, x_h, residual_h, out_h, dev_inputs=None, stream=None):
+        """Whole layer from host buffers: copy the step's inputs host->device,
+        run moe_layer_forward, copy the output device->host, all on one stream.
+        Host tensors should be pinned for the copies to be asynchronous."""
+        st = torch.cuda.current_stream() if stream is None else stream
+        if dev_inputs is None:
+            dev_inputs = (torch.empty_like(logits_h, device="cuda"),
+                          torch.empty_like(x_h, device="cuda"),
+                          None if residual_h is None else torch.empty_like(residual_h, device="cuda"))
+        L_d, x_d, r_d = dev_inputs
+        with torch.cuda.stream(st):
+            L_d.copy_(logits_h, non_blocking=True)
+            x_d.copy_(x_h, non_blocking=True)
+            if residual_h is not None:
+                r_d.copy_(residual_h, non_blocking=True)
+            out = self.forward(L_d, x_d, r_d if residual_h is not None else None, stream=st)
+            out_h.copy_(out, non_blocking=True)
+        return out_h
 
     def check_device_errors(self, stream=None):
         st = moe_get_error(self.ws, stream)

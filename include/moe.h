@@ -136,6 +136,27 @@ moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const mo
                           uint16_t* xe, uint16_t* h, uint16_t* y, void* ws, size_t ws_bytes,
                           void* stream);
 
+/* The three steps of moe_expert_ffn as separate calls (kernel-fusion page,
+ * "Fusing the layer into one kernel": stage 3 "group", stages 4-5 "MatMul" +
+ * "SwiGLU", stage 6 "MatMul").  moe_expert_ffn is exactly
+ *   [dedup: moe_expand(xd -> xe)]; moe_ffn_gate_up(rows -> h); moe_ffn_down(h -> y)
+ * on one stream.
+ * moe_expand:      xe[i, :] = xd[expand_src[i], :] for the N*k expert-major rows
+ *                  (dedup only; bit-exact copies).  Returns MOE_ERR_INVALID_ARG
+ *                  when shape->dedup == 0.
+ * moe_ffn_gate_up: h = bf16(SiLU(rows Wg[e]^T) * (rows Wu[e]^T)) for the
+ *                  expert-major rows [N*k, H] (xd when plain, xe when dedup).
+ * moe_ffn_down:    y = bf16(h Wd[e]^T).
+ * Both GEMM calls take the workspace (they write their tile schedule there). */
+moe_status moe_expand(const uint16_t* xd, const moe_layout* layout, const moe_shape* shape,
+                      uint16_t* xe, void* stream);
+moe_status moe_ffn_gate_up(const uint16_t* rows, const moe_layout* layout, const moe_shape* shape,
+                           const uint16_t* w_gate, const uint16_t* w_up, uint16_t* h, void* ws,
+                           size_t ws_bytes, void* stream);
+moe_status moe_ffn_down(const uint16_t* h, const moe_layout* layout, const moe_shape* shape,
+                        const uint16_t* w_down, uint16_t* y, void* ws, size_t ws_bytes,
+                        void* stream);
+
 /* Combine (kernel-fusion page, "Expert parallelism: dispatch and combine" and
  * stage 7 "reduce"; residual add of FarSkip-Collective Sec. 3).
  * Plain: out[t, :] = bf16( residual[t, :] + sum_j topk_w[t, j] * y[pair_row[t, j], :] ),
