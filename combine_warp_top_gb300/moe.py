@@ -328,3 +328,57 @@ class MoELayer:
         st = moe_get_error(self.ws, stream)
         if st != 0:
             raise MoeError(st, "device")
+
+
+class HostPipeline:
+    """Runs one MoELayer over a sequence of host-resident batches with the
+    transfers overlapped: while batch i computes on the compute stream, batch
+    i+1's inputs are copied host->device on one copy stream and batch i-1's
+    output device->host on another.  Two sets of device input/output buffers
+    alternate; events order every reuse.  Host tensors should be pinned."""
+
+    def __init__(self, layer: "MoELayer", with_residual=True, device="cuda"):
+        s = layer.shape
+        self.layer = layer
+        bf = dict(dtype=torch.bfloat16, device=device)
+        self.bufs = []
+        for _ in range(2):
+            self.bufs.append(dict(
+                logits=torch.empty(max(s.N, 1), s.E, dtype=torch.float32, device=device),
+                x=torch.empty(max(s.N, 1), s.H, **bf),
+                res=torch.empty(max(s.N, 1), s.H, **bf) if with_residual else None,
+                out=torch.empty(max(s.N, 1), s.H, **bf)))
+        self.h2d = torch.cuda.Stream(device=device)
+        self.d2h = torch.cuda.Stream(device=device)
+        mk = lambda: [torch.cuda.Event(), torch.cuda.Event()]  # noqa: E731
+        self.loaded, self.computed, self.saved = mk(), mk(), mk()
+
+    def run(self, batches, stream=None):
+        """batches: iterable of (logits_h, x_h, residual_h or None, out_h).
+        Enqueues everything; the caller synchronizes (or waits on `stream`,
+        which is made to wait for the last device->host copy)."""
+        comp = torch.cuda.current_stream() if stream is None else stream
+        self.h2d.wait_stream(comp)
+        self.d2h.wait_stream(comp)
+        for i, (L_h, x_h, r_h, out_h) in enumerate(batches):
+            b = i % 2
+            buf = self.bufs[b]
+            if i >= 2:
+                self.h2d.wait_event(self.computed[b])  # inputs of batch i-2 consumed
+            with torch.cuda.stream(self.h2d):
+                buf["logits"].copy_(L_h, non_blocking=True)
+                buf["x"].copy_(x_h, non_blocking=True)
+                if r_h is not None:
+                    buf["res"].copy_(r_h, non_blocking=True)
+                self.loaded[b].record(self.h2d)
+            comp.wait_event(self.loaded[b])
+            if i >= 2:
+                comp.wait_event(self.saved[b])  # output of batch i-2 copied out
+            self.layer.forward(buf["logits"], buf["x"], buf["res"] if r_h is not None else None,
+                               out=buf["out"], stream=comp)
+            self.computed[b].record(comp)
+            self.d2h.wait_event(self.computed[b])
+            with torch.cuda.stream(self.d2h):
+                out_h.copy_(buf["out"], non_blocking=True)
+                self.saved[b].record(self.d2h)
+        comp.wait_stream(self.d2h)

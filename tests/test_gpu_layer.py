@@ -129,3 +129,23 @@ def test_bad_placement_is_reported_by_the_device():
     assert moe.moe_get_error(ws) == 0  # cleared by the read
     moe.moe_dispatch_layout(dev_i32(ids), None, shape, lay, ws)
     assert moe.moe_get_error(ws) == 0
+
+
+def test_host_pipeline_matches_device_forward():
+    """The overlapped host-buffer path returns, batch by batch, exactly what the
+    device-resident call returns."""
+    wl = SMALL["wide"]
+    layer, _ = build_layer(wl, False)
+    batches, want = [], []
+    for seed in range(4):
+        L = torch.from_numpy(synth.make_logits(wl, seed)).pin_memory()
+        x = torch.from_numpy(synth.make_x(wl, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
+        r = torch.from_numpy(synth.make_residual(wl, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
+        out = torch.empty(wl.N, wl.H, dtype=torch.bfloat16).pin_memory()
+        batches.append((L, x, r, out))
+        want.append(layer.forward(L.cuda(), x.cuda(), r.cuda()).cpu().clone())
+    pipe = moe.HostPipeline(layer)
+    pipe.run(batches)
+    torch.cuda.synchronize()
+    for (_, _, _, out), w in zip(batches, want):
+        assert torch.equal(out.view(torch.int16), w.view(torch.int16))
