@@ -63,6 +63,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_combine": (I32, [P, P, lay, shp, P, P, P, P]),
         "moe_layer_forward": (I32, [P, P, P, P, P, P, P, shp, P, P, lay, P, P, P, P, P, P, P, S,
                                     P]),
+        "moe_dispatch_layout_noalloc": (I32, [P, P, shp, lay, P]),
         "moe_get_error": (I32, [P, P]),
         "moe_status_str": (ctypes.c_char_p, [I32]),
     }
@@ -169,6 +170,12 @@ def moe_dispatch_layout(topk_ids, placement, shape: Shape, layout: Layout, ws, s
     _check(load().moe_dispatch_layout(_ptr(topk_ids), _ptr(placement), ctypes.byref(shape.c()),
                                       ctypes.byref(layout.c), _ptr(ws), ws.numel(),
                                       _stream(stream)), "moe_dispatch_layout")
+
+
+def moe_dispatch_layout_noalloc(topk_ids, placement, shape: Shape, layout: Layout, stream=None):
+    _check(load().moe_dispatch_layout_noalloc(_ptr(topk_ids), _ptr(placement),
+                                              ctypes.byref(shape.c()), ctypes.byref(layout.c),
+                                              _stream(stream)), "moe_dispatch_layout_noalloc")
 
 
 def moe_dispatch(x, layout: Layout, shape: Shape, xd, stream=None):

@@ -184,6 +184,21 @@ moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32
                              uint16_t* y, uint16_t* partial, uint16_t* out, void* ws,
                              size_t ws_bytes, void* stream);
 
+/* moe_dispatch_layout without a workspace argument, for callers that cannot
+ * allocate device memory when they call the library (an inference runtime's
+ * enqueue path that forbids allocation while it executes, a host whose device
+ * memory is entirely owned by its own pool).  The pages have no counterpart:
+ * it exists only for such callers.  Same inputs, outputs and results as
+ * moe_dispatch_layout; its scratch is a static 1 MiB device array per GPU
+ * (held until the process exits), so shapes with moe_workspace_bytes() > 1 MiB
+ * return MOE_ERR_WORKSPACE.  It allocates nothing.  Every call on a GPU shares
+ * that array: calls that overlap on the GPU race.  The first call on a device
+ * looks up the array's address; make it before any stream capture.
+ * Device-detected input problems are not reported by this variant. */
+moe_status moe_dispatch_layout_noalloc(const int32_t* topk_ids, const int32_t* placement,
+                                       const moe_shape* shape, const moe_layout* layout,
+                                       void* stream);
+
 /* Synchronizes `stream`, reads the workspace error word, clears it, and
  * returns it (MOE_OK if no device-side problem was recorded). */
 moe_status moe_get_error(void* ws, void* stream);
