@@ -53,18 +53,23 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
     return o;
 }
 
-// acc += sum over the set bits j of `srcs` (ascending) of w_j * rows[row_j][c]
-// where lane j holds row_j / w_j.  Warp-uniform control flow.
-__device__ __forceinline__ void gather_weighted(float (&acc)[8], const uint4* __restrict__ rows,
-                                                int C, int c, bool active, uint32_t srcs,
-                                                int my_row, float my_w) {
+// acc[u] += sum over the set bits j of `srcs` (ascending) of w_j * rows[row_j][c_u]
+// for U chunks c_u = c0 + u*32 + lane at once, where lane j holds row_j / w_j.
+// Loads of up to kLoads (row, chunk) pairs are issued before any is used.
+// Warp-uniform control flow.
+template <int U>
+__device__ __forceinline__ void gather_weighted(float (&acc)[U][8], const uint4* __restrict__ rows,
+                                                int C, int c0, uint32_t srcs, int my_row,
+                                                float my_w) {
+    constexpr int kRows = kBatch / U > 0 ? kBatch / U : 1;  // source rows per batch
+    const int lane = threadIdx.x & 31;
     while (srcs) {
-        uint4 v[kBatch];
-        int js[kBatch];
+        uint4 v[kRows][U];
+        int js[kRows];
         int n = 0;
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-            js[b] = -1;
+        for (int b = 0; b < kRows; ++b) {
+            js[b] = 0;
             if (srcs) {
                 js[b] = __ffs(srcs) - 1;
                 srcs &= srcs - 1;
@@ -72,23 +77,64 @@ __device__ __forceinline__ void gather_weighted(float (&acc)[8], const uint4* __
             }
         }
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
+        for (int b = 0; b < kRows; ++b) {
             if (b < n) {
                 const int r = __shfl_sync(0xffffffffu, my_row, js[b]);
-                if (active) v[b] = rows[(size_t)r * C + c];
+                const uint4* src = rows + (size_t)r * C;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = c0 + u * 32 + lane;
+                    if (c < C) v[b][u] = src[c];
+                }
             }
         }
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
+        for (int b = 0; b < kRows; ++b) {
             if (b < n) {
                 const float w = __shfl_sync(0xffffffffu, my_w, js[b]);
-                if (active) acc_bf16x8(acc, v[b], w);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = c0 + u * 32 + lane;
+                    if (c < C) acc_bf16x8(acc[u], v[b][u], w);
+                }
             }
         }
     }
 }
 
+template <int U>
+__device__ __forceinline__ void zero(float (&acc)[U][8]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
+}
+
+// out[c] = bf16(acc (+ residual[c])) for the U chunks of this lane.
+template <int U>
+__device__ __forceinline__ void finish(float (&acc)[U][8], const uint4* residual, uint4* out,
+                                       size_t row_base, int C, int c0) {
+    const int lane = threadIdx.x & 31;
+    uint4 r[U];
+    if (residual) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = c0 + u * 32 + lane;
+            if (c < C) r[u] = residual[row_base + c];
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < C) {
+            if (residual) add_bf16x8(acc[u], r[u]);
+            out[row_base + c] = pack_bf16x8(acc[u]);
+        }
+    }
+}
+
 // Plain combine: out[t] = bf16(residual[t] + sum_j w[t,j] * y[pair_row[t,j]]).
+template <int U>
 __global__ void __launch_bounds__(kThreads) combine_kernel(
     const uint4* __restrict__ y, const float* __restrict__ topk_w,
     const int32_t* __restrict__ pair_row, int N, int C, int k, int R,
@@ -99,20 +145,17 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
     const int my_row = lane < k ? clamp_row(pair_row[(size_t)t * k + lane], R) : 0;
     const float my_w = lane < k ? topk_w[(size_t)t * k + lane] : 0.f;
     const uint32_t all = k >= 32 ? 0xffffffffu : ((1u << k) - 1u);
-    for (int c0 = 0; c0 < C; c0 += 32) {
-        const int c = c0 + lane;
-        const bool active = c < C;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        gather_weighted(acc, y, C, c, active, all, my_row, my_w);
-        if (active) {
-            if (residual) add_bf16x8(acc, residual[(size_t)t * C + c]);
-            out[(size_t)t * C + c] = pack_bf16x8(acc);
-        }
+    for (int c0 = 0; c0 < C; c0 += 32 * U) {
+        float acc[U][8];
+        zero(acc);
+        gather_weighted<U>(acc, y, C, c0, all, my_row, my_w);
+        finish<U>(acc, residual, out, (size_t)t * C, C, c0);
     }
 }
 
 // Dedup, expert-rank side: partial[d] = bf16(sum over the j of token t carried
 // by dedup row d of w[t,j] * y[pair_row[t,j]]), j ascending.
+template <int U>
 __global__ void __launch_bounds__(kThreads) rank_reduce_kernel(
     const uint4* __restrict__ y, const float* __restrict__ topk_w,
     const int32_t* __restrict__ pair_row, const int32_t* __restrict__ pair_dedup_row,
@@ -127,17 +170,17 @@ __global__ void __launch_bounds__(kThreads) rank_reduce_kernel(
     const float my_w = lane < k ? topk_w[(size_t)t * k + lane] : 0.f;
     const bool mine = lane < k && pair_dedup_row[(size_t)t * k + lane] == d;
     const uint32_t srcs = __ballot_sync(0xffffffffu, mine);
-    for (int c0 = 0; c0 < C; c0 += 32) {
-        const int c = c0 + lane;
-        const bool active = c < C;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        gather_weighted(acc, y, C, c, active, srcs, my_row, my_w);
-        if (active) partial[(size_t)d * C + c] = pack_bf16x8(acc);
+    for (int c0 = 0; c0 < C; c0 += 32 * U) {
+        float acc[U][8];
+        zero(acc);
+        gather_weighted<U>(acc, y, C, c0, srcs, my_row, my_w);
+        finish<U>(acc, nullptr, partial, (size_t)d * C, C, c0);
     }
 }
 
 // Dedup, owner side: out[t] = bf16(residual[t] + sum of the token's partial
 // rows in ascending rank order).
+template <int U>
 __global__ void __launch_bounds__(kThreads) owner_sum_kernel(
     const uint4* __restrict__ partial, const int32_t* __restrict__ pair_dedup_row, int N, int C,
     int k, int Rd_bound, const uint4* residual, uint4* out) {
@@ -167,15 +210,11 @@ __global__ void __launch_bounds__(kThreads) owner_sum_kernel(
         if (((firsts >> jj) & 1u) && b == lane) sorted_d = o;
     }
     const uint32_t srcs = nd >= 32 ? 0xffffffffu : ((1u << nd) - 1u);
-    for (int c0 = 0; c0 < C; c0 += 32) {
-        const int c = c0 + lane;
-        const bool active = c < C;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        gather_weighted(acc, partial, C, c, active, srcs, sorted_d, 1.0f);
-        if (active) {
-            if (residual) add_bf16x8(acc, residual[(size_t)t * C + c]);
-            out[(size_t)t * C + c] = pack_bf16x8(acc);
-        }
+    for (int c0 = 0; c0 < C; c0 += 32 * U) {
+        float acc[U][8];
+        zero(acc);
+        gather_weighted<U>(acc, partial, C, c0, srcs, sorted_d, 1.0f);
+        finish<U>(acc, residual, out, (size_t)t * C, C, c0);
     }
 }
 
@@ -190,21 +229,46 @@ cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& 
     const int C = s.H / 8;
     const int R = s.N * s.k;
     const uint4* res = reinterpret_cast<const uint4*>(residual);
+    // chunks per lane per iteration: keep ~8 source loads in flight per lane
+    const int kk = s.dedup ? (s.k < s.W ? s.k : s.W) : s.k;
+    const int U = kk <= 2 ? 4 : (kk <= 4 ? 2 : 1);
     if (!s.dedup) {
-        combine_kernel<<<warps_grid(s.N), kThreads, 0, st>>>(
-            reinterpret_cast<const uint4*>(y), w, L.pair_row, s.N, C, s.k, R, res,
-            reinterpret_cast<uint4*>(out));
+        const uint4* yy = reinterpret_cast<const uint4*>(y);
+        uint4* o = reinterpret_cast<uint4*>(out);
+        if (U == 4)
+            combine_kernel<4><<<warps_grid(s.N), kThreads, 0, st>>>(yy, w, L.pair_row, s.N, C, s.k, R, res, o);
+        else if (U == 2)
+            combine_kernel<2><<<warps_grid(s.N), kThreads, 0, st>>>(yy, w, L.pair_row, s.N, C, s.k, R, res, o);
+        else
+            combine_kernel<1><<<warps_grid(s.N), kThreads, 0, st>>>(yy, w, L.pair_row, s.N, C, s.k, R, res, o);
         return cudaGetLastError();
     }
     const int Rd_max = s.N * (s.k < s.W ? s.k : s.W);
-    rank_reduce_kernel<<<warps_grid(Rd_max), kThreads, 0, st>>>(
-        reinterpret_cast<const uint4*>(y), w, L.pair_row, L.pair_dedup_row, L.dedup_row_token,
-        L.n_dedup_rows, s.N, C, s.k, R, reinterpret_cast<uint4*>(partial));
+    const uint4* yy = reinterpret_cast<const uint4*>(y);
+    uint4* pp = reinterpret_cast<uint4*>(partial);
+    // a dedup row carries the token's experts on one rank: at most min(k, E/W) rows
+    const int per_rank = s.E / s.W;
+    const int kr = s.k < per_rank ? s.k : per_rank;
+    const int Ur = kr <= 2 ? 4 : (kr <= 4 ? 2 : 1);
+    if (Ur == 4)
+        rank_reduce_kernel<4><<<warps_grid(Rd_max), kThreads, 0, st>>>(
+            yy, w, L.pair_row, L.pair_dedup_row, L.dedup_row_token, L.n_dedup_rows, s.N, C, s.k, R, pp);
+    else if (Ur == 2)
+        rank_reduce_kernel<2><<<warps_grid(Rd_max), kThreads, 0, st>>>(
+            yy, w, L.pair_row, L.pair_dedup_row, L.dedup_row_token, L.n_dedup_rows, s.N, C, s.k, R, pp);
+    else
+        rank_reduce_kernel<1><<<warps_grid(Rd_max), kThreads, 0, st>>>(
+            yy, w, L.pair_row, L.pair_dedup_row, L.dedup_row_token, L.n_dedup_rows, s.N, C, s.k, R, pp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    owner_sum_kernel<<<warps_grid(s.N), kThreads, 0, st>>>(
-        reinterpret_cast<const uint4*>(partial), L.pair_dedup_row, s.N, C, s.k, Rd_max, res,
-        reinterpret_cast<uint4*>(out));
+    uint4* o = reinterpret_cast<uint4*>(out);
+    const uint4* cp = reinterpret_cast<const uint4*>(partial);
+    if (U == 4)
+        owner_sum_kernel<4><<<warps_grid(s.N), kThreads, 0, st>>>(cp, L.pair_dedup_row, s.N, C, s.k, Rd_max, res, o);
+    else if (U == 2)
+        owner_sum_kernel<2><<<warps_grid(s.N), kThreads, 0, st>>>(cp, L.pair_dedup_row, s.N, C, s.k, Rd_max, res, o);
+    else
+        owner_sum_kernel<1><<<warps_grid(s.N), kThreads, 0, st>>>(cp, L.pair_dedup_row, s.N, C, s.k, Rd_max, res, o);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,120 @@
+"""Parity at the full sizes of the five benchmark workloads, in the launch
+configuration bench.py times (one moe_layer_forward per step, weights filled
+in device memory).
+
+Integer results are checked in full against the oracle: routing ids, every
+layout table, the dedup row count.  Copies are checked bit for bit on sampled
+rows.  Float outputs are checked on sampled tokens, each recomputed by the
+oracle straight from the MoE definition with host-generated weights of the
+experts those tokens use."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_warp_top_gb300 import moe, synth
+from gpu_util import assert_close, dev_i32, host_f64, host_u16
+
+pytestmark = pytest.mark.gpu
+
+# workload -> number of sampled tokens for the float check
+SAMPLES = {"deepseek_v3": 8, "mixtral": 16, "correlated_contiguous": 24, "correlated_placed": 24,
+           "skewed": 12}
+
+
+def bf16_host(a):
+    return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+
+
+@pytest.fixture(scope="module")
+def runs():
+    return {}
+
+
+def run_full(name):
+    wl = synth.WORKLOADS[name]
+    shape = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=wl.dedup)
+    placement = synth.make_placement(wl)
+    pl_d = None if wl.placement == "contiguous" else dev_i32(placement)
+    layer = moe.MoELayer(shape, synth.make_weight_device(wl, "gate"),
+                         synth.make_weight_device(wl, "up"), synth.make_weight_device(wl, "down"),
+                         pl_d)
+    L = synth.make_logits(wl)
+    x = synth.make_x(wl)
+    res = synth.make_residual(wl)
+    out = layer.forward(torch.from_numpy(L).cuda(), bf16_host(x).cuda(), bf16_host(res).cuda())
+    torch.cuda.synchronize()
+    layer.check_device_errors()
+    return wl, layer, L, x, res, placement, out
+
+
+@pytest.mark.parametrize("name", list(SAMPLES))
+def test_full_size_workload(name):
+    wl, layer, L, x, res, placement, out = run_full(name)
+    N, k = wl.N, wl.k
+    # routing: ids bit-exact, weights to fp32 rounding
+    ids = layer.topk_ids.view(N, k).cpu().numpy()
+    w = layer.topk_w.view(N, k).cpu().numpy()
+    ref_ids, ref_w = oracle.route(L, k)
+    assert np.array_equal(ids, ref_ids)
+    np.testing.assert_allclose(w, ref_w, rtol=0, atol=2e-6)
+    # every layout table, bit-exact
+    ref = oracle.dispatch_layout(ref_ids, placement, wl.E, wl.W)
+    got = {n: t.cpu().numpy() for n, t in layer.layout.tensors.items()}
+    for key in ("expert_counts", "expert_offsets", "rank_offsets", "row_token"):
+        assert np.array_equal(got[key][:len(ref[key])], ref[key]), key
+    assert np.array_equal(got["pair_row"].reshape(N, k), ref["pair_row"])
+    rng = np.random.default_rng(7)
+    if wl.dedup:
+        Rd = ref["n_dedup_rows"]
+        assert int(got["n_dedup_rows"][0]) == Rd
+        for key in ("dedup_counts", "dedup_offsets", "expand_src"):
+            assert np.array_equal(got[key][:len(ref[key])], ref[key]), key
+        assert np.array_equal(got["dedup_row_token"][:Rd], ref["dedup_row_token"])
+        assert np.array_equal(got["pair_dedup_row"].reshape(N, k), ref["pair_dedup_row"])
+        rows = rng.choice(Rd, size=min(512, Rd), replace=False)
+        xd = layer.xd[torch.from_numpy(rows).cuda()]
+        assert np.array_equal(host_u16(xd), x[ref["dedup_row_token"][rows]])
+        rows = rng.choice(N * k, size=512, replace=False)
+        xe = layer.xe[torch.from_numpy(rows).cuda()]
+        assert np.array_equal(host_u16(xe), x[ref["row_token"][rows]])
+    else:
+        rows = rng.choice(N * k, size=512, replace=False)
+        xd = layer.xd[torch.from_numpy(rows).cuda()]
+        assert np.array_equal(host_u16(xd), x[ref["row_token"][rows]])
+    # float outputs on sampled tokens (the first, the last and random ones)
+    n = SAMPLES[wl.name]
+    toks = np.unique(np.concatenate([[0, N - 1], rng.choice(N, size=n - 2, replace=False)]))
+    cache = {}
+
+    def weights_of(e):
+        if e not in cache:
+            cache.clear()
+            cache[e] = tuple(synth.make_weight(wl, m, experts=[e])[0] for m in ("gate", "up", "down"))
+        return cache[e]
+
+    want, y_want = oracle.token_outputs(x[toks], ref_ids[toks], ref_w[toks], weights_of, res[toks])
+    got_out = host_f64(out[torch.from_numpy(toks).cuda()])
+    assert_close(got_out, want, f"{name} out")
+    # the MoE delta alone: rerun without the residual (subtracting it from the
+    # bf16 total would measure the total's rounding against a smaller delta)
+    delta = layer.forward(torch.from_numpy(L).cuda(), bf16_host(x).cuda(), None)
+    torch.cuda.synchronize()
+    got_delta = host_f64(delta[torch.from_numpy(toks).cuda()])
+    assert_close(got_delta, want - oracle.widen_bf16(res[toks]), f"{name} MoE delta")
+    pr = ref["pair_row"][toks].reshape(-1)
+    y_got = host_f64(layer.y[torch.from_numpy(pr.astype(np.int64)).cuda()])
+    assert_close(y_got, y_want.reshape(-1, wl.H), f"{name} y rows")
+
+
+def test_device_weight_generator_matches_host():
+    """The device twin of the normal_bf16 stream gives the host generator's bits
+    (it may differ only where the two math libraries round a transcendental
+    differently right at a bf16 rounding boundary)."""
+    n = 1 << 22
+    for stream, offset in ((3, 0), (5, 123456789)):
+        d = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+        synth.normal_bf16_device(d, 0, stream, std=0.02, offset=offset)
+        h = synth.normal_bf16(0, stream, (n,), std=0.02, offset=offset)
+        mismatches = int(np.count_nonzero(host_u16(d) != h))
+        assert mismatches <= 4, mismatches
