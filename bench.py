@@ -44,6 +44,8 @@ def parse_args(argv=None):
     p.add_argument("--tokens", type=int, default=None, help="override N (profiling cases)")
     p.add_argument("--experts", type=int, default=None, help="override E (profiling cases)")
     p.add_argument("--dedup", choices=["auto", "on", "off"], default="auto")
+    p.add_argument("--placement-search", action="store_true",
+                   help="place experts by the co-selection search before timing the layer")
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -269,11 +271,13 @@ def dist_init(world, local):
 
 
 def max_over_ranks(value, world):
+    """Largest value over the ranks (the job's time is its slowest rank's)."""
     import torch
     import torch.distributed as dist
     if world == 1:
         return value
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -282,6 +286,52 @@ def barrier(world):
     import torch.distributed as dist
     if world > 1:
         dist.barrier()
+
+
+# ---------------------------------------------------------------------------- placement search
+
+def placement_search(wl, shape, logits_d, repeats=20):
+    """Correlated placement from this batch's routing: co-selection counts on
+    the GPU (timed with CUDA events), best-swap search on the host (timed by
+    wall clock), and the dedup rows under contiguous, planted and searched
+    placement."""
+    import torch
+
+    from combine_warp_top_gb300 import moe, synth
+    ids = torch.empty(wl.N * wl.k, dtype=torch.int32, device="cuda")
+    w = torch.empty(wl.N * wl.k, dtype=torch.float32, device="cuda")
+    moe.moe_route(logits_d, shape, ids, w)
+    ws = moe.workspace(shape)
+    W = torch.empty(wl.E, wl.E, dtype=torch.int32, device="cuda")
+    moe.moe_coselection(ids, shape, W, ws)  # warm-up
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(repeats):
+        moe.moe_coselection(ids, shape, W, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    cos_ms = e0.elapsed_time(e1) / repeats
+    W_h = W.cpu()
+    t0 = time.perf_counter()
+    placement, swaps = moe.moe_placement_search(W_h, wl.W)
+    search_ms = (time.perf_counter() - t0) * 1e3
+
+    def rows(pl):
+        dshape = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=True)
+        lay = moe.Layout(dshape)
+        moe.moe_dispatch_layout(ids, None if pl is None else pl.cuda(), dshape, lay, moe.workspace(dshape))
+        torch.cuda.synchronize()
+        return int(lay["n_dedup_rows"].item())
+
+    out = {"coselection_ms": round(cos_ms, 4),
+           "coselection_pairs_per_s": round(wl.N * wl.k * wl.k / cos_ms * 1e3, 1),
+           "search_ms": round(search_ms, 2), "swaps": swaps,
+           "dedup_rows_contiguous": rows(None), "dedup_rows_searched": rows(placement),
+           "placement": placement}
+    if wl.logits == "hot_pairs":
+        out["dedup_rows_planted"] = rows(torch.from_numpy(synth.make_placement(
+            synth.WORKLOADS["correlated_placed"])))
+    return out
 
 
 # ---------------------------------------------------------------------------- our arm
@@ -304,9 +354,13 @@ def run_ours(args):
     w_down = synth.make_weight_device(wl, "down")
     placement = synth.make_placement(wl)
     placement_d = None if wl.placement == "contiguous" else torch.from_numpy(placement).cuda()
+    L_h = torch.from_numpy(synth.make_logits(wl, seed)).pin_memory()
+    search = None
+    if args.placement_search:
+        search = placement_search(wl, shape, L_h.cuda())
+        placement_d = search.pop("placement").cuda()
     layer = moe.MoELayer(shape, w_gate, w_up, w_down, placement_d)
 
-    L_h = torch.from_numpy(synth.make_logits(wl, seed)).pin_memory()
     x_h = torch.from_numpy(synth.make_x(wl, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
     r_h = torch.from_numpy(synth.make_residual(wl, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
     out_h = torch.empty(wl.N, wl.H, dtype=torch.bfloat16).pin_memory()
@@ -435,6 +489,8 @@ def run_ours(args):
                           "dedup_reduction": round(1 - R_d / (wl.N * wl.k), 4),
                           "max_over_mean_expert_load": round(float(counts.max() / counts.mean()), 3)},
     }
+    if search is not None:
+        line["placement_search"] = search
     if not args.no_cpu_baseline and world == 1:
         cb = run_oracle(strip_args(sys.argv[1:]), args.cpu_seconds)["steps"][0]
         line["cpu_baseline"] = {

@@ -185,6 +185,27 @@ moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32
     return moe_combine(y, topk_w, layout, shape, partial, residual, out, stream);
 }
 
+moe_status moe_coselection(const int32_t* topk_ids, const moe_shape* shape, int32_t* coselect,
+                           void* ws, size_t ws_bytes, void* stream) {
+    MOE_TRY(check_shape(shape));
+    MOE_TRY(check_ws(shape, ws, ws_bytes));
+    if (!coselect || (shape->N > 0 && !topk_ids)) return MOE_ERR_INVALID_ARG;
+    int* err = ws_ptr<int>(ws, workspace_layout(*shape).err);
+    return cuda_status(
+        launch_coselection(topk_ids, *shape, coselect, err, as_stream(stream)));
+}
+
+moe_status moe_placement_search(const int32_t* coselect, int32_t E, int32_t ranks, int32_t nodes,
+                                int64_t max_swaps, int32_t* placement, int64_t* swaps_made) {
+    if (!coselect || !placement || E <= 0 || ranks <= 0 || nodes <= 0 || max_swaps < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (ranks % nodes != 0 || E % ranks != 0) return MOE_ERR_INVALID_ARG;
+    long long made = 0;
+    const moe_status st = placement_search(coselect, E, ranks, nodes, max_swaps, placement, &made);
+    if (swaps_made) *swaps_made = made;
+    return st;
+}
+
 moe_status moe_get_error(void* ws, void* stream) {
     if (!ws) return MOE_ERR_WORKSPACE;
     cudaStream_t st = as_stream(stream);

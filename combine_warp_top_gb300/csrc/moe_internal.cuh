@@ -79,6 +79,13 @@ moe_status launch_gate_up(const uint16_t* rows, const moe_layout& L, const moe_s
 moe_status launch_down(const uint16_t* h, const moe_layout& L, const moe_shape& s,
                        const uint16_t* wd, uint16_t* y, void* ws, cudaStream_t st);
 
+cudaError_t launch_coselection(const int32_t* ids, const moe_shape& s, int32_t* W, int* err,
+                               cudaStream_t st);
+
+// Host-only: balanced best-swap partition of Algorithm 1 (placement.cu).
+moe_status placement_search(const int32_t* W, int E, int ranks, int nodes, long long max_swaps,
+                            int32_t* placement, long long* swaps_made);
+
 int sm_count();
 
 }  // namespace moe

@@ -64,6 +64,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_layer_forward": (I32, [P, P, P, P, P, P, P, shp, P, P, lay, P, P, P, P, P, P, P, S,
                                     P]),
         "moe_dispatch_layout_noalloc": (I32, [P, P, shp, lay, P]),
+        "moe_coselection": (I32, [P, shp, P, P, S, P]),
+        "moe_placement_search": (I32, [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.c_int64, P, P]),
         "moe_get_error": (I32, [P, P]),
         "moe_status_str": (ctypes.c_char_p, [I32]),
     }
@@ -221,6 +224,26 @@ def moe_layer_forward(logits, x, placement, w_gate, w_up, w_down, residual, shap
         _ptr(residual), ctypes.byref(shape.c()), _ptr(topk_ids), _ptr(topk_w),
         ctypes.byref(layout.c), _ptr(xd), _ptr(xe), _ptr(h), _ptr(y), _ptr(partial), _ptr(out),
         _ptr(ws), ws.numel(), _stream(stream)), "moe_layer_forward")
+
+
+def moe_coselection(topk_ids, shape: Shape, coselect, ws, stream=None):
+    _check(load().moe_coselection(_ptr(topk_ids), ctypes.byref(shape.c()), _ptr(coselect),
+                                  _ptr(ws), ws.numel(), _stream(stream)), "moe_coselection")
+
+
+def moe_placement_search(coselect_host, ranks: int, nodes: int = 1, max_swaps: int = 1 << 20):
+    """Host call: coselect_host is a CPU int32 tensor [E, E]; returns
+    (placement int32 CPU tensor [E], number of swaps)."""
+    if coselect_host.is_cuda or coselect_host.dtype != torch.int32:
+        raise ValueError("coselect must be a CPU int32 tensor")
+    c = coselect_host.contiguous()
+    E = c.shape[0]
+    placement = torch.empty(E, dtype=torch.int32)
+    swaps = ctypes.c_int64(0)
+    _check(load().moe_placement_search(ctypes.c_void_p(c.data_ptr()), E, ranks, nodes, max_swaps,
+                                       ctypes.c_void_p(placement.data_ptr()), ctypes.byref(swaps)),
+           "moe_placement_search")
+    return placement, int(swaps.value)
 
 
 def moe_get_error(ws, stream=None) -> int:

@@ -184,6 +184,31 @@ moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32
                              uint16_t* y, uint16_t* partial, uint16_t* out, void* ws,
                              size_t ws_bytes, void* stream);
 
+/* Co-selection counts of "Expert Coupling" Sec. V-A / Appendix A-D Algorithm 1:
+ * coselect[e*E + e'] = number of tokens whose topk_ids contain both e and e'
+ * (symmetric; the diagonal counts the tokens that select e).  coselect is a
+ * device int32 [E, E], overwritten.  Integer counts: bit-exact and
+ * deterministic.  Ids out of range are reported in the workspace error word
+ * and counted as expert 0. */
+moe_status moe_coselection(const int32_t* topk_ids, const moe_shape* shape, int32_t* coselect,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* Correlated placement search ("Expert Coupling" Sec. V-A, Appendix A-D
+ * Algorithm 1), on the HOST: coselect is a host int32 [E, E] (as written by
+ * moe_coselection and copied back), placement a host int32 [E] output.  The
+ * experts are partitioned into `ranks` equal groups that keep frequently
+ * co-selected experts together: from contiguous groups, the swap of two
+ * experts of different groups with the largest gain in within-group
+ * co-selection is applied (ties: the pair (a, b), a < b, first in
+ * lexicographic order) until no swap gains or max_swaps swaps were made.
+ * With nodes > 1 the experts are first split across nodes, then each node's
+ * experts (ascending ids) across its ranks/nodes ranks.  Output: slot p holds
+ * expert placement[p]; rank r owns slots [r*E/ranks, (r+1)*E/ranks), its
+ * experts in ascending id order.  swaps_made (nullable) receives the number of
+ * swaps.  Requires nodes | ranks and ranks | E.  Synchronous. */
+moe_status moe_placement_search(const int32_t* coselect, int32_t E, int32_t ranks, int32_t nodes,
+                                int64_t max_swaps, int32_t* placement, int64_t* swaps_made);
+
 /* moe_dispatch_layout without a workspace argument, for callers that cannot
  * allocate device memory when they call the library (an inference runtime's
  * enqueue path that forbids allocation while it executes, a host whose device

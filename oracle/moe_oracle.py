@@ -329,3 +329,99 @@ def dense_forward(logits, x, wg, wu, wd, k, residual=None):
         _, ye = swiglu_mlp(X, widen_bf16(wg[e]), widen_bf16(wu[e]), widen_bf16(wd[e]))
         out += G[:, e:e + 1] * ye
     return out
+
+
+# ----------------------------------------------------------------------------- placement search
+
+def coselection(topk_ids, E):
+    """Co-selection counts of "Expert Coupling" Sec. V-A and Appendix A-D
+    (Algorithm 1): W[e, e'] = number of tokens whose selected set contains both
+    e and e'.  Symmetric; the diagonal W[e, e] counts the tokens that select e."""
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    W = np.zeros((E, E), dtype=np.int64)
+    for j in range(ids.shape[1]):
+        for j2 in range(ids.shape[1]):
+            np.add.at(W, (ids[:, j], ids[:, j2]), 1)
+    return W
+
+
+def swap_gain(W, group, a, b):
+    """Change of the within-group co-selection total when experts a and b
+    (in different groups) trade places."""
+    A, B = group[a], group[b]
+    in_A = (group == A)
+    in_B = (group == B)
+    in_A[a] = False
+    in_B[b] = False
+    return int(W[a, in_B].sum() + W[b, in_A].sum() - W[a, in_A].sum() - W[b, in_B].sum())
+
+
+def partition(W, G, max_swaps):
+    """Balanced partition ("Expert Coupling" Appendix A-D, procedure Partition):
+    start from G contiguous groups of E/G experts; repeatedly apply the swap of
+    two experts from different groups with the largest gain in within-group
+    co-selection, until no swap has a positive gain or max_swaps swaps were
+    made.  Reading of "the swap with the largest gain" when several tie: the
+    pair (a, b), a < b, that comes first in lexicographic order.
+    Returns (group of each expert, number of swaps made)."""
+    W = np.asarray(W, dtype=np.int64)
+    E = W.shape[0]
+    if E % G != 0:
+        raise ValueError("E must be a multiple of the number of groups")
+    group = np.arange(E) // (E // G)
+    swaps = 0
+    for _ in range(max_swaps):
+        best, pair = 0, None
+        for a in range(E):
+            for b in range(a + 1, E):
+                if group[a] == group[b]:
+                    continue
+                g = swap_gain(W, group, a, b)
+                if g > best:
+                    best, pair = g, (a, b)
+        if pair is None:
+            break
+        a, b = pair
+        group[a], group[b] = group[b], group[a]
+        swaps += 1
+    return group, swaps
+
+
+def correlated_placement(W, ranks, nodes=1, max_swaps=10_000):
+    """Algorithm 1 of "Expert Coupling": one node -> Partition(W, P); several
+    nodes -> Partition across nodes first, then each node's experts (in
+    ascending id order) across its P/N ranks; rank(e) = n * P/N + rho_n(e).
+    Returned as a placement permutation: slot p holds placement[p], ranks take
+    E/P consecutive slots, experts of a rank in ascending id order."""
+    W = np.asarray(W, dtype=np.int64)
+    E = W.shape[0]
+    if ranks % nodes != 0 or E % ranks != 0:
+        raise ValueError("need nodes | ranks | E")
+    rank = np.empty(E, dtype=np.int64)
+    swaps = 0
+    if nodes == 1:
+        rank, swaps = partition(W, ranks, max_swaps)
+    else:
+        node, s = partition(W, nodes, max_swaps)
+        swaps += s
+        per = ranks // nodes
+        for n in range(nodes):
+            members = np.nonzero(node == n)[0]
+            rho, s = partition(W[np.ix_(members, members)], per, max_swaps)
+            swaps += s
+            rank[members] = n * per + rho
+    placement = np.concatenate([np.nonzero(rank == r)[0] for r in range(ranks)])
+    return placement.astype(np.int32), swaps
+
+
+def within_rank_coselection(W, placement, ranks):
+    """Total co-selection of expert pairs that share a rank (the objective)."""
+    E = len(placement)
+    rank = np.empty(E, dtype=np.int64)
+    rank[np.asarray(placement)] = np.arange(E) // (E // ranks)
+    total = 0
+    for a in range(E):
+        for b in range(a + 1, E):
+            if rank[a] == rank[b]:
+                total += int(W[a, b])
+    return total

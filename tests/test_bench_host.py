@@ -1,0 +1,60 @@
+"""Host-side logic of bench.py: argument handling, algorithmic byte counts and
+the multi-rank timing reduction (world_size 2 over gloo on the CPU)."""
+import os
+import socket
+
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    bench.barrier(world)
+    got = bench.max_over_ranks(10.0 + rank, world)
+    q.put((rank, got))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_world2_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == {0: 11.0, 1: 11.0}
+
+
+def test_strip_args_keeps_the_workload():
+    argv = ["--impl", "reference", "--workload", "mixtral", "--steps", "5", "--tokens", "64",
+            "--no-cpu-baseline"]
+    assert bench.strip_args(argv) == ["--workload", "mixtral", "--tokens", "64"]
+
+
+def test_algorithmic_bytes_of_the_deepseek_layer():
+    args = bench.parse_args([])
+    wl = bench.workload(args)
+    alg = bench.algorithmic(wl, R_d=0)
+    # gate/up streams 2 * E * I * H bf16 weights plus its rows in and out
+    assert alg["gate_up"]["bytes"] == 2 * 256 * 2048 * 7168 * 2 + 32768 * 7168 * 2 + 32768 * 2048 * 2
+    assert alg["gate_up"]["flops"] == 4 * 32768 * 7168 * 2048
+    assert alg["dispatch"]["bytes"] == 4096 * 7168 * 2 * (1 + 8)
+
+
+def test_workload_overrides():
+    wl = bench.workload(bench.parse_args(["--tokens", "512", "--experts", "32"]))
+    assert (wl.N, wl.E, wl.W, wl.H) == (512, 32, 8, 7168)
