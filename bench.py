@@ -46,6 +46,8 @@ def parse_args(argv=None):
     p.add_argument("--dedup", choices=["auto", "on", "off"], default="auto")
     p.add_argument("--placement-search", action="store_true",
                    help="place experts by the co-selection search before timing the layer")
+    p.add_argument("--shared-expert", type=int, default=0, metavar="I_S",
+                   help="add a shared expert of SwiGLU width I_S to every step")
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -359,7 +361,13 @@ def run_ours(args):
     if args.placement_search:
         search = placement_search(wl, shape, L_h.cuda())
         placement_d = search.pop("placement").cuda()
-    layer = moe.MoELayer(shape, w_gate, w_up, w_down, placement_d)
+    shared = None
+    if args.shared_expert:
+        I_s = args.shared_expert
+        shared = tuple(synth.normal_bf16_device(
+            torch.empty(*shp, dtype=torch.bfloat16, device="cuda"), 0, stream_id, std=0.02)
+            for stream_id, shp in ((103, (I_s, wl.H)), (104, (I_s, wl.H)), (105, (wl.H, I_s))))
+    layer = moe.MoELayer(shape, w_gate, w_up, w_down, placement_d, shared=shared)
 
     x_h = torch.from_numpy(synth.make_x(wl, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
     r_h = torch.from_numpy(synth.make_residual(wl, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -383,7 +391,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     layer.check_device_errors()
 
-    stages = [s for s in moe.MoELayer.STAGES if s != "expand" or wl.dedup]
+    stages = [s for s in moe.MoELayer.STAGES
+              if (s != "expand" or wl.dedup) and (s != "shared" or shared is not None)]
     ev = [{s: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for s in stages} for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -429,6 +438,11 @@ def run_ours(args):
 
     pk, pk_src = peaks()
     alg = algorithmic(wl, R_d)
+    if shared is not None:
+        I_s = args.shared_expert
+        alg["shared"] = dict(bytes=3 * I_s * wl.H * 2 + 2 * wl.N * wl.H * 2 + 2 * wl.N * I_s * 2,
+                             flops=6 * wl.N * wl.H * I_s)
+        alg["combine"]["bytes"] += wl.N * wl.H * 2
     ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     stage_report = {}
     for s in stages:
@@ -475,6 +489,7 @@ def run_ours(args):
         "data": "synthetic (seeded SplitMix64/Box-Muller; random-init expert weights)",
         "config": {"workload": wl.name, "N": wl.N, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
                    "W": wl.W, "dedup": wl.dedup, "placement": wl.placement,
+                   "shared_expert_I": args.shared_expert or None,
                    "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU",
                    "l2": f"no flush: {3 * wl.E * wl.H * wl.I * 2 / 1e9:.2f} GB of expert weights "
                          "read per step, larger than the 129 MB L2"},

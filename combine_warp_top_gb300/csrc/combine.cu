@@ -10,9 +10,9 @@
 // owner); FarSkip-Collective Sec. 3 (the layer output is added into the
 // residual stream).
 //
-// One warp per output row.  Each lane owns 16-byte chunks (8 bf16) of the row;
-// the k source rows of a chunk are loaded together, then accumulated in fp32
-// in j order.
+// One warp per output row.  Each lane owns U 16-byte chunks (8 bf16 each) per
+// step along the row; the source rows of a chunk are loaded together, then
+// accumulated in fp32 in j order.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -110,25 +110,39 @@ __device__ __forceinline__ void zero(float (&acc)[U][8]) {
         for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
 }
 
-// out[c] = bf16(acc (+ residual[c])) for the U chunks of this lane.
+// out[c] = bf16(acc (+ shared[c]) (+ residual[c])) for the U chunks of this lane.
+// With several chunks per lane all their loads are issued before any add;
+// with one, the load-add-store chain per chunk measured faster.
 template <int U>
-__device__ __forceinline__ void finish(float (&acc)[U][8], const uint4* residual, uint4* out,
-                                       size_t row_base, int C, int c0) {
+__device__ __forceinline__ void finish(float (&acc)[U][8], const uint4* shared,
+                                       const uint4* residual, uint4* out, size_t row_base, int C,
+                                       int c0) {
     const int lane = threadIdx.x & 31;
-    uint4 r[U];
-    if (residual) {
+    if constexpr (U == 1) {
+        const int c = c0 + lane;
+        if (c < C) {
+            if (shared) add_bf16x8(acc[0], shared[row_base + c]);
+            if (residual) add_bf16x8(acc[0], residual[row_base + c]);
+            out[row_base + c] = pack_bf16x8(acc[0]);
+        }
+    } else {
+        uint4 r[U], sh[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int c = c0 + u * 32 + lane;
-            if (c < C) r[u] = residual[row_base + c];
+            if (c < C) {
+                if (shared) sh[u] = shared[row_base + c];
+                if (residual) r[u] = residual[row_base + c];
+            }
         }
-    }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int c = c0 + u * 32 + lane;
-        if (c < C) {
-            if (residual) add_bf16x8(acc[u], r[u]);
-            out[row_base + c] = pack_bf16x8(acc[u]);
+        for (int u = 0; u < U; ++u) {
+            const int c = c0 + u * 32 + lane;
+            if (c < C) {
+                if (shared) add_bf16x8(acc[u], sh[u]);
+                if (residual) add_bf16x8(acc[u], r[u]);
+                out[row_base + c] = pack_bf16x8(acc[u]);
+            }
         }
     }
 }
@@ -137,7 +151,7 @@ __device__ __forceinline__ void finish(float (&acc)[U][8], const uint4* residual
 template <int U>
 __global__ void __launch_bounds__(kThreads) combine_kernel(
     const uint4* __restrict__ y, const float* __restrict__ topk_w,
-    const int32_t* __restrict__ pair_row, int N, int C, int k, int R,
+    const int32_t* __restrict__ pair_row, int N, int C, int k, int R, const uint4* shared,
     const uint4* residual, uint4* out) {
     const int lane = threadIdx.x & 31;
     const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
@@ -149,7 +163,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
         float acc[U][8];
         zero(acc);
         gather_weighted<U>(acc, y, C, c0, all, my_row, my_w);
-        finish<U>(acc, residual, out, (size_t)t * C, C, c0);
+        finish<U>(acc, shared, residual, out, (size_t)t * C, C, c0);
     }
 }
 
@@ -174,7 +188,7 @@ __global__ void __launch_bounds__(kThreads) rank_reduce_kernel(
         float acc[U][8];
         zero(acc);
         gather_weighted<U>(acc, y, C, c0, srcs, my_row, my_w);
-        finish<U>(acc, nullptr, partial, (size_t)d * C, C, c0);
+        finish<U>(acc, nullptr, nullptr, partial, (size_t)d * C, C, c0);
     }
 }
 
@@ -183,7 +197,7 @@ __global__ void __launch_bounds__(kThreads) rank_reduce_kernel(
 template <int U>
 __global__ void __launch_bounds__(kThreads) owner_sum_kernel(
     const uint4* __restrict__ partial, const int32_t* __restrict__ pair_dedup_row, int N, int C,
-    int k, int Rd_bound, const uint4* residual, uint4* out) {
+    int k, int Rd_bound, const uint4* shared, const uint4* residual, uint4* out) {
     const int lane = threadIdx.x & 31;
     const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
     if (t >= N) return;
@@ -214,7 +228,7 @@ __global__ void __launch_bounds__(kThreads) owner_sum_kernel(
         float acc[U][8];
         zero(acc);
         gather_weighted<U>(acc, partial, C, c0, srcs, sorted_d, 1.0f);
-        finish<U>(acc, residual, out, (size_t)t * C, C, c0);
+        finish<U>(acc, shared, residual, out, (size_t)t * C, C, c0);
     }
 }
 
@@ -223,12 +237,13 @@ inline int warps_grid(long long n) { return (int)((n + kThreads / 32 - 1) / (kTh
 }  // namespace
 
 cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& L,
-                           const moe_shape& s, uint16_t* partial, const uint16_t* residual,
-                           uint16_t* out, cudaStream_t st) {
+                           const moe_shape& s, uint16_t* partial, const uint16_t* shared,
+                           const uint16_t* residual, uint16_t* out, cudaStream_t st) {
     if (s.N == 0) return cudaSuccess;
     const int C = s.H / 8;
     const int R = s.N * s.k;
     const uint4* res = reinterpret_cast<const uint4*>(residual);
+    const uint4* sh = reinterpret_cast<const uint4*>(shared);
     // chunks per lane per iteration: keep ~8 source loads in flight per lane
     const int kk = s.dedup ? (s.k < s.W ? s.k : s.W) : s.k;
     const int U = kk <= 2 ? 4 : (kk <= 4 ? 2 : 1);
@@ -236,11 +251,11 @@ cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& 
         const uint4* yy = reinterpret_cast<const uint4*>(y);
         uint4* o = reinterpret_cast<uint4*>(out);
         if (U == 4)
-            combine_kernel<4><<<warps_grid(s.N), kThreads, 0, st>>>(yy, w, L.pair_row, s.N, C, s.k, R, res, o);
+            combine_kernel<4><<<warps_grid(s.N), kThreads, 0, st>>>(yy, w, L.pair_row, s.N, C, s.k, R, sh, res, o);
         else if (U == 2)
-            combine_kernel<2><<<warps_grid(s.N), kThreads, 0, st>>>(yy, w, L.pair_row, s.N, C, s.k, R, res, o);
+            combine_kernel<2><<<warps_grid(s.N), kThreads, 0, st>>>(yy, w, L.pair_row, s.N, C, s.k, R, sh, res, o);
         else
-            combine_kernel<1><<<warps_grid(s.N), kThreads, 0, st>>>(yy, w, L.pair_row, s.N, C, s.k, R, res, o);
+            combine_kernel<1><<<warps_grid(s.N), kThreads, 0, st>>>(yy, w, L.pair_row, s.N, C, s.k, R, sh, res, o);
         return cudaGetLastError();
     }
     const int Rd_max = s.N * (s.k < s.W ? s.k : s.W);
@@ -264,11 +279,11 @@ cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& 
     uint4* o = reinterpret_cast<uint4*>(out);
     const uint4* cp = reinterpret_cast<const uint4*>(partial);
     if (U == 4)
-        owner_sum_kernel<4><<<warps_grid(s.N), kThreads, 0, st>>>(cp, L.pair_dedup_row, s.N, C, s.k, Rd_max, res, o);
+        owner_sum_kernel<4><<<warps_grid(s.N), kThreads, 0, st>>>(cp, L.pair_dedup_row, s.N, C, s.k, Rd_max, sh, res, o);
     else if (U == 2)
-        owner_sum_kernel<2><<<warps_grid(s.N), kThreads, 0, st>>>(cp, L.pair_dedup_row, s.N, C, s.k, Rd_max, res, o);
+        owner_sum_kernel<2><<<warps_grid(s.N), kThreads, 0, st>>>(cp, L.pair_dedup_row, s.N, C, s.k, Rd_max, sh, res, o);
     else
-        owner_sum_kernel<1><<<warps_grid(s.N), kThreads, 0, st>>>(cp, L.pair_dedup_row, s.N, C, s.k, Rd_max, res, o);
+        owner_sum_kernel<1><<<warps_grid(s.N), kThreads, 0, st>>>(cp, L.pair_dedup_row, s.N, C, s.k, Rd_max, sh, res, o);
     return cudaGetLastError();
 }
 

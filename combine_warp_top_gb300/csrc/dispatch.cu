@@ -8,9 +8,11 @@
 // kernel"; "Expert Coupling" Sec. V-A (one copy per unique (token, rank)) and
 // Appendix A-A2 (the receiver expands the rows into expert-major order).
 //
-// The copy is source-major: one warp reads its token's row once with 16-byte
-// loads and stores it to each destination, so x is read from HBM exactly once
-// whatever k is.  Rows are bit-exact copies.
+// The copy is source-major: a token's row is read once with 16-byte loads and
+// stored to each destination, so x is read from HBM exactly once whatever k
+// is.  One warp handles one slice of 32*kUnroll chunks of one row, so a long
+// row is spread over several warps that each make a single round trip.  Rows
+// are bit-exact copies.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -31,14 +33,18 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
     return v;
 }
 
-// dest_of_pair: pair_row (plain) or pair_dedup_row (dedup), [N*k].
+// dest_of_pair: pair_row (plain) or pair_dedup_row (dedup), [N*k].  Warp g
+// copies slice g % slices of token g / slices.
 __global__ void __launch_bounds__(kThreads) dispatch_kernel(const uint4* __restrict__ x, int N,
                                                             int C, int k,
                                                             const int32_t* __restrict__ dest_of_pair,
                                                             int dedup, int row_bound,
                                                             uint4* __restrict__ xd) {
     const int lane = threadIdx.x & 31;
-    const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    const long long g = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const int slices = (C + 32 * kUnroll - 1) / (32 * kUnroll);
+    const int t = (int)(g / slices);
+    const int cs = (int)(g % slices) * 32 * kUnroll;
     if (t >= N) return;
     int d = lane < k ? clamp_row(dest_of_pair[(size_t)t * k + lane], row_bound) : -1;
     bool keep = lane < k;
@@ -51,7 +57,8 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(const uint4* __restr
     }
     const uint32_t dests = __ballot_sync(0xffffffffu, keep);
     const uint4* src = x + (size_t)t * C;
-    for (int c0 = 0; c0 < C; c0 += 32 * kUnroll) {
+    {
+        const int c0 = cs;
         uint4 v[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
@@ -108,7 +115,8 @@ cudaError_t launch_dispatch(const uint16_t* x, const moe_layout& L, const moe_sh
     if (s.N == 0) return cudaSuccess;
     const int C = s.H / 8;
     const int rows = s.dedup ? s.N * (s.k < s.W ? s.k : s.W) : s.N * s.k;
-    dispatch_kernel<<<warps_grid(s.N), kThreads, 0, st>>>(
+    const long long slices = (C + 32 * kUnroll - 1) / (32 * kUnroll);
+    dispatch_kernel<<<warps_grid(s.N * slices), kThreads, 0, st>>>(
         reinterpret_cast<const uint4*>(x), s.N, C, s.k, s.dedup ? L.pair_dedup_row : L.pair_row,
         s.dedup, rows, reinterpret_cast<uint4*>(xd));
     return cudaGetLastError();

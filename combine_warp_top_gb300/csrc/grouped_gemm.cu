@@ -558,64 +558,63 @@ bool set_smem_attr() {
                                 (int)kSmemBytes) == cudaSuccess;
 }
 
-// Writes the m-block prefix of the tile schedule into the workspace and
-// returns the persistent grid size for a GEMM with `n_tiles_per_mblock`
-// n-blocks: never more CTAs than tiles, never more than one per SM.
-moe_status schedule(const moe_layout& L, const moe_shape& s, void* ws, cudaStream_t st,
-                    long long n_blocks, int32_t** prefix_out, int* grid) {
-    const Workspace wl = workspace_layout(s);
-    int32_t* prefix = ws_ptr<int32_t>(ws, wl.mblk_prefix);
-    schedule_kernel<<<1, 1024, 0, st>>>(L.expert_counts, s.E, prefix);
+// Writes the m-block prefix of the tile schedule and returns the persistent
+// grid size for a GEMM with `n_blocks` n-blocks: never more CTAs than tiles,
+// never more than one per SM.
+moe_status schedule(const GemmGroup& g, long long n_blocks, cudaStream_t st, int* grid) {
+    schedule_kernel<<<1, 1024, 0, st>>>(g.counts, g.E, g.prefix);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     // tiles <= n_blocks * (ceil(R / BM) + E): each expert adds at most one ragged m-block
-    const long long R = (long long)s.N * s.k;
-    const long long tiles = n_blocks * ((R + BM - 1) / BM + s.E);
+    const long long tiles = n_blocks * ((g.R + BM - 1) / BM + g.E);
     const int sms = sm_count();
     *grid = (int)(tiles < sms ? tiles : sms);
-    *prefix_out = prefix;
     return MOE_OK;
 }
 
 }  // namespace
 
-moe_status launch_gate_up(const uint16_t* rows, const moe_layout& L, const moe_shape& s,
-                          const uint16_t* wg, const uint16_t* wu, uint16_t* h, void* ws,
-                          cudaStream_t st) {
-    const int R = s.N * s.k;
-    if (R == 0) return MOE_OK;
+moe_status launch_gate_up(const uint16_t* rows, const GemmGroup& g, int H, int I,
+                          const uint16_t* wg, const uint16_t* wu, uint16_t* h, cudaStream_t st) {
+    if (g.R == 0) return MOE_OK;
     CUtensorMap a, bg, bu;
-    if (!map_2d(&a, rows, R, s.H, BM) || !map_3d(&bg, wg, s.E, s.I, s.H, kMmaN / 2) ||
-        !map_3d(&bu, wu, s.E, s.I, s.H, kMmaN / 2))
+    if (!map_2d(&a, rows, g.R, H, BM) || !map_3d(&bg, wg, g.E, I, H, kMmaN / 2) ||
+        !map_3d(&bu, wu, g.E, I, H, kMmaN / 2))
         return MOE_ERR_UNSUPPORTED;
     if (!set_smem_attr()) return MOE_ERR_CUDA;
-    int32_t* prefix;
     int grid;
-    const moe_status ss = schedule(L, s, ws, st, (s.I + kMmaN / 2 - 1) / (kMmaN / 2), &prefix, &grid);
+    const moe_status ss = schedule(g, (I + kMmaN / 2 - 1) / (kMmaN / 2), st, &grid);
     if (ss != MOE_OK) return ss;
-    int* err = ws_ptr<int>(ws, workspace_layout(s).err);
     grouped_gemm_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(
-        a, bg, bu, L.expert_offsets, L.expert_counts, prefix, s.E, s.H, s.I,
-        reinterpret_cast<__nv_bfloat16*>(h), err);
+        a, bg, bu, g.offsets, g.counts, g.prefix, g.E, H, I,
+        reinterpret_cast<__nv_bfloat16*>(h), g.err);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-moe_status launch_down(const uint16_t* h, const moe_layout& L, const moe_shape& s,
-                       const uint16_t* wd, uint16_t* y, void* ws, cudaStream_t st) {
-    const int R = s.N * s.k;
-    if (R == 0) return MOE_OK;
+moe_status launch_down(const uint16_t* h, const GemmGroup& g, int H, int I, const uint16_t* wd,
+                       uint16_t* y, cudaStream_t st) {
+    if (g.R == 0) return MOE_OK;
     CUtensorMap a, bd;
-    if (!map_2d(&a, h, R, s.I, BM) || !map_3d(&bd, wd, s.E, s.H, s.I, kMmaN))
+    if (!map_2d(&a, h, g.R, I, BM) || !map_3d(&bd, wd, g.E, H, I, kMmaN))
         return MOE_ERR_UNSUPPORTED;
     if (!set_smem_attr()) return MOE_ERR_CUDA;
-    int32_t* prefix;
     int grid;
-    const moe_status ss = schedule(L, s, ws, st, (s.H + kMmaN - 1) / kMmaN, &prefix, &grid);
+    const moe_status ss = schedule(g, (H + kMmaN - 1) / kMmaN, st, &grid);
     if (ss != MOE_OK) return ss;
-    int* err = ws_ptr<int>(ws, workspace_layout(s).err);
     grouped_gemm_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(
-        a, bd, bd, L.expert_offsets, L.expert_counts, prefix, s.E, s.I, s.H,
-        reinterpret_cast<__nv_bfloat16*>(y), err);
+        a, bd, bd, g.offsets, g.counts, g.prefix, g.E, I, H,
+        reinterpret_cast<__nv_bfloat16*>(y), g.err);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+__global__ void dense_group_kernel(int N, int32_t* counts, int32_t* offsets) {
+    counts[0] = N;
+    offsets[0] = 0;
+    offsets[1] = N;
+}
+
+cudaError_t launch_dense_group(int N, int32_t* counts, int32_t* offsets, cudaStream_t st) {
+    dense_group_kernel<<<1, 1, 0, st>>>(N, counts, offsets);
+    return cudaGetLastError();
 }
 
 }  // namespace moe

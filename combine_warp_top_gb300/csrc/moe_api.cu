@@ -50,6 +50,20 @@ moe_status check_ws(const moe_shape* s, void* ws, size_t ws_bytes) {
 
 inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// The routed experts' GEMM problem: the plain expert-major rows of the layout.
+GemmGroup routed_group(const moe_layout& L, const moe_shape& s, void* ws) {
+    const Workspace wl = workspace_layout(s);
+    return GemmGroup{L.expert_counts, L.expert_offsets, s.E, (long long)s.N * s.k,
+                     ws_ptr<int32_t>(ws, wl.mblk_prefix), ws_ptr<int>(ws, wl.err)};
+}
+
+// The shared expert's GEMM problem: all N token rows as one segment.
+GemmGroup dense_group(const moe_shape& s, void* ws) {
+    const Workspace wl = workspace_layout(s);
+    int32_t* d = ws_ptr<int32_t>(ws, wl.dense);
+    return GemmGroup{d, d + 1, 1, (long long)s.N, d + 4, ws_ptr<int>(ws, wl.err)};
+}
+
 inline cudaStream_t as_stream(void* p) { return reinterpret_cast<cudaStream_t>(p); }
 
 #define MOE_TRY(expr)                     \
@@ -75,8 +89,17 @@ moe_status moe_route(const float* logits, const moe_shape* shape, int32_t* topk_
     MOE_TRY(check_shape(shape));
     if (shape->N == 0) return MOE_OK;
     if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
-    return cuda_status(
-        launch_route(logits, shape->N, shape->E, shape->k, topk_ids, topk_w, as_stream(stream)));
+    return cuda_status(launch_route(logits, shape->N, shape->E, shape->k, topk_ids, topk_w, true,
+                                    as_stream(stream)));
+}
+
+moe_status moe_route_full_softmax(const float* logits, const moe_shape* shape, int32_t* topk_ids,
+                                  float* topk_w, void* stream) {
+    MOE_TRY(check_shape(shape));
+    if (shape->N == 0) return MOE_OK;
+    if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_route(logits, shape->N, shape->E, shape->k, topk_ids, topk_w, false,
+                                    as_stream(stream)));
 }
 
 moe_status moe_dispatch_layout(const int32_t* topk_ids, const int32_t* placement,
@@ -117,7 +140,8 @@ moe_status moe_ffn_gate_up(const uint16_t* rows, const moe_layout* layout, const
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (shape->N == 0) return MOE_OK;
     if (!rows || !w_gate || !w_up || !h) return MOE_ERR_INVALID_ARG;
-    return launch_gate_up(rows, *layout, *shape, w_gate, w_up, h, ws, as_stream(stream));
+    return launch_gate_up(rows, routed_group(*layout, *shape, ws), shape->H, shape->I, w_gate, w_up,
+                          h, as_stream(stream));
 }
 
 moe_status moe_ffn_down(const uint16_t* h, const moe_layout* layout, const moe_shape* shape,
@@ -128,7 +152,8 @@ moe_status moe_ffn_down(const uint16_t* h, const moe_layout* layout, const moe_s
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (shape->N == 0) return MOE_OK;
     if (!h || !w_down || !y) return MOE_ERR_INVALID_ARG;
-    return launch_down(h, *layout, *shape, w_down, y, ws, as_stream(stream));
+    return launch_down(h, routed_group(*layout, *shape, ws), shape->H, shape->I, w_down, y,
+                       as_stream(stream));
 }
 
 moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const moe_shape* shape,
@@ -158,8 +183,38 @@ moe_status moe_combine(const uint16_t* y, const float* topk_w, const moe_layout*
     if (shape->N == 0) return MOE_OK;
     if (!y || !topk_w || !out) return MOE_ERR_INVALID_ARG;
     if (shape->dedup && !partial) return MOE_ERR_INVALID_ARG;
-    return cuda_status(
-        launch_combine(y, topk_w, *layout, *shape, partial, residual, out, as_stream(stream)));
+    return cuda_status(launch_combine(y, topk_w, *layout, *shape, partial, nullptr, residual, out,
+                                      as_stream(stream)));
+}
+
+moe_status moe_shared_expert_ffn(const uint16_t* x, const moe_shape* shape, int32_t I_shared,
+                                 const uint16_t* w_gate_s, const uint16_t* w_up_s,
+                                 const uint16_t* w_down_s, uint16_t* h_s, uint16_t* y_s, void* ws,
+                                 size_t ws_bytes, void* stream) {
+    MOE_TRY(check_shape(shape));
+    MOE_TRY(check_ws(shape, ws, ws_bytes));
+    if (I_shared <= 0) return MOE_ERR_INVALID_ARG;
+    if (I_shared % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (shape->N == 0) return MOE_OK;
+    if (!x || !w_gate_s || !w_up_s || !w_down_s || !h_s || !y_s) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = as_stream(stream);
+    const GemmGroup g = dense_group(*shape, ws);
+    MOE_TRY(cuda_status(launch_dense_group(shape->N, const_cast<int32_t*>(g.counts),
+                                           const_cast<int32_t*>(g.offsets), st)));
+    MOE_TRY(launch_gate_up(x, g, shape->H, I_shared, w_gate_s, w_up_s, h_s, st));
+    return launch_down(h_s, g, shape->H, I_shared, w_down_s, y_s, st);
+}
+
+moe_status moe_combine_shared(const uint16_t* y, const float* topk_w, const moe_layout* layout,
+                              const moe_shape* shape, uint16_t* partial, const uint16_t* y_shared,
+                              const uint16_t* residual, uint16_t* out, void* stream) {
+    MOE_TRY(check_shape(shape));
+    MOE_TRY(check_layout(layout, shape));
+    if (shape->N == 0) return MOE_OK;
+    if (!y || !topk_w || !out || !y_shared) return MOE_ERR_INVALID_ARG;
+    if (shape->dedup && !partial) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_combine(y, topk_w, *layout, *shape, partial, y_shared, residual, out,
+                                      as_stream(stream)));
 }
 
 moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32_t* placement,

@@ -25,6 +25,7 @@ struct Workspace {
     size_t blk_rcounts;  // int32 [nblk][W]  per-block dedup counts by rank
     size_t slot_start;   // int32 [E+1]      first row of each slot
     size_t mblk_prefix;  // int32 [E+1]      GEMM m-blocks before expert e
+    size_t dense;        // int32 [8]        shared expert: count, offsets, schedule
     size_t total;
 };
 
@@ -41,6 +42,7 @@ inline Workspace workspace_layout(const moe_shape& s) {
     w.blk_rcounts = o; o = align256(o + nb * s.W * 4);
     w.slot_start = o;  o = align256(o + (size_t)(s.E + 1) * 4);
     w.mblk_prefix = o; o = align256(o + (size_t)(s.E + 1) * 4);
+    w.dense = o;       o = align256(o + 8 * 4);
     w.total = o;
     return w;
 }
@@ -55,8 +57,9 @@ __device__ __forceinline__ void set_error(int* err, int code) {
 
 // ---- kernel launchers (one per .cu file) -------------------------------------------
 
+// renorm: softmax over the selected k (true) or the full softmax over E (false).
 cudaError_t launch_route(const float* logits, int N, int E, int k, int32_t* ids, float* w,
-                         cudaStream_t st);
+                         bool renorm, cudaStream_t st);
 
 cudaError_t launch_layout(const int32_t* ids, const int32_t* placement, const moe_shape& s,
                           const moe_layout& L, void* ws, cudaStream_t st);
@@ -67,17 +70,31 @@ cudaError_t launch_dispatch(const uint16_t* x, const moe_layout& L, const moe_sh
 cudaError_t launch_expand(const uint16_t* xd, const moe_layout& L, const moe_shape& s,
                           uint16_t* xe, cudaStream_t st);
 
+// shared: nullable [N, H] rows added to every token's output (shared expert).
 cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& L,
-                           const moe_shape& s, uint16_t* partial, const uint16_t* residual,
-                           uint16_t* out, cudaStream_t st);
+                           const moe_shape& s, uint16_t* partial, const uint16_t* shared,
+                           const uint16_t* residual, uint16_t* out, cudaStream_t st);
+
+// One grouped GEMM problem: R rows in E expert segments (device arrays
+// counts[E], offsets[E] of the segments), plus device scratch for its tile
+// schedule (prefix[E+1]) and the error word.
+struct GemmGroup {
+    const int32_t* counts;
+    const int32_t* offsets;
+    int E;
+    long long R;
+    int32_t* prefix;
+    int* err;
+};
 
 // Return MOE_OK, or an error status when a host-side step (tensor-map
 // encoding, launch) failed.
-moe_status launch_gate_up(const uint16_t* rows, const moe_layout& L, const moe_shape& s,
-                          const uint16_t* wg, const uint16_t* wu, uint16_t* h, void* ws,
-                          cudaStream_t st);
-moe_status launch_down(const uint16_t* h, const moe_layout& L, const moe_shape& s,
-                       const uint16_t* wd, uint16_t* y, void* ws, cudaStream_t st);
+moe_status launch_gate_up(const uint16_t* rows, const GemmGroup& g, int H, int I,
+                          const uint16_t* wg, const uint16_t* wu, uint16_t* h, cudaStream_t st);
+moe_status launch_down(const uint16_t* h, const GemmGroup& g, int H, int I, const uint16_t* wd,
+                       uint16_t* y, cudaStream_t st);
+// counts = {N}, offsets = {0, N}: one dense segment of N rows.
+cudaError_t launch_dense_group(int N, int32_t* counts, int32_t* offsets, cudaStream_t st);
 
 cudaError_t launch_coselection(const int32_t* ids, const moe_shape& s, int32_t* W, int* err,
                                cudaStream_t st);

@@ -23,7 +23,9 @@ __device__ __forceinline__ bool beats(float av, int ai, float bv, int bi) {
     return av > bv || (av == bv && ai < bi);
 }
 
-template <int VPL>
+// kRenorm: weights are a softmax over the k selected logits; otherwise the
+// full softmax over all E logits, read at the selected experts.
+template <int VPL, bool kRenorm>
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int N, int E,
                                                     int k, int32_t* __restrict__ ids,
                                                     float* __restrict__ w) {
@@ -76,10 +78,16 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
         }
     }
 
-    // softmax over the selected k; the first pick holds the maximum
+    // softmax; the first pick holds the maximum of all E logits
     const float m = __shfl_sync(0xffffffffu, my_val, 0);
     const float z = lane < k ? expf(my_val - m) : 0.f;
     float s = z;
+    if (!kRenorm) {
+        s = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i)
+            if (i * 32 + lane < E) s += expf(v[i] - m);
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (lane < k) {
@@ -89,25 +97,29 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
 }
 
 template <int VPL>
-cudaError_t go(const float* logits, int N, int E, int k, int32_t* ids, float* w, cudaStream_t st) {
+cudaError_t go(const float* logits, int N, int E, int k, int32_t* ids, float* w, bool renorm,
+               cudaStream_t st) {
     const int threads = 256;
     const int tokens_per_block = threads / 32;
     const int blocks = (N + tokens_per_block - 1) / tokens_per_block;
-    route_kernel<VPL><<<blocks, threads, 0, st>>>(logits, N, E, k, ids, w);
+    if (renorm)
+        route_kernel<VPL, true><<<blocks, threads, 0, st>>>(logits, N, E, k, ids, w);
+    else
+        route_kernel<VPL, false><<<blocks, threads, 0, st>>>(logits, N, E, k, ids, w);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_route(const float* logits, int N, int E, int k, int32_t* ids, float* w,
-                         cudaStream_t st) {
+                         bool renorm, cudaStream_t st) {
     if (N == 0) return cudaSuccess;
-    if (E <= 32) return go<1>(logits, N, E, k, ids, w, st);
-    if (E <= 64) return go<2>(logits, N, E, k, ids, w, st);
-    if (E <= 128) return go<4>(logits, N, E, k, ids, w, st);
-    if (E <= 256) return go<8>(logits, N, E, k, ids, w, st);
-    if (E <= 512) return go<16>(logits, N, E, k, ids, w, st);
-    return go<32>(logits, N, E, k, ids, w, st);
+    if (E <= 32) return go<1>(logits, N, E, k, ids, w, renorm, st);
+    if (E <= 64) return go<2>(logits, N, E, k, ids, w, renorm, st);
+    if (E <= 128) return go<4>(logits, N, E, k, ids, w, renorm, st);
+    if (E <= 256) return go<8>(logits, N, E, k, ids, w, renorm, st);
+    if (E <= 512) return go<16>(logits, N, E, k, ids, w, renorm, st);
+    return go<32>(logits, N, E, k, ids, w, renorm, st);
 }
 
 }  // namespace moe

@@ -54,6 +54,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     sigs = {
         "moe_workspace_bytes": (S, [shp]),
         "moe_route": (I32, [P, shp, P, P, P]),
+        "moe_route_full_softmax": (I32, [P, shp, P, P, P]),
         "moe_dispatch_layout": (I32, [P, P, shp, lay, P, S, P]),
         "moe_dispatch": (I32, [P, lay, shp, P, P]),
         "moe_expert_ffn": (I32, [P, lay, shp, P, P, P, P, P, P, P, S, P]),
@@ -65,6 +66,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                     P]),
         "moe_dispatch_layout_noalloc": (I32, [P, P, shp, lay, P]),
         "moe_coselection": (I32, [P, shp, P, P, S, P]),
+        "moe_shared_expert_ffn": (I32, [P, shp, ctypes.c_int32, P, P, P, P, P, P, S, P]),
+        "moe_combine_shared": (I32, [P, P, lay, shp, P, P, P, P, P]),
         "moe_placement_search": (I32, [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_int64, P, P]),
         "moe_get_error": (I32, [P, P]),
@@ -169,6 +172,11 @@ def moe_route(logits, shape: Shape, topk_ids, topk_w, stream=None):
                             _stream(stream)), "moe_route")
 
 
+def moe_route_full_softmax(logits, shape: Shape, topk_ids, topk_w, stream=None):
+    _check(load().moe_route_full_softmax(_ptr(logits), ctypes.byref(shape.c()), _ptr(topk_ids),
+                                         _ptr(topk_w), _stream(stream)), "moe_route_full_softmax")
+
+
 def moe_dispatch_layout(topk_ids, placement, shape: Shape, layout: Layout, ws, stream=None):
     _check(load().moe_dispatch_layout(_ptr(topk_ids), _ptr(placement), ctypes.byref(shape.c()),
                                       ctypes.byref(layout.c), _ptr(ws), ws.numel(),
@@ -226,6 +234,21 @@ def moe_layer_forward(logits, x, placement, w_gate, w_up, w_down, residual, shap
         _ptr(ws), ws.numel(), _stream(stream)), "moe_layer_forward")
 
 
+def moe_shared_expert_ffn(x, shape: Shape, I_shared: int, w_gate_s, w_up_s, w_down_s, h_s, y_s, ws,
+                          stream=None):
+    _check(load().moe_shared_expert_ffn(_ptr(x), ctypes.byref(shape.c()), I_shared, _ptr(w_gate_s),
+                                        _ptr(w_up_s), _ptr(w_down_s), _ptr(h_s), _ptr(y_s), _ptr(ws),
+                                        ws.numel(), _stream(stream)), "moe_shared_expert_ffn")
+
+
+def moe_combine_shared(y, topk_w, layout: Layout, shape: Shape, partial, y_shared, residual, out,
+                       stream=None):
+    _check(load().moe_combine_shared(_ptr(y), _ptr(topk_w), ctypes.byref(layout.c),
+                                     ctypes.byref(shape.c()), _ptr(partial), _ptr(y_shared),
+                                     _ptr(residual), _ptr(out), _stream(stream)),
+           "moe_combine_shared")
+
+
 def moe_coselection(topk_ids, shape: Shape, coselect, ws, stream=None):
     _check(load().moe_coselection(_ptr(topk_ids), ctypes.byref(shape.c()), _ptr(coselect),
                                   _ptr(ws), ws.numel(), _stream(stream)), "moe_coselection")
@@ -261,10 +284,19 @@ class MoELayer:
     runs moe_layer_forward on them.  Weights are bf16 tensors [E, I, H] (gate,
     up) and [E, H, I] (down); placement int32 [E] or None."""
 
-    def __init__(self, shape: Shape, w_gate, w_up, w_down, placement=None, device="cuda"):
+    def __init__(self, shape: Shape, w_gate, w_up, w_down, placement=None, device="cuda",
+                 shared=None):
+        """shared: optional (w_gate_s [I_s, H], w_up_s [I_s, H], w_down_s [H, I_s])
+        of a shared expert run on every token."""
         self.shape = shape
         self.w_gate, self.w_up, self.w_down = w_gate, w_up, w_down
         self.placement = placement
+        self.shared = shared
+        if shared is not None:
+            I_s = shared[0].shape[0]
+            self.I_shared = I_s
+            self.h_s = torch.empty(max(shape.N, 1), I_s, dtype=torch.bfloat16, device=device)
+            self.y_s = torch.empty(max(shape.N, 1), shape.H, dtype=torch.bfloat16, device=device)
         N, H, I, k = shape.N, shape.H, shape.I, shape.k
         bf = dict(dtype=torch.bfloat16, device=device)
         self.topk_ids = torch.empty(max(N * k, 1), dtype=torch.int32, device=device)
@@ -281,12 +313,14 @@ class MoELayer:
 
     def forward(self, logits, x, residual=None, out=None, stream=None):
         out = self.out if out is None else out
+        if self.shared is not None:
+            return self.forward_stages(logits, x, residual, out, stream)
         moe_layer_forward(logits, x, self.placement, self.w_gate, self.w_up, self.w_down,
                           residual, self.shape, self.topk_ids, self.topk_w, self.layout,
                           self.xd, self.xe, self.h, self.y, self.partial, out, self.ws, stream)
         return out
 
-    STAGES = ("route", "layout", "dispatch", "expand", "gate_up", "down", "combine")
+    STAGES = ("route", "layout", "dispatch", "expand", "gate_up", "down", "shared", "combine")
 
     def forward_stages(self, logits, x, residual=None, out=None, stream=None, events=None):
         """The same kernels as forward(), one C call per stage of the pages'
@@ -321,8 +355,16 @@ class MoELayer:
         rec("down", 0)
         moe_ffn_down(self.h, self.layout, s, self.w_down, self.y, self.ws, st)
         rec("down", 1)
+        if self.shared is not None:
+            rec("shared", 0)
+            moe_shared_expert_ffn(x, s, self.I_shared, *self.shared, self.h_s, self.y_s, self.ws, st)
+            rec("shared", 1)
         rec("combine", 0)
-        moe_combine(self.y, self.topk_w, self.layout, s, self.partial, residual, out, st)
+        if self.shared is not None:
+            moe_combine_shared(self.y, self.topk_w, self.layout, s, self.partial, self.y_s,
+                               residual, out, st)
+        else:
+            moe_combine(self.y, self.topk_w, self.layout, s, self.partial, residual, out, st)
         rec("combine", 1)
         return out
 
@@ -333,7 +375,8 @@ class MoELayer:
         s = self.shape
         if s.N == 0:
             return 0
-        return 1 + 3 + 1 + (1 if s.dedup else 0) + 2 + 2 + (2 if s.dedup else 1)
+        shared = 5 if self.shared is not None else 0  # dense segment + 2 x (schedule + GEMM)
+        return 1 + 3 + 1 + (1 if s.dedup else 0) + 2 + 2 + (2 if s.dedup else 1) + shared
 
     def forward_host(self, logits_h, x_h, residual_h, out_h, dev_inputs=None, stream=None):
         """Whole layer from host buffers: copy the step's inputs host->device,

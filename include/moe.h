@@ -103,6 +103,14 @@ size_t moe_workspace_bytes(const moe_shape* shape);
 moe_status moe_route(const float* logits, const moe_shape* shape, int32_t* topk_ids,
                      float* topk_w, void* stream);
 
+/* Router variant with the literal reading of "Expert Coupling" Appendix A-A1,
+ * Table II ("softmax over all E, then top-k; gate weights = selected softmax
+ * probabilities"): the same topk_ids as moe_route, and
+ * topk_w[t, j] = exp(L_j - L_max) / sum over all E of exp(L_e - L_max),
+ * which do not sum to one. */
+moe_status moe_route_full_softmax(const float* logits, const moe_shape* shape, int32_t* topk_ids,
+                                  float* topk_w, void* stream);
+
 /* Dispatch layout (kernel-fusion page, "Expert parallelism: dispatch and
  * combine" and "Fusing the layer into one kernel" stage 3 "group"; "Expert
  * Coupling" Sec. V-A and Appendix A-A2).  Stable counting sort of the (t, j)
@@ -172,6 +180,29 @@ moe_status moe_ffn_down(const uint16_t* h, const moe_layout* layout, const moe_s
 moe_status moe_combine(const uint16_t* y, const float* topk_w, const moe_layout* layout,
                        const moe_shape* shape, uint16_t* partial, const uint16_t* residual,
                        uint16_t* out, void* stream);
+
+/* Shared expert (FarSkip-Collective Sec. 2.1: "shared-experts" MLP layers run
+ * on all tokens in addition to the routed experts): one dense SwiGLU MLP over
+ * every token row of x, on the same tensor-core kernels as the routed
+ * experts, reading x directly (no dispatch):
+ *   h_s = bf16(SiLU(x Wg_s^T) * (x Wu_s^T))   bf16 [N, I_shared]
+ *   y_s = bf16(h_s Wd_s^T)                    bf16 [N, H]
+ * w_gate_s, w_up_s bf16 [I_shared, H]; w_down_s bf16 [H, I_shared];
+ * I_shared % 8 == 0.  ws: the layer's workspace (a reserved corner holds this
+ * call's schedule). */
+moe_status moe_shared_expert_ffn(const uint16_t* x, const moe_shape* shape, int32_t I_shared,
+                                 const uint16_t* w_gate_s, const uint16_t* w_up_s,
+                                 const uint16_t* w_down_s, uint16_t* h_s, uint16_t* y_s, void* ws,
+                                 size_t ws_bytes, void* stream);
+
+/* moe_combine plus the shared expert's output:
+ *   out[t, :] = bf16( sum_j topk_w[t, j] * y[pair_row[t, j], :]   (j order; dedup:
+ *                     the owner's sum of partials, ascending rank)
+ *                     + y_shared[t, :] + residual[t, :] )          fp32 sums
+ * y_shared bf16 [N, H] (required); residual nullable; out may equal residual. */
+moe_status moe_combine_shared(const uint16_t* y, const float* topk_w, const moe_layout* layout,
+                              const moe_shape* shape, uint16_t* partial, const uint16_t* y_shared,
+                              const uint16_t* residual, uint16_t* out, void* stream);
 
 /* The whole layer in order on one stream: moe_route, moe_dispatch_layout,
  * moe_dispatch, moe_expert_ffn, moe_combine, with the buffers documented for

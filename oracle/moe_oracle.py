@@ -72,13 +72,16 @@ def rank_of_expert(placement, E, W):
 
 # ----------------------------------------------------------------------------- route
 
-def route(logits, k):
+def route(logits, k, renormalize=True):
     """Top-k routing over fp32 logits.
 
     For every token t the pairs (-L[t,e], e) are sorted lexicographically and
     the first k kept: the k largest logits, in descending order, ties to the
     lower expert index.  The weights are a softmax over the k kept logits,
     w_j = exp(L_j - L_max) / sum_j' exp(L_j' - L_max), here in float64.
+    renormalize=False keeps instead the full-softmax probabilities of the kept
+    experts ("Expert Coupling" Table II read literally): the denominator sums
+    over all E logits.
 
     Returns topk_ids int32 [N, k] and topk_w float64 [N, k].
     """
@@ -93,7 +96,11 @@ def route(logits, k):
     ids = order[:, :k]
     sel = np.take_along_axis(L, ids, axis=1).astype(np.float64)
     z = np.exp(sel - sel.max(axis=1, keepdims=True))
-    w = z / z.sum(axis=1, keepdims=True)
+    if renormalize:
+        w = z / z.sum(axis=1, keepdims=True)
+    else:
+        Lf = L.astype(np.float64)
+        w = z / np.exp(Lf - sel.max(axis=1, keepdims=True)).sum(axis=1, keepdims=True)
     return ids.astype(np.int32), w
 
 
@@ -267,8 +274,18 @@ def combine_dedup(y, topk_w, pair_row, pair_dedup_row, n_dedup_rows, residual=No
 
 # ----------------------------------------------------------------------------- whole layer
 
-def layer_forward(logits, x, wg, wu, wd, k, W, placement=None, residual=None, dedup=False):
-    """The whole forward pass: route -> layout -> dispatch -> FFN -> combine."""
+def shared_expert(x, shared):
+    """Shared expert (FarSkip-Collective Sec. 2.1: an MLP run on every token in
+    addition to the routed experts): the SwiGLU MLP of (wg_s, wu_s, wd_s),
+    bf16 weights [I_s, H], [I_s, H], [H, I_s], over all rows of x."""
+    wg_s, wu_s, wd_s = shared
+    return swiglu_mlp(widen_bf16(x), widen_bf16(wg_s), widen_bf16(wu_s), widen_bf16(wd_s))
+
+
+def layer_forward(logits, x, wg, wu, wd, k, W, placement=None, residual=None, dedup=False,
+                  shared=None):
+    """The whole forward pass: route -> layout -> dispatch -> FFN -> combine,
+    plus, if given, the shared expert's output added to every token."""
     N, E = np.shape(logits)
     placement = np.arange(E) if placement is None else placement
     ids, w = route(logits, k)
@@ -285,8 +302,12 @@ def layer_forward(logits, x, wg, wu, wd, k, W, placement=None, residual=None, de
                                      lay["n_dedup_rows"], residual)
     else:
         partial, out = None, combine(y, w, lay["pair_row"], residual)
+    h_s = y_s = None
+    if shared is not None:
+        h_s, y_s = shared_expert(x, shared)
+        out = out + y_s
     return dict(topk_ids=ids, topk_w=w, layout=lay, xd=xe, xd_dedup=xd_dedup, h=h, y=y,
-                partial=partial, out=out)
+                partial=partial, out=out, h_shared=h_s, y_shared=y_s)
 
 
 def token_outputs(x_rows, ids_rows, w_rows, expert_weights, residual_rows=None):

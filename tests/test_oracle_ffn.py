@@ -116,3 +116,26 @@ def test_expert_with_no_rows_and_ragged_segments():
     dense = oracle.dense_forward(L, x, wg, wu, wd, 1, residual=res)
     np.testing.assert_allclose(r["out"], dense, rtol=1e-12, atol=1e-12)
     assert (r["layout"]["expert_counts"] == 0).any()
+
+
+def check_shared_expert_is_added_to_every_token(layer_fn):
+    """With the routed down projections zeroed, the layer is residual + the
+    shared SwiGLU MLP, written here with torch's F.linear / F.silu."""
+    L, x, wg, wu, wd, res, wl = make_case(N=20, H=24, E=4, k=2, I=16, W=2, seed=9)
+    ws_ = synth.Workload("s", 20, 24, 1, 1, 40, 1)
+    shared = tuple(synth.make_weight(ws_, m, seed=9)[0] for m in ("gate", "up", "down"))
+    got = layer_fn(L, x, wg, wu, np.zeros_like(wd), 2, 2, residual=res, shared=shared)["out"]
+    X = torch.from_numpy(oracle.widen_bf16(x))
+    g = F.linear(X, torch.from_numpy(oracle.widen_bf16(shared[0])))
+    u = F.linear(X, torch.from_numpy(oracle.widen_bf16(shared[1])))
+    y = F.linear(F.silu(g) * u, torch.from_numpy(oracle.widen_bf16(shared[2])))
+    want = torch.from_numpy(oracle.widen_bf16(res)) + y
+    np.testing.assert_allclose(got, want.numpy(), rtol=1e-12, atol=1e-12)
+    # and with routed experts: shared part and routed part add
+    both = layer_fn(L, x, wg, wu, wd, 2, 2, residual=res, shared=shared)["out"]
+    routed = layer_fn(L, x, wg, wu, wd, 2, 2, residual=res)["out"]
+    np.testing.assert_allclose(both - routed, y.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_shared_expert_pin():
+    check_shared_expert_is_added_to_every_token(oracle.layer_forward)

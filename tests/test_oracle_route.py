@@ -138,3 +138,21 @@ def test_route_rejects_bad_arguments():
         oracle.route(np.zeros((2, 4), np.float32), 5)
     with pytest.raises(ValueError):
         oracle.route(np.array([[np.nan, 1.0]], np.float32), 1)
+
+
+def test_full_softmax_variant():
+    """renormalize=False: the same experts, weighted by their probability under
+    the softmax over all E (closed form for E = 2, k = 1: 1 / (1 + e^{L_2 - L_1}))."""
+    L = synth.normal_f32(0, 14, (300, 2))
+    ids, w = oracle.route(L, 1, renormalize=False)
+    Lsel = np.take_along_axis(L, ids.astype(np.int64), 1)[:, 0].astype(np.float64)
+    Loth = np.take_along_axis(L, 1 - ids.astype(np.int64), 1)[:, 0].astype(np.float64)
+    np.testing.assert_allclose(w[:, 0], 1.0 / (1.0 + np.exp(Loth - Lsel)), atol=1e-12)
+    L = synth.normal_f32(0, 15, (200, 16))
+    ids_r, w_r = oracle.route(L, 4)
+    ids_f, w_f = oracle.route(L, 4, renormalize=False)
+    assert np.array_equal(ids_r, ids_f)
+    assert np.all(w_f.sum(1) < 1.0)
+    np.testing.assert_allclose(w_f / w_f.sum(1, keepdims=True), w_r, rtol=1e-12)
+    ids_all, w_all = oracle.route(L, 16, renormalize=False)
+    np.testing.assert_allclose(w_all.sum(1), 1.0, atol=1e-12)  # k = E: all probabilities
