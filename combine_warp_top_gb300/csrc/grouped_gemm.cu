@@ -15,7 +15,9 @@
 // ring (128B swizzle), warp 1 owns TMEM and issues tcgen05.mma from one thread
 // (fp32 accumulators, two 256-column buffers so the epilogue of one tile
 // overlaps the main loop of the next), warps 2-5 read the accumulators back
-// with tcgen05.ld and write the outputs.  Tiles of an expert never cross into
+// with tcgen05.ld, stage 64 output columns of their 32 rows in shared memory
+// and write them out with a TMA store (or masked row-line stores at the ragged
+// end of an expert's segment).  Tiles of an expert never cross into
 // the next expert's rows on store: rows past the segment end are masked, so
 // no padding of the expert-major layout is needed.  Every wait is bounded; a
 // wait that runs out of time records MOE_ERR_TIMEOUT, the CTA drains what it
@@ -54,7 +56,17 @@ struct Ctl {
     int cnts[kMaxE];
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * STAGE_BYTES + sizeof(Ctl);
+// Epilogue staging: each epilogue warp writes its 32 rows x 64 output columns
+// (bf16, 4 KB) into shared memory in the 128-byte swizzled layout of a TMA
+// box; a slice whose 32 rows all belong to the tile's expert leaves by one
+// asynchronous TMA tensor store, a ragged slice at the end of an expert's
+// segment by masked 16-byte stores of whole row lines.
+constexpr int kStageCols = 64;
+constexpr int kStageWarpBytes = 32 * kStageCols * 2;  // 4 KB, 1024-byte aligned
+constexpr size_t kCtlBytes = (sizeof(Ctl) + 15) & ~size_t(15);
+
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * STAGE_BYTES +
+                              (size_t)kEpilogueWarps * kStageWarpBytes + kCtlBytes;
 
 // ---- PTX wrappers -------------------------------------------------------------------
 
@@ -128,6 +140,30 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
+}
+
+// TMA tensor store of a 2-D box from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until every committed bulk store has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until every committed bulk store has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Order this thread's generic-proxy shared-memory writes before async-proxy reads.
+__device__ __forceinline__ void fence_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
@@ -247,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmB1,
+                        const __grid_constant__ CUtensorMap tmOut,
                         const int32_t* __restrict__ expert_offsets,
                         const int32_t* __restrict__ expert_counts,
                         const int32_t* __restrict__ mblk_prefix, int E, int K, int n_out,
@@ -255,7 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* tiles = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     const uint32_t tiles_addr = smem_u32(tiles);
-    Ctl* ctl = reinterpret_cast<Ctl*>(tiles + (size_t)kStages * STAGE_BYTES);
+    uint8_t* stage_area = tiles + (size_t)kStages * STAGE_BYTES;  // 1024-byte aligned
+    Ctl* ctl = reinterpret_cast<Ctl*>(stage_area + (size_t)kEpilogueWarps * kStageWarpBytes);
     volatile int* abort_flag = &ctl->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -285,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_map(&tmA);
         prefetch_map(&tmB0);
         if (kSwiGLU) prefetch_map(&tmB1);
+        prefetch_map(&tmOut);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
@@ -385,17 +424,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_bar_drain(smem_u32(&ctl->done), 0);
         }
     } else {
-        // ---------------- epilogue: TMEM -> registers -> global ----------------
+        // ---------------- epilogue: TMEM -> registers -> smem -> global ----------------
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
-        const int r_in_tile = q * 32 + lane;
+        uint8_t* stage = stage_area + (size_t)(warp - 2) * kStageWarpBytes;
+        const uint32_t stage_addr = smem_u32(stage);
+        // lane r's row; 16-byte chunk j of it sits at chunk (j ^ (r & 7)) (128B swizzle)
+        uint8_t* my_row = stage + lane * 128;
+        const int sw = lane & 7;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             int e, mb, nb;
             decode_tile(ctl->prefix, E, NB, tile, e, mb, nb);
-            const int seg_end = ctl->offs[e] + ctl->cnts[e];
-            const int row = ctl->offs[e] + mb * BM + r_in_tile;
-            const bool row_ok = row < seg_end;
+            const int row_base = ctl->offs[e] + mb * BM + q * 32;  // this warp's first row
+            int rows_valid = ctl->offs[e] + ctl->cnts[e] - row_base;
+            rows_valid = rows_valid < 0 ? 0 : (rows_valid > 32 ? 32 : rows_valid);
             const int n0 = nb * BNo;
             int ready = 0;
             if (lane == 0) ready = wait_bar(smem_u32(&ctl->tfull[acc]), acc_phase, abort_flag, err);
@@ -403,56 +446,65 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ready) break;
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kMmaN);
-            __nv_bfloat16* orow = out + (size_t)(row_ok ? row : 0) * n_out;
-            if (kSwiGLU) {
 #pragma unroll 1
-                for (int c = 0; c < BNo / 32; ++c) {
+            for (int c = 0; c < BNo / kStageCols; ++c) {
+                // the staging tile is free once the previous TMA store has read it
+                if (lane == 0) bulk_wait_read();
+                __syncwarp();
+                // 1) this lane's row: 64 bf16 values into its staged row
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const uint32_t col_t = (uint32_t)(c * kStageCols + half * 32);
                     uint32_t g[32], u[32];
-                    tmem_ld32(tbase + c * 32, g);
-                    tmem_ld32(tbase + BNo + c * 32, u);
+                    tmem_ld32(tbase + col_t, g);
+                    if (kSwiGLU) tmem_ld32(tbase + BNo + col_t, u);
                     tmem_wait_ld();
-                    if (row_ok) {
 #pragma unroll
-                        for (int grp = 0; grp < 4; ++grp) {
-                            const int col = n0 + c * 32 + grp * 8;
-                            if (col < n_out) {
-                                uint4 o;
-                                uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+                    for (int grp = 0; grp < 4; ++grp) {
+                        uint4 o;
+                        uint32_t* op = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const int j = grp * 8 + 2 * i;
-                                    const float h0 = silu(__uint_as_float(g[j])) * __uint_as_float(u[j]);
-                                    const float h1 =
-                                        silu(__uint_as_float(g[j + 1])) * __uint_as_float(u[j + 1]);
-                                    op[i] = pack2(h0, h1);
-                                }
-                                *reinterpret_cast<uint4*>(orow + col) = o;
+                        for (int i = 0; i < 4; ++i) {
+                            const int j = grp * 8 + 2 * i;
+                            if (kSwiGLU) {
+                                const float h0 = silu(__uint_as_float(g[j])) * __uint_as_float(u[j]);
+                                const float h1 =
+                                    silu(__uint_as_float(g[j + 1])) * __uint_as_float(u[j + 1]);
+                                op[i] = pack2(h0, h1);
+                            } else {
+                                op[i] = pack2(__uint_as_float(g[j]), __uint_as_float(g[j + 1]));
                             }
                         }
+                        const int chunk = half * 4 + grp;
+                        *reinterpret_cast<uint4*>(my_row + ((chunk ^ sw) << 4)) = o;
                     }
                 }
-            } else {
-#pragma unroll 1
-                for (int c = 0; c < BNo / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(tbase + c * 32, v);
-                    tmem_wait_ld();
-                    if (row_ok) {
+                const int col0 = n0 + c * kStageCols;
+                if (rows_valid == 32) {
+                    // 2a) whole slice inside the expert: one TMA store (columns past
+                    // n_out are clipped by the tensor map)
+                    fence_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmOut, stage_addr, col0, row_base);
+                        bulk_commit();
+                    }
+                } else {
+                    // 2b) ragged slice: whole row lines, masked; pass i stores rows 4i..4i+3
+                    __syncwarp();
+                    const int qq = lane & 7;
+                    const int col = col0 + qq * 8;
 #pragma unroll
-                        for (int grp = 0; grp < 4; ++grp) {
-                            const int col = n0 + c * 32 + grp * 8;
-                            if (col < n_out) {
-                                uint4 o;
-                                uint32_t* op = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const int j = grp * 8 + 2 * i;
-                                    op[i] = pack2(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
-                                }
-                                *reinterpret_cast<uint4*>(orow + col) = o;
-                            }
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = i * 4 + (lane >> 3);
+                        if (rr < rows_valid && col < n_out) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(
+                                stage + rr * 128 + ((qq ^ (rr & 7)) << 4));
+                            *reinterpret_cast<uint4*>(out + (size_t)(row_base + rr) * n_out + col) =
+                                v;
                         }
                     }
+                    __syncwarp();
                 }
             }
             tc_fence_before();
@@ -463,6 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc_phase ^= 1u;
             }
         }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -576,16 +630,16 @@ moe_status schedule(const GemmGroup& g, long long n_blocks, cudaStream_t st, int
 moe_status launch_gate_up(const uint16_t* rows, const GemmGroup& g, int H, int I,
                           const uint16_t* wg, const uint16_t* wu, uint16_t* h, cudaStream_t st) {
     if (g.R == 0) return MOE_OK;
-    CUtensorMap a, bg, bu;
+    CUtensorMap a, bg, bu, o;
     if (!map_2d(&a, rows, g.R, H, BM) || !map_3d(&bg, wg, g.E, I, H, kMmaN / 2) ||
-        !map_3d(&bu, wu, g.E, I, H, kMmaN / 2))
+        !map_3d(&bu, wu, g.E, I, H, kMmaN / 2) || !map_2d(&o, h, g.R, I, 32))
         return MOE_ERR_UNSUPPORTED;
     if (!set_smem_attr()) return MOE_ERR_CUDA;
     int grid;
     const moe_status ss = schedule(g, (I + kMmaN / 2 - 1) / (kMmaN / 2), st, &grid);
     if (ss != MOE_OK) return ss;
     grouped_gemm_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(
-        a, bg, bu, g.offsets, g.counts, g.prefix, g.E, H, I,
+        a, bg, bu, o, g.offsets, g.counts, g.prefix, g.E, H, I,
         reinterpret_cast<__nv_bfloat16*>(h), g.err);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -593,15 +647,16 @@ moe_status launch_gate_up(const uint16_t* rows, const GemmGroup& g, int H, int I
 moe_status launch_down(const uint16_t* h, const GemmGroup& g, int H, int I, const uint16_t* wd,
                        uint16_t* y, cudaStream_t st) {
     if (g.R == 0) return MOE_OK;
-    CUtensorMap a, bd;
-    if (!map_2d(&a, h, g.R, I, BM) || !map_3d(&bd, wd, g.E, H, I, kMmaN))
+    CUtensorMap a, bd, o;
+    if (!map_2d(&a, h, g.R, I, BM) || !map_3d(&bd, wd, g.E, H, I, kMmaN) ||
+        !map_2d(&o, y, g.R, H, 32))
         return MOE_ERR_UNSUPPORTED;
     if (!set_smem_attr()) return MOE_ERR_CUDA;
     int grid;
     const moe_status ss = schedule(g, (H + kMmaN - 1) / kMmaN, st, &grid);
     if (ss != MOE_OK) return ss;
     grouped_gemm_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(
-        a, bd, bd, g.offsets, g.counts, g.prefix, g.E, I, H,
+        a, bd, bd, o, g.offsets, g.counts, g.prefix, g.E, I, H,
         reinterpret_cast<__nv_bfloat16*>(y), g.err);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
