@@ -48,6 +48,8 @@ def parse_args(argv=None):
                    help="place experts by the co-selection search before timing the layer")
     p.add_argument("--shared-expert", type=int, default=0, metavar="I_S",
                    help="add a shared expert of SwiGLU width I_S to every step")
+    p.add_argument("--microbatch", type=int, default=0, metavar="T",
+                   help="run the step as a two-stream pipeline of T-token microbatches")
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -386,15 +388,28 @@ def run_ours(args):
     del dlay, dws
 
     stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
-        layer.forward_stages(L_d, x_d, r_d)
-    torch.cuda.synchronize()
-    layer.check_device_errors()
+    pipe = None
+    if args.microbatch:
+        pipe = moe.MicrobatchPipeline(shape, w_gate, w_up, w_down, placement_d,
+                                      microbatch=args.microbatch, shared=shared)
+    runner = pipe if pipe is not None else layer
+    n_mb = len(pipe.chunks()) if pipe is not None else 0
+
+    def step(i):
+        if pipe is None:
+            layer.forward_stages(L_d, x_d, r_d, events=ev[i])
+        else:
+            pipe.forward(L_d, x_d, r_d, out=layer.out, gemm_events=gev[i])
 
     stages = [s for s in moe.MoELayer.STAGES
               if (s != "expand" or wl.dedup) and (s != "shared" or shared is not None)]
-    ev = [{s: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for s in stages} for _ in range(args.steps)]
+    mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))  # noqa: E731
+    ev = [{s: mk() for s in stages} for _ in range(args.steps)] if pipe is None else None
+    gev = [[mk() for _ in range(n_mb)] for _ in range(args.steps)] if pipe is not None else None
+    for i in range(args.warmup):
+        step(i % args.steps)
+    torch.cuda.synchronize()
+    runner.check_device_errors()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
@@ -405,7 +420,7 @@ def run_ours(args):
         sampler.mark("t0")
     t_start.record(stream)
     for i in range(args.steps):
-        layer.forward_stages(L_d, x_d, r_d, events=ev[i])
+        step(i)
     t_end.record(stream)
     torch.cuda.synchronize()
     if sampler:
@@ -413,25 +428,30 @@ def run_ours(args):
     barrier(world)
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
     clocks = sampler.stop() if sampler else None
-    layer.check_device_errors()
-    stage_ms = {s: statistics.mean(e[s][0].elapsed_time(e[s][1]) for e in ev) for s in stages}
+    runner.check_device_errors()
+    if pipe is None:
+        stage_ms = {s: statistics.mean(e[s][0].elapsed_time(e[s][1]) for e in ev) for s in stages}
+    else:
+        # gate/up launches of all microbatches of a step, on the GEMM stream
+        stage_ms = {"gate_up": statistics.mean(sum(a.elapsed_time(b) for a, b in g) for g in gev)}
+        stages = ["gate_up"]
 
     # end to end through the public host-buffer API: every step copies its
     # inputs from pinned host memory and its output back, overlapped with the
     # neighbouring steps' compute (moe.HostPipeline)
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 50))
-    pipe = moe.HostPipeline(layer, with_residual=True)
+    host = moe.HostPipeline(runner, with_residual=True)
     batches = [(L_h, x_h, r_h, out_h)] * e2e_steps
-    pipe.run(batches[:2])
+    host.run(batches[:2])
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    pipe.run(batches)
+    host.run(batches)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    layer.check_device_errors()
+    runner.check_device_errors()
 
     if rank != 0:
         return None
@@ -467,7 +487,8 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 3)
     roof["traffic"] = recorded_traffic(wl)
-    roof["kernel"] = "grouped_gemm_kernel<SwiGLU> (moe_ffn_gate_up)"
+    roof["kernel"] = "grouped_gemm_kernel<SwiGLU> (moe_ffn_gate_up)" + (
+        f", summed over the {n_mb} microbatches of a step" if pipe is not None else "")
     roof["peak_source"] = f"{pk_src} ({'bf16_tflops_sustained' if roof['unit'] == 'TFLOP/s' else 'hbm_gbs'})"
     roof["algorithmic_per_launch"] = {"bytes": a["bytes"], "flops": a["flops"]}
 
@@ -490,6 +511,7 @@ def run_ours(args):
         "config": {"workload": wl.name, "N": wl.N, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
                    "W": wl.W, "dedup": wl.dedup, "placement": wl.placement,
                    "shared_expert_I": args.shared_expert or None,
+                   "microbatch": args.microbatch or None,
                    "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU",
                    "l2": f"no flush: {3 * wl.E * wl.H * wl.I * 2 / 1e9:.2f} GB of expert weights "
                          "read per step, larger than the 129 MB L2"},
@@ -497,7 +519,7 @@ def run_ours(args):
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": wl.N * wl.E * 4 + 2 * wl.N * wl.H * 2,
                 "d2h_bytes_per_step": wl.N * wl.H * 2},
-        "gpu_launches": layer.kernel_launches_per_step() * args.steps,
+        "gpu_launches": runner.kernel_launches_per_step() * args.steps,
         "clocks": clocks,
         "stages": stage_report,
         "dispatch_rows": {"plain": wl.N * wl.k, "dedup": R_d,

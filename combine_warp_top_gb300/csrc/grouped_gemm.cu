@@ -661,6 +661,36 @@ moe_status launch_down(const uint16_t* h, const GemmGroup& g, int H, int I, cons
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Self-test of the bounded wait: one warp waits on an mbarrier whose phase
+// nothing completes, with the limit given in SM clock cycles.  The wait must
+// give up, record MOE_ERR_TIMEOUT and let the kernel return.
+__global__ void wait_selftest_kernel(long long limit_cycles, int* err) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(smem_u32(&bar), 0)) {
+            if (clock64() - t0 > limit_cycles) {
+                abort_flag = 1;
+                set_error(err, MOE_ERR_TIMEOUT);
+                break;
+            }
+        }
+    }
+    __syncthreads();
+}
+
+cudaError_t launch_wait_selftest(long long limit_cycles, int* err, cudaStream_t st) {
+    wait_selftest_kernel<<<1, 32, 0, st>>>(limit_cycles, err);
+    return cudaGetLastError();
+}
+
 __global__ void dense_group_kernel(int N, int32_t* counts, int32_t* offsets) {
     counts[0] = N;
     offsets[0] = 0;

@@ -261,6 +261,12 @@ moe_status moe_placement_search(const int32_t* coselect, int32_t E, int32_t rank
     return st;
 }
 
+moe_status moe_selftest_wait_timeout(void* ws, int64_t limit_cycles, void* stream) {
+    if (!ws) return MOE_ERR_WORKSPACE;
+    if (limit_cycles <= 0 || limit_cycles > (int64_t)1 << 32) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_wait_selftest(limit_cycles, ws_ptr<int>(ws, 0), as_stream(stream)));
+}
+
 moe_status moe_get_error(void* ws, void* stream) {
     if (!ws) return MOE_ERR_WORKSPACE;
     cudaStream_t st = as_stream(stream);

@@ -93,6 +93,8 @@ moe_status launch_gate_up(const uint16_t* rows, const GemmGroup& g, int H, int I
                           const uint16_t* wg, const uint16_t* wu, uint16_t* h, cudaStream_t st);
 moe_status launch_down(const uint16_t* h, const GemmGroup& g, int H, int I, const uint16_t* wd,
                        uint16_t* y, cudaStream_t st);
+// One warp waits on an mbarrier that never completes, up to limit_cycles.
+cudaError_t launch_wait_selftest(long long limit_cycles, int* err, cudaStream_t st);
 // counts = {N}, offsets = {0, N}: one dense segment of N rows.
 cudaError_t launch_dense_group(int N, int32_t* counts, int32_t* offsets, cudaStream_t st);
 

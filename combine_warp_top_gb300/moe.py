@@ -70,6 +70,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_combine_shared": (I32, [P, P, lay, shp, P, P, P, P, P]),
         "moe_placement_search": (I32, [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_int64, P, P]),
+        "moe_selftest_wait_timeout": (I32, [P, ctypes.c_int64, P]),
         "moe_get_error": (I32, [P, P]),
         "moe_status_str": (ctypes.c_char_p, [I32]),
     }
@@ -269,6 +270,11 @@ def moe_placement_search(coselect_host, ranks: int, nodes: int = 1, max_swaps: i
     return placement, int(swaps.value)
 
 
+def moe_selftest_wait_timeout(ws, limit_cycles: int, stream=None):
+    _check(load().moe_selftest_wait_timeout(_ptr(ws), limit_cycles, _stream(stream)),
+           "moe_selftest_wait_timeout")
+
+
 def moe_get_error(ws, stream=None) -> int:
     return int(load().moe_get_error(_ptr(ws), _stream(stream)))
 
@@ -455,3 +461,109 @@ class HostPipeline:
                 out_h.copy_(buf["out"], non_blocking=True)
                 self.saved[b].record(self.d2h)
         comp.wait_stream(self.d2h)
+
+
+class MicrobatchPipeline:
+    """The layer over microbatches of `microbatch` tokens, with the vector-unit
+    stages of one microbatch overlapping the tensor-core stages of another
+    ("Kernel fusion for expert parallelism", section "Pipelining and three-way
+    overlap": while the matrix units multiply microbatch m, the vector units
+    route, dispatch and combine its neighbours; buffers are alive per pipeline
+    slot, not per microbatch).
+
+    Two streams: `vec` runs route, layout, dispatch, expansion and combine;
+    `mat` runs the gate/up and down GEMMs (and the shared expert).  Microbatch
+    m uses buffer set m % depth.  Enqueue order on `vec` is A0, A1, C0, A2, C1,
+    ... so a set is overwritten only after its previous microbatch's combine
+    (which itself waited for that microbatch's GEMMs).  The GEMM CTAs fill the
+    SMs' shared memory but leave threads and registers free, so the copy-stage
+    blocks run on the same SMs at the same time.  Every token's output is
+    computed exactly as by MoELayer.forward (same kernels, same summation
+    order), so the results are bit-identical."""
+
+    def __init__(self, shape: Shape, w_gate, w_up, w_down, placement=None, microbatch=2048,
+                 depth=2, shared=None, device="cuda"):
+        if depth < 2:
+            raise ValueError("the two-stream schedule needs at least two buffer sets")
+        self.shape = shape
+        self.mb = max(1, min(microbatch, shape.N))
+        self.depth = depth
+        self.placement = placement
+        self.w = (w_gate, w_up, w_down)
+        self.shared = shared
+        sub = Shape(self.mb, shape.H, shape.E, shape.k, shape.W, shape.I, shape.dedup)
+        self.sets = [MoELayer(sub, w_gate, w_up, w_down, placement, device, shared)
+                     for _ in range(depth)]
+        self.vec = torch.cuda.Stream(device=device)
+        self.mat = torch.cuda.Stream(device=device)
+        self.gemm_events = None  # optional [(start, end)] per microbatch, on `mat`
+
+    def chunks(self):
+        N = self.shape.N
+        return [(t0, min(t0 + self.mb, N)) for t0 in range(0, N, self.mb)]
+
+    def forward(self, logits, x, residual=None, out=None, stream=None, gemm_events=None):
+        s = self.shape
+        comp = torch.cuda.current_stream() if stream is None else stream
+        out = out if out is not None else torch.empty(s.N, s.H, dtype=torch.bfloat16,
+                                                      device=x.device)
+        vec, mat = self.vec, self.mat
+        vec.wait_stream(comp)
+        mat.wait_stream(comp)
+        chunks = self.chunks()
+        a_done = [torch.cuda.Event() for _ in chunks]
+        b_done = [torch.cuda.Event() for _ in chunks]
+
+        def sub_shape(t0, t1):
+            return Shape(t1 - t0, s.H, s.E, s.k, s.W, s.I, s.dedup)
+
+        def combine(m):
+            t0, t1 = chunks[m]
+            L = self.sets[m % self.depth]
+            sm = sub_shape(t0, t1)
+            res = None if residual is None else residual[t0:t1]
+            vec.wait_event(b_done[m])
+            if self.shared is not None:
+                moe_combine_shared(L.y, L.topk_w, L.layout, sm, L.partial, L.y_s, res,
+                                   out[t0:t1], vec)
+            else:
+                moe_combine(L.y, L.topk_w, L.layout, sm, L.partial, res, out[t0:t1], vec)
+
+        for m, (t0, t1) in enumerate(chunks):
+            L = self.sets[m % self.depth]
+            sm = sub_shape(t0, t1)
+            # vector-unit stages of microbatch m
+            moe_route(logits[t0:t1], sm, L.topk_ids, L.topk_w, vec)
+            moe_dispatch_layout(L.topk_ids, self.placement, sm, L.layout, L.ws, vec)
+            moe_dispatch(x[t0:t1], L.layout, sm, L.xd, vec)
+            rows = L.xd
+            if s.dedup:
+                moe_expand(L.xd, L.layout, sm, L.xe, vec)
+                rows = L.xe
+            a_done[m].record(vec)
+            # tensor-core stages of microbatch m
+            mat.wait_event(a_done[m])
+            if gemm_events is not None:
+                gemm_events[m][0].record(mat)
+            moe_ffn_gate_up(rows, L.layout, sm, self.w[0], self.w[1], L.h, L.ws, mat)
+            if gemm_events is not None:
+                gemm_events[m][1].record(mat)
+            moe_ffn_down(L.h, L.layout, sm, self.w[2], L.y, L.ws, mat)
+            if self.shared is not None:
+                moe_shared_expert_ffn(x[t0:t1], sm, L.I_shared, *self.shared, L.h_s, L.y_s,
+                                      L.ws, mat)
+            b_done[m].record(mat)
+            # combine of the previous microbatch while this one multiplies
+            if m >= 1:
+                combine(m - 1)
+        combine(len(chunks) - 1)
+        comp.wait_stream(vec)
+        comp.wait_stream(mat)
+        return out
+
+    def check_device_errors(self):
+        for L in self.sets:
+            L.check_device_errors()
+
+    def kernel_launches_per_step(self) -> int:
+        return sum(self.sets[0].kernel_launches_per_step() for _ in self.chunks())

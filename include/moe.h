@@ -255,6 +255,14 @@ moe_status moe_dispatch_layout_noalloc(const int32_t* topk_ids, const int32_t* p
                                        const moe_shape* shape, const moe_layout* layout,
                                        void* stream);
 
+/* Self-test of the device-side wait limit that guards every wait of the
+ * kernels (no counterpart in the pages: it checks the library's own failure
+ * reporting).  Launches one warp that waits on an mbarrier that nothing
+ * completes; after limit_cycles SM clock cycles (1 .. 2^32) the wait gives
+ * up, MOE_ERR_TIMEOUT is recorded in the workspace error word (read it with
+ * moe_get_error) and the kernel returns, leaving the context usable. */
+moe_status moe_selftest_wait_timeout(void* ws, int64_t limit_cycles, void* stream);
+
 /* Synchronizes `stream`, reads the workspace error word, clears it, and
  * returns it (MOE_OK if no device-side problem was recorded). */
 moe_status moe_get_error(void* ws, void* stream);

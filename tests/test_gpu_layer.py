@@ -149,3 +149,22 @@ def test_host_pipeline_matches_device_forward():
     torch.cuda.synchronize()
     for (_, _, _, out), w in zip(batches, want):
         assert torch.equal(out.view(torch.int16), w.view(torch.int16))
+
+
+def test_wait_timeout_is_reported_and_the_context_survives():
+    """A device-side wait on a barrier that nothing completes gives up after its
+    limit (about 1 ms of SM clock here), records MOE_ERR_TIMEOUT, and the next
+    layer call runs normally."""
+    wl = SMALL["tiny"]
+    layer, _ = build_layer(wl, False)
+    moe.moe_selftest_wait_timeout(layer.ws, 2_000_000)
+    assert moe.moe_get_error(layer.ws) == 5  # MOE_ERR_TIMEOUT
+    assert moe.moe_get_error(layer.ws) == 0
+    L = torch.from_numpy(synth.make_logits(wl)).cuda()
+    x, res = dev_bf16(synth.make_x(wl)), dev_bf16(synth.make_residual(wl))
+    a = layer.forward(L, x, res).clone()
+    torch.cuda.synchronize()
+    layer.check_device_errors()
+    b = layer.forward(L, x, res)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
