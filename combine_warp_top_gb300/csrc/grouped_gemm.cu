@@ -166,6 +166,16 @@ __device__ __forceinline__ void fence_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Four rows (r0..r3) x 64 columns of a 2-D map whose box is one row high.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int r0, int r1, int r2, int r3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -278,7 +288,9 @@ __device__ __forceinline__ void decode_tile(const int* prefix, int E, int NB, in
     mb = local - nb * MB;
 }
 
-template <bool kSwiGLU>
+// kGatherA: A row i of the problem is row a_rows[i] of the map's tensor
+// (gathered by the producer warp with tile::gather4); otherwise row i itself.
+template <bool kSwiGLU, bool kGatherA>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB0,
@@ -287,7 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int32_t* __restrict__ expert_offsets,
                         const int32_t* __restrict__ expert_counts,
                         const int32_t* __restrict__ mblk_prefix, int E, int K, int n_out,
-                        __nv_bfloat16* __restrict__ out, int* err) {
+                        __nv_bfloat16* __restrict__ out, int* err,
+                        const int32_t* __restrict__ a_rows, int a_total, int a_src_rows) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* tiles = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -337,7 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
-        if (lane == 0) {
+        // Plain rows: lane 0 issues everything.  Gathered rows: every lane
+        // issues one 4-row gather of A per stage; lane 0 arms the barrier and
+        // loads B.
+        if (kGatherA || lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
@@ -347,23 +363,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 decode_tile(ctl->prefix, E, NB, tile, e, mb, nb);
                 const int row0 = ctl->offs[e] + mb * BM;
                 const int n0 = nb * BNo;
+                int gi[4] = {0, 0, 0, 0};
+                if (kGatherA) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int r = row0 + lane * 4 + q;  // rows past the data read row 0
+                        int v = r < a_total ? a_rows[r] : 0;
+                        gi[q] = (unsigned)v < (unsigned)a_src_rows ? v : 0;
+                    }
+                }
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!wait_bar(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag, err)) {
+                    int go = 1;
+                    if (lane == 0)
+                        go = wait_bar(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag, err);
+                    if (kGatherA) go = __shfl_sync(0xffffffffu, go, 0);
+                    if (!go) {
                         ok = false;
                         break;
                     }
                     const uint32_t full = smem_u32(&ctl->full[stage]);
                     const uint32_t a_s = tiles_addr + stage * STAGE_BYTES;
                     const uint32_t b_s = a_s + A_BYTES;
-                    mbar_expect_tx(full, STAGE_BYTES);
-                    armed |= 1u << stage;
-                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-                    tma_load_2d(a_s, &tmA, full, kb * BK, row0);
-                    if (kSwiGLU) {
-                        tma_load_3d(b_s, &tmB0, full, kb * BK, n0, e);
-                        tma_load_3d(b_s + B_BYTES / 2, &tmB1, full, kb * BK, n0, e);
+                    if (lane == 0) {
+                        mbar_expect_tx(full, STAGE_BYTES);
+                        armed |= 1u << stage;
+                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                        if (kSwiGLU) {
+                            tma_load_3d(b_s, &tmB0, full, kb * BK, n0, e);
+                            tma_load_3d(b_s + B_BYTES / 2, &tmB1, full, kb * BK, n0, e);
+                        } else {
+                            tma_load_3d(b_s, &tmB0, full, kb * BK, n0, e);
+                        }
+                    }
+                    if (kGatherA) {
+                        __syncwarp();
+                        tma_gather4(a_s + lane * 4 * 128, &tmA, full, kb * BK, gi[0], gi[1], gi[2],
+                                    gi[3]);
                     } else {
-                        tma_load_3d(b_s, &tmB0, full, kb * BK, n0, e);
+                        tma_load_2d(a_s, &tmA, full, kb * BK, row0);
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -371,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (*abort_flag) {
+            if (lane == 0 && *abort_flag) {
                 // let every copy still in flight land before the CTA exits
                 for (int s = 0; s < kStages; ++s)
                     if ((armed >> s) & 1u)
@@ -604,10 +641,13 @@ bool map_3d(CUtensorMap* m, const void* ptr, uint64_t E, uint64_t rows, uint64_t
 namespace {
 
 bool set_smem_attr() {
-    return cudaFuncSetAttribute(grouped_gemm_kernel<true>,
+    return cudaFuncSetAttribute(grouped_gemm_kernel<true, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kSmemBytes) == cudaSuccess &&
-           cudaFuncSetAttribute(grouped_gemm_kernel<false>,
+           cudaFuncSetAttribute(grouped_gemm_kernel<true, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kSmemBytes) == cudaSuccess &&
+           cudaFuncSetAttribute(grouped_gemm_kernel<false, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kSmemBytes) == cudaSuccess;
 }
@@ -628,19 +668,26 @@ moe_status schedule(const GemmGroup& g, long long n_blocks, cudaStream_t st, int
 }  // namespace
 
 moe_status launch_gate_up(const uint16_t* rows, const GemmGroup& g, int H, int I,
-                          const uint16_t* wg, const uint16_t* wu, uint16_t* h, cudaStream_t st) {
+                          const uint16_t* wg, const uint16_t* wu, uint16_t* h, cudaStream_t st,
+                          const int32_t* gather, long long src_rows) {
     if (g.R == 0) return MOE_OK;
     CUtensorMap a, bg, bu, o;
-    if (!map_2d(&a, rows, g.R, H, BM) || !map_3d(&bg, wg, g.E, I, H, kMmaN / 2) ||
+    const bool ok_a = gather ? map_2d(&a, rows, src_rows, H, 1) : map_2d(&a, rows, g.R, H, BM);
+    if (!ok_a || !map_3d(&bg, wg, g.E, I, H, kMmaN / 2) ||
         !map_3d(&bu, wu, g.E, I, H, kMmaN / 2) || !map_2d(&o, h, g.R, I, 32))
         return MOE_ERR_UNSUPPORTED;
     if (!set_smem_attr()) return MOE_ERR_CUDA;
     int grid;
     const moe_status ss = schedule(g, (I + kMmaN / 2 - 1) / (kMmaN / 2), st, &grid);
     if (ss != MOE_OK) return ss;
-    grouped_gemm_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(
-        a, bg, bu, o, g.offsets, g.counts, g.prefix, g.E, H, I,
-        reinterpret_cast<__nv_bfloat16*>(h), g.err);
+    if (gather)
+        grouped_gemm_kernel<true, true><<<grid, kThreads, kSmemBytes, st>>>(
+            a, bg, bu, o, g.offsets, g.counts, g.prefix, g.E, H, I,
+            reinterpret_cast<__nv_bfloat16*>(h), g.err, gather, (int)g.R, (int)src_rows);
+    else
+        grouped_gemm_kernel<true, false><<<grid, kThreads, kSmemBytes, st>>>(
+            a, bg, bu, o, g.offsets, g.counts, g.prefix, g.E, H, I,
+            reinterpret_cast<__nv_bfloat16*>(h), g.err, nullptr, 0, 0);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -655,9 +702,9 @@ moe_status launch_down(const uint16_t* h, const GemmGroup& g, int H, int I, cons
     int grid;
     const moe_status ss = schedule(g, (H + kMmaN - 1) / kMmaN, st, &grid);
     if (ss != MOE_OK) return ss;
-    grouped_gemm_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(
+    grouped_gemm_kernel<false, false><<<grid, kThreads, kSmemBytes, st>>>(
         a, bd, bd, o, g.offsets, g.counts, g.prefix, g.E, I, H,
-        reinterpret_cast<__nv_bfloat16*>(y), g.err);
+        reinterpret_cast<__nv_bfloat16*>(y), g.err, nullptr, 0, 0);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

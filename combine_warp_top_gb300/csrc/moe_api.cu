@@ -144,6 +144,20 @@ moe_status moe_ffn_gate_up(const uint16_t* rows, const moe_layout* layout, const
                           h, as_stream(stream));
 }
 
+moe_status moe_ffn_gate_up_gather(const uint16_t* src, const int32_t* row_index, int64_t src_rows,
+                                  const moe_layout* layout, const moe_shape* shape,
+                                  const uint16_t* w_gate, const uint16_t* w_up, uint16_t* h,
+                                  void* ws, size_t ws_bytes, void* stream) {
+    MOE_TRY(check_shape(shape));
+    MOE_TRY(check_layout(layout, shape));
+    MOE_TRY(check_ws(shape, ws, ws_bytes));
+    if (shape->N == 0) return MOE_OK;
+    if (!src || !row_index || !w_gate || !w_up || !h) return MOE_ERR_INVALID_ARG;
+    if (src_rows <= 0 || src_rows >= ((int64_t)1 << 31)) return MOE_ERR_INVALID_ARG;
+    return launch_gate_up(src, routed_group(*layout, *shape, ws), shape->H, shape->I, w_gate, w_up,
+                          h, as_stream(stream), row_index, src_rows);
+}
+
 moe_status moe_ffn_down(const uint16_t* h, const moe_layout* layout, const moe_shape* shape,
                         const uint16_t* w_down, uint16_t* y, void* ws, size_t ws_bytes,
                         void* stream) {
@@ -168,6 +182,7 @@ moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const mo
     if (shape->dedup && !xe) return MOE_ERR_INVALID_ARG;
     const uint16_t* rows = xd;
     if (shape->dedup) {
+        // materialised expansion: measured faster than gathering inside the GEMM
         MOE_TRY(moe_expand(xd, layout, shape, xe, stream));
         rows = xe;
     }

@@ -61,6 +61,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_expand": (I32, [P, lay, shp, P, P]),
         "moe_ffn_gate_up": (I32, [P, lay, shp, P, P, P, P, S, P]),
         "moe_ffn_down": (I32, [P, lay, shp, P, P, P, S, P]),
+        "moe_ffn_gate_up_gather": (I32, [P, P, ctypes.c_int64, lay, shp, P, P, P, P, S, P]),
         "moe_combine": (I32, [P, P, lay, shp, P, P, P, P]),
         "moe_layer_forward": (I32, [P, P, P, P, P, P, P, shp, P, P, lay, P, P, P, P, P, P, P, S,
                                     P]),
@@ -211,6 +212,14 @@ def moe_ffn_gate_up(rows, layout: Layout, shape: Shape, w_gate, w_up, h, ws, str
     _check(load().moe_ffn_gate_up(_ptr(rows), ctypes.byref(layout.c), ctypes.byref(shape.c()),
                                   _ptr(w_gate), _ptr(w_up), _ptr(h), _ptr(ws), ws.numel(),
                                   _stream(stream)), "moe_ffn_gate_up")
+
+
+def moe_ffn_gate_up_gather(src, row_index, layout: Layout, shape: Shape, w_gate, w_up, h, ws,
+                           stream=None):
+    _check(load().moe_ffn_gate_up_gather(_ptr(src), _ptr(row_index), src.shape[0],
+                                         ctypes.byref(layout.c), ctypes.byref(shape.c()),
+                                         _ptr(w_gate), _ptr(w_up), _ptr(h), _ptr(ws), ws.numel(),
+                                         _stream(stream)), "moe_ffn_gate_up_gather")
 
 
 def moe_ffn_down(h, layout: Layout, shape: Shape, w_down, y, ws, stream=None):
@@ -377,7 +386,7 @@ class MoELayer:
     def kernel_launches_per_step(self) -> int:
         """Kernels of this library launched by one forward (route 1, layout 3,
         dispatch 1, expand 1 with dedup, each GEMM 2 with its schedule, combine
-        1 or 2 with dedup)."""
+        1 or 2 with dedup, shared expert 5)."""
         s = self.shape
         if s.N == 0:
             return 0

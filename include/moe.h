@@ -165,6 +165,22 @@ moe_status moe_ffn_down(const uint16_t* h, const moe_layout* layout, const moe_s
                         const uint16_t* w_down, uint16_t* y, void* ws, size_t ws_bytes,
                         void* stream);
 
+/* moe_ffn_gate_up with the rows gathered inside the GEMM (the kernel-fusion
+ * page's MegaKernel idea of feeding the MatMul without a separate "group" or
+ * "pack" copy): problem row i (expert-major, i < N*k) is row row_index[i] of
+ * src bf16 [src_rows, H].  With src = the dedup rows and row_index =
+ * layout->expand_src this is the dedup expansion; with src = x and row_index
+ * = layout->row_token it is the plain dispatch.  Out-of-range indices read
+ * row 0.  Results are bit-identical to materialising the rows first.  The
+ * producer issues one 4-row TMA gather per lane and stage; on GB300 this is
+ * about 3x slower than the 2-D box load of materialised rows for these
+ * GEMMs (the gather re-runs for every 64-column k-block), so moe_expert_ffn
+ * keeps the materialised expansion. */
+moe_status moe_ffn_gate_up_gather(const uint16_t* src, const int32_t* row_index, int64_t src_rows,
+                                  const moe_layout* layout, const moe_shape* shape,
+                                  const uint16_t* w_gate, const uint16_t* w_up, uint16_t* h,
+                                  void* ws, size_t ws_bytes, void* stream);
+
 /* Combine (kernel-fusion page, "Expert parallelism: dispatch and combine" and
  * stage 7 "reduce"; residual add of FarSkip-Collective Sec. 3).
  * Plain: out[t, :] = bf16( residual[t, :] + sum_j topk_w[t, j] * y[pair_row[t, j], :] ),

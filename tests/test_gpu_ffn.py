@@ -28,15 +28,21 @@ def run_ffn(wl, dedup, ids=None, placement=None):
     rows = shape.R_d_max if dedup else shape.R
     xd = torch.zeros(rows, wl.H, dtype=torch.bfloat16, device="cuda")
     moe.moe_dispatch(dev_bf16(x), lay, shape, xd)
-    xe = torch.empty(shape.R, wl.H, dtype=torch.bfloat16, device="cuda") if dedup else None
     h = torch.empty(shape.R, wl.I, dtype=torch.bfloat16, device="cuda")
     y = torch.empty(shape.R, wl.H, dtype=torch.bfloat16, device="cuda")
+    xe = torch.empty(shape.R, wl.H, dtype=torch.bfloat16, device="cuda") if dedup else None
     moe.moe_expert_ffn(xd, lay, shape, dev_bf16(wg), dev_bf16(wu), dev_bf16(wd), xe, h, y, ws)
     torch.cuda.synchronize()
     assert moe.moe_get_error(ws) == 0
     xe_ref = oracle.dispatch(x, ref["row_token"])
     if dedup:
         assert np.array_equal(host_u16(xe), xe_ref)
+        # the same rows gathered inside the GEMM give the same h, bit for bit
+        h2 = torch.empty_like(h)
+        moe.moe_ffn_gate_up_gather(xd, lay["expand_src"], lay, shape, dev_bf16(wg), dev_bf16(wu),
+                                   h2, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(h.view(torch.int16), h2.view(torch.int16))
     h_ref, y_ref = oracle.expert_ffn(xe_ref, ref["expert_offsets"], ref["expert_counts"], wg, wu, wd)
     return host_f64(h), host_f64(y), h_ref, y_ref
 
@@ -87,3 +93,26 @@ def test_ffn_permuted_placement():
     placement = synth.permutation(0, 52, wl.E).astype(np.int32)
     h, y, h_ref, y_ref = run_ffn(wl, dedup=False, ids=ids, placement=placement)
     assert_close(y, y_ref, "y")
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "wide", "odd_h", "deep_k", "e256"])
+def test_gathered_rows_equal_dispatched_rows(name):
+    """The gate/up GEMM fed by gather4 straight from x through row_token gives
+    bit for bit the h of the GEMM fed by the dispatched rows."""
+    wl = SMALL[name]
+    ids, _ = oracle.route(synth.make_logits(wl), wl.k)
+    x = dev_bf16(synth.make_x(wl))
+    wg, wu = dev_bf16(synth.make_weight(wl, "gate")), dev_bf16(synth.make_weight(wl, "up"))
+    shape = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I)
+    lay = moe.Layout(shape)
+    ws = moe.workspace(shape)
+    moe.moe_dispatch_layout(dev_i32(ids), None, shape, lay, ws)
+    xd = torch.empty(shape.R, wl.H, dtype=torch.bfloat16, device="cuda")
+    moe.moe_dispatch(x, lay, shape, xd)
+    h1 = torch.empty(shape.R, wl.I, dtype=torch.bfloat16, device="cuda")
+    h2 = torch.empty_like(h1)
+    moe.moe_ffn_gate_up(xd, lay, shape, wg, wu, h1, ws)
+    moe.moe_ffn_gate_up_gather(x, lay["row_token"], lay, shape, wg, wu, h2, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_error(ws) == 0
+    assert torch.equal(h1.view(torch.int16), h2.view(torch.int16))
