@@ -102,6 +102,15 @@ moe_status moe_route_full_softmax(const float* logits, const moe_shape* shape, i
                                     as_stream(stream)));
 }
 
+moe_status moe_route_sigmoid_bias(const float* logits, const float* bias, const moe_shape* shape,
+                                  int32_t* topk_ids, float* topk_w, void* stream) {
+    MOE_TRY(check_shape(shape));
+    if (shape->N == 0) return MOE_OK;
+    if (!logits || !bias || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_route_sigmoid(logits, bias, shape->N, shape->E, shape->k, topk_ids,
+                                            topk_w, as_stream(stream)));
+}
+
 moe_status moe_dispatch_layout(const int32_t* topk_ids, const int32_t* placement,
                                const moe_shape* shape, const moe_layout* layout, void* ws,
                                size_t ws_bytes, void* stream) {

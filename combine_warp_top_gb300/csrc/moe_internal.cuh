@@ -61,6 +61,9 @@ __device__ __forceinline__ void set_error(int* err, int code) {
 cudaError_t launch_route(const float* logits, int N, int E, int k, int32_t* ids, float* w,
                          bool renorm, cudaStream_t st);
 
+cudaError_t launch_route_sigmoid(const float* logits, const float* bias, int N, int E, int k,
+                                 int32_t* ids, float* w, cudaStream_t st);
+
 cudaError_t launch_layout(const int32_t* ids, const int32_t* placement, const moe_shape& s,
                           const moe_layout& L, void* ws, cudaStream_t st);
 

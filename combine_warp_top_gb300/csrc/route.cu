@@ -96,6 +96,83 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
     }
 }
 
+// Sigmoid router with a per-expert selection bias (the auxiliary-loss-free
+// router of "Expert Coupling" Appendix A-B): score s_e = sigmoid(L_e),
+// evaluated in double and rounded once to fp32; the k largest s_e + bias_e
+// (fp32 add; ties to the lower expert index) are selected; the weights are
+// s_e / sum of the selected s_e (the bias only steers the selection).
+template <int VPL>
+__global__ void __launch_bounds__(256) route_sigmoid_kernel(const float* __restrict__ logits,
+                                                            const float* __restrict__ bias, int N,
+                                                            int E, int k,
+                                                            int32_t* __restrict__ ids,
+                                                            float* __restrict__ w) {
+    const int lane = threadIdx.x & 31;
+    const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    if (t >= N) return;
+    const float* row = logits + (size_t)t * E;
+    float v[VPL], sc[VPL];
+    uint32_t taken = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int e = i * 32 + lane;
+        if (e < E) {
+            const double L = (double)__ldg(row + e);
+            sc[i] = (float)(1.0 / (1.0 + exp(-L)));
+            v[i] = sc[i] + __ldg(bias + e);
+        } else {
+            sc[i] = 0.f;
+            v[i] = 0.f;
+            taken |= 1u << i;
+        }
+    }
+    int my_id = -1;
+    float my_s = 0.f;
+    for (int j = 0; j < k; ++j) {
+        float bv = 0.f, bs = 0.f;
+        int bi = -1;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            if (!((taken >> i) & 1u) && (bi < 0 || v[i] > bv)) {
+                bv = v[i];
+                bs = sc[i];
+                bi = i * 32 + lane;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const float os = __shfl_xor_sync(0xffffffffu, bs, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (beats(ov, oi, bv, bi)) {
+                bv = ov;
+                bs = os;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == j) {
+            my_id = bi;
+            my_s = bs;
+        }
+    }
+    float sum = lane < k ? my_s : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane < k) {
+        ids[(size_t)t * k + lane] = my_id;
+        w[(size_t)t * k + lane] = my_s / sum;
+    }
+}
+
+template <int VPL>
+cudaError_t go_sigmoid(const float* logits, const float* bias, int N, int E, int k, int32_t* ids,
+                       float* w, cudaStream_t st) {
+    const int blocks = (N + 7) / 8;
+    route_sigmoid_kernel<VPL><<<blocks, 256, 0, st>>>(logits, bias, N, E, k, ids, w);
+    return cudaGetLastError();
+}
+
 template <int VPL>
 cudaError_t go(const float* logits, int N, int E, int k, int32_t* ids, float* w, bool renorm,
                cudaStream_t st) {
@@ -120,6 +197,17 @@ cudaError_t launch_route(const float* logits, int N, int E, int k, int32_t* ids,
     if (E <= 256) return go<8>(logits, N, E, k, ids, w, renorm, st);
     if (E <= 512) return go<16>(logits, N, E, k, ids, w, renorm, st);
     return go<32>(logits, N, E, k, ids, w, renorm, st);
+}
+
+cudaError_t launch_route_sigmoid(const float* logits, const float* bias, int N, int E, int k,
+                                 int32_t* ids, float* w, cudaStream_t st) {
+    if (N == 0) return cudaSuccess;
+    if (E <= 32) return go_sigmoid<1>(logits, bias, N, E, k, ids, w, st);
+    if (E <= 64) return go_sigmoid<2>(logits, bias, N, E, k, ids, w, st);
+    if (E <= 128) return go_sigmoid<4>(logits, bias, N, E, k, ids, w, st);
+    if (E <= 256) return go_sigmoid<8>(logits, bias, N, E, k, ids, w, st);
+    if (E <= 512) return go_sigmoid<16>(logits, bias, N, E, k, ids, w, st);
+    return go_sigmoid<32>(logits, bias, N, E, k, ids, w, st);
 }
 
 }  // namespace moe

@@ -55,6 +55,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_workspace_bytes": (S, [shp]),
         "moe_route": (I32, [P, shp, P, P, P]),
         "moe_route_full_softmax": (I32, [P, shp, P, P, P]),
+        "moe_route_sigmoid_bias": (I32, [P, P, shp, P, P, P]),
         "moe_dispatch_layout": (I32, [P, P, shp, lay, P, S, P]),
         "moe_dispatch": (I32, [P, lay, shp, P, P]),
         "moe_expert_ffn": (I32, [P, lay, shp, P, P, P, P, P, P, P, S, P]),
@@ -177,6 +178,12 @@ def moe_route(logits, shape: Shape, topk_ids, topk_w, stream=None):
 def moe_route_full_softmax(logits, shape: Shape, topk_ids, topk_w, stream=None):
     _check(load().moe_route_full_softmax(_ptr(logits), ctypes.byref(shape.c()), _ptr(topk_ids),
                                          _ptr(topk_w), _stream(stream)), "moe_route_full_softmax")
+
+
+def moe_route_sigmoid_bias(logits, bias, shape: Shape, topk_ids, topk_w, stream=None):
+    _check(load().moe_route_sigmoid_bias(_ptr(logits), _ptr(bias), ctypes.byref(shape.c()),
+                                         _ptr(topk_ids), _ptr(topk_w), _stream(stream)),
+           "moe_route_sigmoid_bias")
 
 
 def moe_dispatch_layout(topk_ids, placement, shape: Shape, layout: Layout, ws, stream=None):
@@ -334,6 +341,20 @@ class MoELayer:
                           residual, self.shape, self.topk_ids, self.topk_w, self.layout,
                           self.xd, self.xe, self.h, self.y, self.partial, out, self.ws, stream)
         return out
+
+    def capture(self, logits, x, residual=None, out=None):
+        """Capture one forward on these exact buffers into a CUDA graph and
+        return it; graph.replay() then reruns the whole layer (all of its
+        kernel launches) on whatever the buffers hold, with one launch of the
+        graph.  The first forward (outside the capture) sets the kernels'
+        shared-memory attributes."""
+        out = self.out if out is None else out
+        self.forward(logits, x, residual, out)  # warm-up outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.forward(logits, x, residual, out)
+        return g
 
     STAGES = ("route", "layout", "dispatch", "expand", "gate_up", "down", "shared", "combine")
 

@@ -111,6 +111,15 @@ moe_status moe_route(const float* logits, const moe_shape* shape, int32_t* topk_
 moe_status moe_route_full_softmax(const float* logits, const moe_shape* shape, int32_t* topk_ids,
                                   float* topk_w, void* stream);
 
+/* Router variant: the auxiliary-loss-free sigmoid router with a per-expert
+ * bias ("Expert Coupling" Appendix A-B, the DeepSeek-V3 router).  Scores
+ * s_e = sigmoid(L_e) are evaluated in double and rounded once to fp32; the
+ * k largest s_e + bias[e] (an fp32 add; descending, ties to the lower expert
+ * index) are selected; topk_w[t, j] = s_j / sum of the selected s (the bias
+ * steers the selection only).  bias: device fp32 [E]. */
+moe_status moe_route_sigmoid_bias(const float* logits, const float* bias, const moe_shape* shape,
+                                  int32_t* topk_ids, float* topk_w, void* stream);
+
 /* Dispatch layout (kernel-fusion page, "Expert parallelism: dispatch and
  * combine" and "Fusing the layer into one kernel" stage 3 "group"; "Expert
  * Coupling" Sec. V-A and Appendix A-A2).  Stable counting sort of the (t, j)

@@ -104,6 +104,28 @@ def route(logits, k, renormalize=True):
     return ids.astype(np.int32), w
 
 
+def route_sigmoid_bias(logits, bias, k):
+    """The auxiliary-loss-free sigmoid router ("Expert Coupling" Appendix A-B:
+    sigmoid scores with a per-expert bias; the DeepSeek-V3 router).  Reading:
+    s_e = sigmoid(L_e) evaluated in float64 and rounded once to fp32; the k
+    largest fp32 sums s_e + bias_e are selected (descending, ties to the lower
+    expert index); the weights are s_e / sum of the selected s_e, in float64.
+    The selection is a floating-point decision, so it is taken on the same
+    fp32 values the kernel compares."""
+    L = np.asarray(logits, dtype=np.float32)
+    b = np.asarray(bias, dtype=np.float32)
+    N, E = L.shape
+    if not (1 <= k <= E):
+        raise ValueError("need 1 <= k <= E")
+    s = (1.0 / (1.0 + np.exp(-L.astype(np.float64)))).astype(np.float32)
+    key = (s + b[None, :]).astype(np.float32)
+    expert = np.broadcast_to(np.arange(E), L.shape)
+    order = np.lexsort((expert, -key.astype(np.float64)), axis=-1)
+    ids = order[:, :k]
+    sel = np.take_along_axis(s, ids, axis=1).astype(np.float64)
+    return ids.astype(np.int32), sel / sel.sum(axis=1, keepdims=True)
+
+
 # ----------------------------------------------------------------------------- layout
 
 def dispatch_layout(topk_ids, placement, E, W):

@@ -168,3 +168,25 @@ def test_wait_timeout_is_reported_and_the_context_survives():
     b = layer.forward(L, x, res)
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("dedup", [False, True])
+def test_cuda_graph_replay_matches_eager(dedup):
+    """The whole layer captured once as a CUDA graph and replayed on new
+    contents of the same input buffers gives the eager results bit for bit."""
+    wl = SMALL["ragged"]
+    layer, _ = build_layer(wl, dedup)
+    L = torch.from_numpy(synth.make_logits(wl, 0)).cuda()
+    x, res = dev_bf16(synth.make_x(wl, 0)), dev_bf16(synth.make_residual(wl, 0))
+    g = layer.capture(L, x, res)
+    for seed in (1, 2):
+        L.copy_(torch.from_numpy(synth.make_logits(wl, seed)))
+        x.copy_(dev_bf16(synth.make_x(wl, seed)))
+        res.copy_(dev_bf16(synth.make_residual(wl, seed)))
+        g.replay()
+        torch.cuda.synchronize()
+        got = layer.out.clone()
+        want = layer.forward(L, x, res)
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    layer.check_device_errors()

@@ -85,3 +85,18 @@ def test_shared_expert_full_size_deepseek():
     routed, _ = oracle.token_outputs(x[toks], ids[toks], w[toks], weights_of, res[toks])
     _, y_s = oracle.shared_expert(x[toks], sh_h)
     assert_close(host_f64(out[torch.from_numpy(toks).cuda()]), routed + y_s, "out with shared")
+
+
+@pytest.mark.parametrize("N,E,k", [(64, 8, 2), (1000, 64, 6), (4096, 256, 8), (500, 1024, 32),
+                                   (300, 7, 7)])
+def test_route_sigmoid_bias(N, E, k):
+    L = synth.normal_f32(0, 93, (N, E))
+    b = synth.normal_f32(0, 94, (E,), std=0.05)
+    shape = moe.Shape(N, 8, E, k, 1, 8)
+    ids = torch.empty(N * k, dtype=torch.int32, device="cuda")
+    w = torch.empty(N * k, dtype=torch.float32, device="cuda")
+    moe.moe_route_sigmoid_bias(torch.from_numpy(L).cuda(), torch.from_numpy(b).cuda(), shape, ids, w)
+    torch.cuda.synchronize()
+    ref_ids, ref_w = oracle.route_sigmoid_bias(L, b, k)
+    assert np.array_equal(ids.view(N, k).cpu().numpy(), ref_ids)
+    np.testing.assert_allclose(w.view(N, k).cpu().numpy(), ref_w, rtol=0, atol=2e-6)

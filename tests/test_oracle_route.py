@@ -156,3 +156,37 @@ def test_full_softmax_variant():
     np.testing.assert_allclose(w_f / w_f.sum(1, keepdims=True), w_r, rtol=1e-12)
     ids_all, w_all = oracle.route(L, 16, renormalize=False)
     np.testing.assert_allclose(w_all.sum(1), 1.0, atol=1e-12)  # k = E: all probabilities
+
+
+def test_sigmoid_bias_router_pins():
+    """The aux-loss-free sigmoid router: selection by fp32(sigmoid(L)) + bias
+    (brute force by definition), weights = selected scores renormalised, bias
+    steering the choice but not the weights."""
+    rng = np.random.default_rng(5)
+    for trial in range(100):
+        E = int(rng.integers(2, 12))
+        k = int(rng.integers(1, E + 1))
+        L = (rng.integers(-8, 9, size=(1, E)) * 0.25).astype(np.float32)
+        b = (rng.integers(-3, 4, size=E) * 0.05).astype(np.float32)
+        ids, w = oracle.route_sigmoid_bias(L, b, k)
+        s = (1.0 / (1.0 + np.exp(-L[0].astype(np.float64)))).astype(np.float32)
+        key = (s + b).astype(np.float32)
+        assert ids[0].tolist() == selected_by_definition(key.tolist(), k)
+        sel = s[ids[0]].astype(np.float64)
+        np.testing.assert_allclose(w[0], sel / sel.sum(), rtol=1e-15)
+    # zero bias and well separated logits: the same experts as the softmax router
+    L = (rng.permuted(np.tile(np.arange(16), (50, 1)), axis=1) * 0.3 - 2.0).astype(np.float32)
+    ids_s, _ = oracle.route_sigmoid_bias(L, np.zeros(16, np.float32), 4)
+    ids_r, _ = oracle.route(L, 4)
+    assert np.array_equal(ids_s, ids_r)
+    # a large bias forces the choice; the weights still come from the scores alone
+    L = synth.normal_f32(0, 16, (20, 8))
+    b = np.zeros(8, np.float32)
+    b[[1, 6]] = 10.0
+    ids, w = oracle.route_sigmoid_bias(L, b, 2)
+    assert all(sorted(r) == [1, 6] for r in ids.tolist())
+    s = 1.0 / (1.0 + np.exp(-L.astype(np.float64)))
+    for t in range(20):
+        a, c = ids[t]
+        np.testing.assert_allclose(w[t], [s[t, a] / (s[t, a] + s[t, c]), s[t, c] / (s[t, a] + s[t, c])],
+                                   rtol=1e-7)
