@@ -125,3 +125,71 @@ def test_layout_mutants_are_caught(mutant):
     ids = layout_pins.random_ids(40, 8, 3, seed=9)
     with pytest.raises(AssertionError):
         layout_pins.check_invariants(mutant, ids, np.arange(8), 8, 4)
+
+
+# ---- placement search and the router variants -----------------------------------------
+
+import test_oracle_placement as placement_pins  # noqa: E402
+
+
+def partition_without_gain_check(W, G, max_swaps):
+    """Plausible slip: apply the best swap even when it does not improve."""
+    W = np.asarray(W, dtype=np.int64)
+    E = W.shape[0]
+    group = np.arange(E) // (E // G)
+    swaps = 0
+    for _ in range(max_swaps):
+        best, pair = None, None
+        for a in range(E):
+            for b in range(a + 1, E):
+                if group[a] != group[b]:
+                    g = mo.swap_gain(W, group, a, b)
+                    if best is None or g > best:
+                        best, pair = g, (a, b)
+        if pair is None or swaps >= 3 * E:
+            break
+        a, b = pair
+        group[a], group[b] = group[b], group[a]
+        swaps += 1
+    return group, swaps
+
+
+def swap_gain_sign_error(W, group, a, b):
+    return -_SWAP_GAIN(W, group, a, b)
+
+
+_SWAP_GAIN = mo.swap_gain
+
+
+@pytest.mark.parametrize("mutant,target", [(partition_without_gain_check, "partition"),
+                                           (swap_gain_sign_error, "swap_gain")])
+def test_placement_mutants_are_caught(mutant, target, monkeypatch):
+    monkeypatch.setattr(mo, target, mutant)
+    monkeypatch.setattr(oracle, target, mutant)
+    pins = [lambda: placement_pins.test_partition_is_balanced_and_locally_optimal(12, 3, 4),
+            placement_pins.test_swap_gain_is_the_change_of_the_objective,
+            placement_pins.test_ties_take_the_first_pair_in_lexicographic_order]
+    caught = False
+    for pin in pins:
+        try:
+            pin()
+        except AssertionError:
+            caught = True
+            break
+    assert caught
+
+
+def test_sigmoid_router_mutant_with_biased_weights_is_caught(monkeypatch):
+    """Slip: the weights renormalise s + bias instead of s."""
+    original = mo.route_sigmoid_bias
+
+    def mutant(logits, bias, k):
+        ids, _ = original(logits, bias, k)
+        L = np.asarray(logits, np.float64)
+        s = 1.0 / (1.0 + np.exp(-L)) + np.asarray(bias, np.float64)[None, :]
+        sel = np.take_along_axis(s, ids.astype(np.int64), 1)
+        return ids, sel / sel.sum(1, keepdims=True)
+
+    monkeypatch.setattr(oracle, "route_sigmoid_bias", mutant)
+    with pytest.raises(AssertionError):
+        route_pins.test_sigmoid_bias_router_pins()
