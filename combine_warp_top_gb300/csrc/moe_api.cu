@@ -2,6 +2,7 @@
 // chaining of the kernels of the other files on the caller's stream.
 // Declarations and the contract of every call are in include/moe.h.
 #include <stdio.h>
+#include <stdlib.h>
 
 #include "moe_internal.cuh"
 
@@ -49,6 +50,16 @@ moe_status check_ws(const moe_shape* s, void* ws, size_t ws_bytes) {
 }
 
 inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// CTA-pair (256-row) GEMM tiles pay off when experts have many rows; with few
+// rows per expert the single-CTA 128-row tiles waste less.  MOE_GEMM_PAIR=0/1
+// forces one or the other (tests run both kernels on small shapes).
+bool use_pair(long long R, int E) {
+    const char* v = getenv("MOE_GEMM_PAIR");
+    if (v && v[0] == '0') return false;
+    if (v && v[0] == '1') return true;
+    return R >= 512LL * E;
+}
 
 // The routed experts' GEMM problem: the plain expert-major rows of the layout.
 GemmGroup routed_group(const moe_layout& L, const moe_shape& s, void* ws) {
@@ -149,8 +160,10 @@ moe_status moe_ffn_gate_up(const uint16_t* rows, const moe_layout* layout, const
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (shape->N == 0) return MOE_OK;
     if (!rows || !w_gate || !w_up || !h) return MOE_ERR_INVALID_ARG;
-    return launch_gate_up(rows, routed_group(*layout, *shape, ws), shape->H, shape->I, w_gate, w_up,
-                          h, as_stream(stream));
+    const GemmGroup g = routed_group(*layout, *shape, ws);
+    if (use_pair(g.R, g.E))
+        return launch_gate_up_pair(rows, g, shape->H, shape->I, w_gate, w_up, h, as_stream(stream));
+    return launch_gate_up(rows, g, shape->H, shape->I, w_gate, w_up, h, as_stream(stream));
 }
 
 moe_status moe_ffn_gate_up_gather(const uint16_t* src, const int32_t* row_index, int64_t src_rows,
@@ -175,8 +188,10 @@ moe_status moe_ffn_down(const uint16_t* h, const moe_layout* layout, const moe_s
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (shape->N == 0) return MOE_OK;
     if (!h || !w_down || !y) return MOE_ERR_INVALID_ARG;
-    return launch_down(h, routed_group(*layout, *shape, ws), shape->H, shape->I, w_down, y,
-                       as_stream(stream));
+    const GemmGroup g = routed_group(*layout, *shape, ws);
+    if (use_pair(g.R, g.E))
+        return launch_down_pair(h, g, shape->H, shape->I, w_down, y, as_stream(stream));
+    return launch_down(h, g, shape->H, shape->I, w_down, y, as_stream(stream));
 }
 
 moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const moe_shape* shape,
@@ -225,6 +240,10 @@ moe_status moe_shared_expert_ffn(const uint16_t* x, const moe_shape* shape, int3
     const GemmGroup g = dense_group(*shape, ws);
     MOE_TRY(cuda_status(launch_dense_group(shape->N, const_cast<int32_t*>(g.counts),
                                            const_cast<int32_t*>(g.offsets), st)));
+    if (use_pair(g.R, g.E)) {
+        MOE_TRY(launch_gate_up_pair(x, g, shape->H, I_shared, w_gate_s, w_up_s, h_s, st));
+        return launch_down_pair(h_s, g, shape->H, I_shared, w_down_s, y_s, st);
+    }
     MOE_TRY(launch_gate_up(x, g, shape->H, I_shared, w_gate_s, w_up_s, h_s, st));
     return launch_down(h_s, g, shape->H, I_shared, w_down_s, y_s, st);
 }

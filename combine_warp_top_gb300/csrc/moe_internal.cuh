@@ -111,6 +111,22 @@ cudaError_t launch_coselection(const int32_t* ids, const moe_shape& s, int32_t* 
 moe_status placement_search(const int32_t* W, int E, int ranks, int nodes, long long max_swaps,
                             int32_t* placement, long long* swaps_made);
 
+// Tensor maps (bf16, 128-byte swizzle, zero fill) and the GEMM tile schedule
+// (grouped_gemm.cu), shared by the single-CTA and the CTA-pair GEMMs.
+bool map_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
+bool map_3d(CUtensorMap* m, const void* ptr, uint64_t E, uint64_t rows, uint64_t cols,
+            uint32_t box_rows);
+// prefix[e] = sum over experts before e of ceil(counts / bm); prefix[E] = total.
+cudaError_t launch_schedule(const int32_t* counts, int E, int bm, int32_t* prefix,
+                            cudaStream_t st);
+
+// CTA-pair GEMMs (grouped_gemm_2sm.cu): 256-row tiles on tcgen05 cta_group::2.
+moe_status launch_gate_up_pair(const uint16_t* rows, const GemmGroup& g, int H, int I,
+                               const uint16_t* wg, const uint16_t* wu, uint16_t* h,
+                               cudaStream_t st);
+moe_status launch_down_pair(const uint16_t* h, const GemmGroup& g, int H, int I,
+                            const uint16_t* wd, uint16_t* y, cudaStream_t st);
+
 int sm_count();
 
 }  // namespace moe
