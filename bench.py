@@ -79,23 +79,25 @@ def workload(args):
     return wl
 
 
-def algorithmic(wl, R_d):
+def algorithmic(wl, R_d, fused_dispatch=False):
     """Bytes each stage must move and flops it must do (bf16 activations and
-    weights, fp32 logits and weights of the router)."""
+    weights, fp32 logits and weights of the router).  The gate/up GEMM reads
+    its A rows once from wherever they live: the dispatched rows (plain), the
+    dedup rows it expands itself (dedup), or x itself when it also does the
+    dispatch (fused_dispatch)."""
     N, H, E, k, I, W = wl.N, wl.H, wl.E, wl.k, wl.I, wl.W
     R = N * k
     rows_d = R_d if wl.dedup else R
+    a_rows = R_d if wl.dedup else (N if fused_dispatch else R)
     st = {
         "route": dict(bytes=N * E * 4 + R * 8),
         "layout": dict(bytes=2 * R * 4 + (5 if wl.dedup else 2) * R * 4),
         "dispatch": dict(bytes=N * H * 2 + rows_d * H * 2),
-        "gate_up": dict(bytes=2 * E * I * H * 2 + R * H * 2 + R * I * 2, flops=4 * R * H * I),
+        "gate_up": dict(bytes=2 * E * I * H * 2 + a_rows * H * 2 + R * I * 2, flops=4 * R * H * I),
         "down": dict(bytes=E * H * I * 2 + R * I * 2 + R * H * 2, flops=2 * R * H * I),
         "combine": dict(bytes=R * H * 2 + 2 * N * H * 2 + R * 8 +
                         (2 * R_d * H * 2 if wl.dedup else 0)),
     }
-    if wl.dedup:
-        st["expand"] = dict(bytes=R_d * H * 2 + R * H * 2)
     return st
 
 
@@ -403,8 +405,7 @@ def run_ours(args):
         else:
             pipe.forward(L_d, x_d, r_d, out=layer.out, gemm_events=gev[i])
 
-    stages = [s for s in moe.MoELayer.STAGES
-              if (s != "expand" or wl.dedup) and (s != "shared" or shared is not None)]
+    stages = layer.stage_names()
     # external events: inside a captured graph they become timing nodes
     mk = lambda: (torch.cuda.Event(enable_timing=True, external=use_graph),  # noqa: E731
                   torch.cuda.Event(enable_timing=True, external=use_graph))
@@ -475,7 +476,7 @@ def run_ours(args):
         return None
 
     pk, pk_src = peaks()
-    alg = algorithmic(wl, R_d)
+    alg = algorithmic(wl, R_d, layer.fused_dispatch)
     if shared is not None:
         I_s = args.shared_expert
         alg["shared"] = dict(bytes=3 * I_s * wl.H * 2 + 2 * wl.N * wl.H * 2 + 2 * wl.N * I_s * 2,
@@ -505,8 +506,16 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 3)
     roof["traffic"] = recorded_traffic(wl)
-    roof["kernel"] = "grouped_gemm_kernel<SwiGLU> (moe_ffn_gate_up)" + (
-        f", summed over the {n_mb} microbatches of a step" if pipe is not None else "")
+    if wl.dedup:
+        roof["kernel"] = ("grouped_gemm_kernel<SwiGLU, gathered rows> (moe_ffn_gate_up_gather: "
+                          "the dedup expansion done by the GEMM's gather warps)")
+    elif layer.fused_dispatch:
+        roof["kernel"] = ("grouped_gemm_kernel<SwiGLU, gathered rows> (moe_ffn_gate_up_gather: "
+                          "the dispatch copy done by the GEMM's gather warps)")
+    else:
+        roof["kernel"] = "grouped_gemm_kernel<SwiGLU> or its CTA-pair form (moe_ffn_gate_up)"
+    if pipe is not None:
+        roof["kernel"] += f", summed over the {n_mb} microbatches of a step"
     roof["peak_source"] = f"{pk_src} ({'bf16_tflops_sustained' if roof['unit'] == 'TFLOP/s' else 'hbm_gbs'})"
     roof["algorithmic_per_launch"] = {"bytes": a["bytes"], "flops": a["flops"]}
 

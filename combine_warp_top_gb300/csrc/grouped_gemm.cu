@@ -24,6 +24,9 @@
 // has in flight, frees TMEM and returns.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 
@@ -42,6 +45,16 @@ constexpr int B_BYTES = kMmaN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int kThreads = 192;
 constexpr int kEpilogueWarps = 4;
+// Gathered A rows (kGather): row i of the problem is row a_rows[i] of a
+// source matrix (x through row_token, or the dedup rows through expand_src),
+// copied by 4 extra gather warps with 16-byte cp.async into the 128B-swizzled
+// layout a TMA box would have produced; B still comes by TMA.  This replaces
+// a separate copy kernel that would write the rows out and read them back.
+constexpr int kGatherWarps = 4;
+constexpr int kGatherThreads = kGatherWarps * 32;
+__host__ __device__ constexpr int threads_for(bool gather) {
+    return gather ? kThreads + kGatherThreads : kThreads;
+}
 
 struct Ctl {
     uint64_t full[kStages];
@@ -70,10 +83,11 @@ constexpr size_t kSmemBytes = 1024 + (size_t)kStages * STAGE_BYTES +
 
 using namespace ptx;
 
-// kGatherA: A row i of the problem is row a_rows[i] of the map's tensor
-// (gathered by the producer warp with tile::gather4); otherwise row i itself.
-template <bool kSwiGLU, bool kGatherA>
-__global__ void __launch_bounds__(kThreads, 1)
+// kGather: A row i of the problem is row a_rows[i] of a_src (rows >= a_total
+// and indices outside [0, a_src_rows) read row 0; such rows are masked on
+// store); otherwise row i of tmA's tensor.
+template <bool kSwiGLU, bool kGather>
+__global__ void __launch_bounds__(threads_for(kGather), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmB1,
@@ -82,7 +96,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int32_t* __restrict__ expert_counts,
                         const int32_t* __restrict__ mblk_prefix, int E, int K, int n_out,
                         __nv_bfloat16* __restrict__ out, int* err,
-                        const int32_t* __restrict__ a_rows, int a_total, int a_src_rows) {
+                        const int32_t* __restrict__ a_rows, int a_total, int a_src_rows,
+                        const uint16_t* __restrict__ a_src) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* tiles = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -103,7 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&ctl->full[s]), 1);
+            // kGather: the producer's arrive plus one cp.async arrival per gather thread
+            mbar_init(smem_u32(&ctl->full[s]), kGather ? 1 + kGatherThreads : 1);
             mbar_init(smem_u32(&ctl->empty[s]), 1);
         }
         for (int a = 0; a < kAccs; ++a) {
@@ -115,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0 && lane == 0) {
-        prefetch_map(&tmA);
+        if (!kGather) prefetch_map(&tmA);
         prefetch_map(&tmB0);
         if (kSwiGLU) prefetch_map(&tmB1);
         prefetch_map(&tmOut);
@@ -131,11 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = ctl->prefix[E] * NB;
 
     if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        // Plain rows: lane 0 issues everything.  Gathered rows: every lane
-        // issues one 4-row gather of A per stage; lane 0 arms the barrier and
-        // loads B.
-        if (kGatherA || lane == 0) {
+        // ---------------- TMA producer (A unless gathered, and B) ----------------
+        if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
@@ -145,52 +158,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 decode_tile(ctl->prefix, E, NB, tile, e, mb, nb);
                 const int row0 = ctl->offs[e] + mb * BM;
                 const int n0 = nb * BNo;
-                int gi[4] = {0, 0, 0, 0};
-                if (kGatherA) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int r = row0 + lane * 4 + q;  // rows past the data read row 0
-                        int v = r < a_total ? a_rows[r] : 0;
-                        gi[q] = (unsigned)v < (unsigned)a_src_rows ? v : 0;
-                    }
-                }
                 for (int kb = 0; kb < KB; ++kb) {
-                    int go = 1;
-                    if (lane == 0)
-                        go = wait_bar(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag, err);
-                    if (kGatherA) go = __shfl_sync(0xffffffffu, go, 0);
-                    if (!go) {
+                    if (!wait_bar(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag, err)) {
                         ok = false;
                         break;
                     }
                     const uint32_t full = smem_u32(&ctl->full[stage]);
                     const uint32_t a_s = tiles_addr + stage * STAGE_BYTES;
                     const uint32_t b_s = a_s + A_BYTES;
-                    if (lane == 0) {
-                        mbar_expect_tx(full, STAGE_BYTES);
-                        armed |= 1u << stage;
-                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-                        if (kSwiGLU) {
-                            tma_load_3d(b_s, &tmB0, full, kb * BK, n0, e);
-                            tma_load_3d(b_s + B_BYTES / 2, &tmB1, full, kb * BK, n0, e);
-                        } else {
-                            tma_load_3d(b_s, &tmB0, full, kb * BK, n0, e);
-                        }
-                    }
-                    if (kGatherA) {
-                        __syncwarp();
-                        tma_gather4(a_s + lane * 4 * 128, &tmA, full, kb * BK, gi[0], gi[1], gi[2],
-                                    gi[3]);
+                    mbar_expect_tx(full, kGather ? B_BYTES : STAGE_BYTES);
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    if (kSwiGLU) {
+                        tma_load_3d(b_s, &tmB0, full, kb * BK, n0, e);
+                        tma_load_3d(b_s + B_BYTES / 2, &tmB1, full, kb * BK, n0, e);
                     } else {
-                        tma_load_2d(a_s, &tmA, full, kb * BK, row0);
+                        tma_load_3d(b_s, &tmB0, full, kb * BK, n0, e);
                     }
+                    if (!kGather) tma_load_2d(a_s, &tmA, full, kb * BK, row0);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            if (lane == 0 && *abort_flag) {
+            if (*abort_flag) {
                 // let every copy still in flight land before the CTA exits
                 for (int s = 0; s < kStages; ++s)
                     if ((armed >> s) & 1u)
@@ -216,6 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
+                    // A rows written through the generic proxy (cp.async) are
+                    // read by the MMA through the async proxy
+                    if (kGather) fence_async_shared();
                     const uint32_t a_s = tiles_addr + stage * STAGE_BYTES;
                     const uint64_t ad = sw128_desc(a_s);
                     const uint64_t bd = sw128_desc(a_s + A_BYTES);
@@ -242,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(smem_u32(&ctl->done));
             wait_bar_drain(smem_u32(&ctl->done), 0);
         }
-    } else {
+    } else if (warp < 2 + kEpilogueWarps) {
         // ---------------- epilogue: TMEM -> registers -> smem -> global ----------------
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         uint8_t* stage = stage_area + (size_t)(warp - 2) * kStageWarpBytes;
@@ -336,6 +331,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
+    } else if (kGather) {
+        // ---------------- gather warps (kGather): A rows by cp.async ----------------
+        // Instruction i of a stage covers rows 16i + 4g .. 16i + 4g + 3 (g = gather
+        // warp); 8 lanes copy the 8 16-byte chunks of one row's 128-byte k-block,
+        // so every instruction reads 4 whole 128-byte lines.
+        const int g = warp - 2 - kEpilogueWarps;
+        const int chunk = lane & 7;
+        const int rsub = g * 4 + (lane >> 3);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+            int e, mb, nb;
+            decode_tile(ctl->prefix, E, NB, tile, e, mb, nb);
+            const int row0 = ctl->offs[e] + mb * BM;
+            const uint16_t* src[BM / 16];
+#pragma unroll
+            for (int i = 0; i < BM / 16; ++i) {
+                const int r = row0 + i * 16 + rsub;  // rows past the data read row 0
+                const int v = r < a_total ? a_rows[r] : 0;
+                src[i] = a_src + (size_t)((unsigned)v < (unsigned)a_src_rows ? v : 0) * K;
+            }
+            for (int kb = 0; kb < KB; ++kb) {
+                int go = 1;
+                if (lane == 0)
+                    go = wait_bar(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag, err);
+                go = __shfl_sync(0xffffffffu, go, 0);
+                if (!go) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t a_s = tiles_addr + stage * STAGE_BYTES;
+                const int col = kb * BK + chunk * 8;
+                const bool in = col < K;  // K % 8 == 0: a chunk is wholly in or out
+#pragma unroll
+                for (int i = 0; i < BM / 16; ++i) {
+                    const int r = i * 16 + rsub;
+                    cp_async_16(a_s + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + (in ? col : 0),
+                                in ? 16u : 0u);
+                }
+                cp_async_arrive_noinc(smem_u32(&ctl->full[stage]));
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        // no copy may land after the CTA has gone
+        cp_async_wait_all();
     }
 
     tc_fence_before();
@@ -460,7 +504,11 @@ moe_status launch_gate_up(const uint16_t* rows, const GemmGroup& g, int H, int I
                           const int32_t* gather, long long src_rows) {
     if (g.R == 0) return MOE_OK;
     CUtensorMap a, bg, bu, o;
-    const bool ok_a = gather ? map_2d(&a, rows, src_rows, H, 1) : map_2d(&a, rows, g.R, H, BM);
+    bool ok_a = true;
+    if (gather)
+        memset(&a, 0, sizeof(a));  // unused: the gather warps read `rows` directly
+    else
+        ok_a = map_2d(&a, rows, g.R, H, BM);
     if (!ok_a || !map_3d(&bg, wg, g.E, I, H, kMmaN / 2) ||
         !map_3d(&bu, wu, g.E, I, H, kMmaN / 2) || !map_2d(&o, h, g.R, I, 32))
         return MOE_ERR_UNSUPPORTED;
@@ -468,14 +516,15 @@ moe_status launch_gate_up(const uint16_t* rows, const GemmGroup& g, int H, int I
     int grid;
     const moe_status ss = schedule(g, (I + kMmaN / 2 - 1) / (kMmaN / 2), st, &grid);
     if (ss != MOE_OK) return ss;
+    __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(h);
     if (gather)
-        grouped_gemm_kernel<true, true><<<grid, kThreads, kSmemBytes, st>>>(
-            a, bg, bu, o, g.offsets, g.counts, g.prefix, g.E, H, I,
-            reinterpret_cast<__nv_bfloat16*>(h), g.err, gather, (int)g.R, (int)src_rows);
+        grouped_gemm_kernel<true, true><<<grid, threads_for(true), kSmemBytes, st>>>(
+            a, bg, bu, o, g.offsets, g.counts, g.prefix, g.E, H, I, hb, g.err, gather, (int)g.R,
+            (int)src_rows, rows);
     else
         grouped_gemm_kernel<true, false><<<grid, kThreads, kSmemBytes, st>>>(
-            a, bg, bu, o, g.offsets, g.counts, g.prefix, g.E, H, I,
-            reinterpret_cast<__nv_bfloat16*>(h), g.err, nullptr, 0, 0);
+            a, bg, bu, o, g.offsets, g.counts, g.prefix, g.E, H, I, hb, g.err, nullptr, 0, 0,
+            nullptr);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -492,7 +541,7 @@ moe_status launch_down(const uint16_t* h, const GemmGroup& g, int H, int I, cons
     if (ss != MOE_OK) return ss;
     grouped_gemm_kernel<false, false><<<grid, kThreads, kSmemBytes, st>>>(
         a, bd, bd, o, g.offsets, g.counts, g.prefix, g.E, I, H,
-        reinterpret_cast<__nv_bfloat16*>(y), g.err, nullptr, 0, 0);
+        reinterpret_cast<__nv_bfloat16*>(y), g.err, nullptr, 0, 0, nullptr);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -203,14 +203,16 @@ moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const mo
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (shape->N == 0) return MOE_OK;
     if (!xd || !w_gate || !w_up || !w_down || !h || !y) return MOE_ERR_INVALID_ARG;
-    if (shape->dedup && !xe) return MOE_ERR_INVALID_ARG;
-    const uint16_t* rows = xd;
+    (void)xe;
     if (shape->dedup) {
-        // materialised expansion: measured faster than gathering inside the GEMM
-        MOE_TRY(moe_expand(xd, layout, shape, xe, stream));
-        rows = xe;
+        // the expansion to expert-major order is done by the GEMM's gather
+        // warps: cheaper than writing the N*k rows out and reading them back
+        const int64_t rd_max = (int64_t)shape->N * (shape->k < shape->W ? shape->k : shape->W);
+        MOE_TRY(moe_ffn_gate_up_gather(xd, layout->expand_src, rd_max, layout, shape, w_gate,
+                                       w_up, h, ws, ws_bytes, stream));
+    } else {
+        MOE_TRY(moe_ffn_gate_up(xd, layout, shape, w_gate, w_up, h, ws, ws_bytes, stream));
     }
-    MOE_TRY(moe_ffn_gate_up(rows, layout, shape, w_gate, w_up, h, ws, ws_bytes, stream));
     return moe_ffn_down(h, layout, shape, w_down, y, ws, ws_bytes, stream);
 }
 
@@ -274,13 +276,28 @@ moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32
     if (!logits || !x || !w_gate || !w_up || !w_down || !topk_ids || !topk_w || !xd || !h ||
         !y || !out)
         return MOE_ERR_INVALID_ARG;
-    if (shape->dedup && (!xe || !partial)) return MOE_ERR_INVALID_ARG;
+    if (shape->dedup && !partial) return MOE_ERR_INVALID_ARG;
     MOE_TRY(moe_route(logits, shape, topk_ids, topk_w, stream));
     MOE_TRY(moe_dispatch_layout(topk_ids, placement, shape, layout, ws, ws_bytes, stream));
-    MOE_TRY(moe_dispatch(x, layout, shape, xd, stream));
-    MOE_TRY(moe_expert_ffn(xd, layout, shape, w_gate, w_up, w_down, xe, h, y, ws, ws_bytes,
-                           stream));
+    if (moe_layer_skips_dispatch(shape)) {
+        // the dispatch copy fused into the gate/up GEMM: rows of x through row_token
+        MOE_TRY(moe_ffn_gate_up_gather(x, layout->row_token, shape->N, layout, shape, w_gate,
+                                       w_up, h, ws, ws_bytes, stream));
+        MOE_TRY(moe_ffn_down(h, layout, shape, w_down, y, ws, ws_bytes, stream));
+    } else {
+        MOE_TRY(moe_dispatch(x, layout, shape, xd, stream));
+        MOE_TRY(moe_expert_ffn(xd, layout, shape, w_gate, w_up, w_down, xe, h, y, ws, ws_bytes,
+                               stream));
+    }
     return moe_combine(y, topk_w, layout, shape, partial, residual, out, stream);
+}
+
+int32_t moe_layer_skips_dispatch(const moe_shape* shape) {
+    if (!shape || check_shape(shape) != MOE_OK || shape->dedup) return 0;
+    // plain rows are gathered when the single-CTA GEMM runs (the weight-streaming
+    // regime, where fusing the copy saves its HBM traffic); the CTA-pair kernel
+    // has no gather mode
+    return use_pair((long long)shape->N * shape->k, shape->E) ? 0 : 1;
 }
 
 moe_status moe_coselection(const int32_t* topk_ids, const moe_shape* shape, int32_t* coselect,

@@ -93,7 +93,7 @@ struct GemmGroup {
 // Return MOE_OK, or an error status when a host-side step (tensor-map
 // encoding, launch) failed.
 // gather != nullptr: problem row i is row gather[i] of `rows` ([src_rows, H]),
-// fetched by the GEMM's producer (tile::gather4) instead of a prior copy.
+// copied into shared memory by the GEMM's gather warps instead of a prior copy.
 moe_status launch_gate_up(const uint16_t* rows, const GemmGroup& g, int H, int I,
                           const uint16_t* wg, const uint16_t* wu, uint16_t* h, cudaStream_t st,
                           const int32_t* gather = nullptr, long long src_rows = 0);

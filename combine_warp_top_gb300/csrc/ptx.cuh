@@ -1,5 +1,5 @@
-// Inline-PTX wrappers for the tensor-core kernels: mbarriers, TMA (tiled,
-// gather4, stores, bulk groups), tcgen05 (TMEM allocation, MMA, commit, loads)
+// Inline-PTX wrappers for the tensor-core kernels: mbarriers, TMA (tiled
+// loads, stores, bulk groups), 16-byte cp.async, tcgen05 (TMEM allocation, MMA, commit, loads)
 // and the shared-memory matrix and instruction descriptors.  Shared by the
 // single-CTA and the CTA-pair grouped GEMMs.
 #pragma once
@@ -111,14 +111,20 @@ __device__ __forceinline__ void fence_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Four rows (r0..r3) x 64 columns of a 2-D map whose box is one row high.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int r0, int r1, int r2, int r3) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-        : "memory");
+// 16-byte asynchronous copy global -> shared, cached in L2 only; with
+// src_bytes = 0 nothing is read and the 16 bytes are zero-filled.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+// One arrival on `bar` (counted in its expected arrivals) once every cp.async
+// this thread has issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {

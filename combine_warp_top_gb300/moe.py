@@ -67,6 +67,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_layer_forward": (I32, [P, P, P, P, P, P, P, shp, P, P, lay, P, P, P, P, P, P, P, S,
                                     P]),
         "moe_dispatch_layout_noalloc": (I32, [P, P, shp, lay, P]),
+        "moe_layer_skips_dispatch": (ctypes.c_int32, [shp]),
         "moe_coselection": (I32, [P, shp, P, P, S, P]),
         "moe_shared_expert_ffn": (I32, [P, shp, ctypes.c_int32, P, P, P, P, P, P, S, P]),
         "moe_combine_shared": (I32, [P, P, lay, shp, P, P, P, P, P]),
@@ -229,6 +230,12 @@ def moe_ffn_gate_up_gather(src, row_index, layout: Layout, shape: Shape, w_gate,
                                          _stream(stream)), "moe_ffn_gate_up_gather")
 
 
+def moe_layer_skips_dispatch(shape: Shape) -> bool:
+    """True when the layer gathers its plain rows inside the gate/up GEMM
+    (no moe_dispatch copy) for this shape."""
+    return bool(load().moe_layer_skips_dispatch(ctypes.byref(shape.c())))
+
+
 def moe_ffn_down(h, layout: Layout, shape: Shape, w_down, y, ws, stream=None):
     _check(load().moe_ffn_down(_ptr(h), ctypes.byref(layout.c), ctypes.byref(shape.c()),
                                _ptr(w_down), _ptr(y), _ptr(ws), ws.numel(), _stream(stream)),
@@ -325,8 +332,10 @@ class MoELayer:
         self.topk_w = torch.empty(max(N * k, 1), dtype=torch.float32, device=device)
         self.layout = Layout(shape, device)
         rows_d = shape.R_d_max if shape.dedup else shape.R
-        self.xd = torch.empty(max(rows_d, 1), H, **bf)
-        self.xe = torch.empty(max(shape.R, 1), H, **bf) if shape.dedup else None
+        # plain rows gathered inside the gate/up GEMM need no dispatch buffer
+        self.fused_dispatch = moe_layer_skips_dispatch(shape)
+        self.xd = torch.empty(1 if self.fused_dispatch else max(rows_d, 1), H, **bf)
+        self.xe = None  # the dedup expansion happens inside the gate/up GEMM
         self.h = torch.empty(max(shape.R, 1), I, **bf)
         self.y = torch.empty(max(shape.R, 1), H, **bf)
         self.partial = torch.empty(max(shape.R_d_max, 1), H, **bf) if shape.dedup else None
@@ -356,7 +365,15 @@ class MoELayer:
             self.forward(logits, x, residual, out)
         return g
 
-    STAGES = ("route", "layout", "dispatch", "expand", "gate_up", "down", "shared", "combine")
+    STAGES = ("route", "layout", "dispatch", "gate_up", "down", "shared", "combine")
+
+    def stage_names(self):
+        """The stages forward_stages() runs for this layer, in order: no
+        separate dispatch when the gate/up GEMM gathers the plain rows from x,
+        no shared expert unless one is set."""
+        return [n for n in self.STAGES
+                if (n != "dispatch" or not self.fused_dispatch)
+                and (n != "shared" or self.shared is not None)]
 
     def forward_stages(self, logits, x, residual=None, out=None, stream=None, events=None):
         """The same kernels as forward(), one C call per stage of the pages'
@@ -376,17 +393,12 @@ class MoELayer:
         rec("layout", 0)
         moe_dispatch_layout(self.topk_ids, self.placement, s, self.layout, self.ws, st)
         rec("layout", 1)
-        rec("dispatch", 0)
-        moe_dispatch(x, self.layout, s, self.xd, st)
-        rec("dispatch", 1)
-        rows = self.xd
-        if s.dedup:
-            rec("expand", 0)
-            moe_expand(self.xd, self.layout, s, self.xe, st)
-            rec("expand", 1)
-            rows = self.xe
+        if not self.fused_dispatch:
+            rec("dispatch", 0)
+            moe_dispatch(x, self.layout, s, self.xd, st)
+            rec("dispatch", 1)
         rec("gate_up", 0)
-        moe_ffn_gate_up(rows, self.layout, s, self.w_gate, self.w_up, self.h, self.ws, st)
+        self._gate_up(x, st)
         rec("gate_up", 1)
         rec("down", 0)
         moe_ffn_down(self.h, self.layout, s, self.w_down, self.y, self.ws, st)
@@ -404,15 +416,30 @@ class MoELayer:
         rec("combine", 1)
         return out
 
+    def _gate_up(self, x, st):
+        """The gate/up stage as moe_layer_forward runs it: dedup rows expanded
+        by the GEMM's gather warps; plain rows gathered from x when the
+        dispatch is fused, else read from the dispatched rows."""
+        s, lay = self.shape, self.layout
+        if s.dedup:
+            moe_ffn_gate_up_gather(self.xd, lay["expand_src"], lay, s, self.w_gate, self.w_up,
+                                   self.h, self.ws, st)
+        elif self.fused_dispatch:
+            moe_ffn_gate_up_gather(x, lay["row_token"], lay, s, self.w_gate, self.w_up, self.h,
+                                   self.ws, st)
+        else:
+            moe_ffn_gate_up(self.xd, lay, s, self.w_gate, self.w_up, self.h, self.ws, st)
+
     def kernel_launches_per_step(self) -> int:
         """Kernels of this library launched by one forward (route 1, layout 3,
-        dispatch 1, expand 1 with dedup, each GEMM 2 with its schedule, combine
-        1 or 2 with dedup, shared expert 5)."""
+        dispatch 1 unless fused into the gate/up GEMM, each GEMM 2 with its
+        schedule, combine 1 or 2 with dedup, shared expert 5)."""
         s = self.shape
         if s.N == 0:
             return 0
         shared = 5 if self.shared is not None else 0  # dense segment + 2 x (schedule + GEMM)
-        return 1 + 3 + 1 + (1 if s.dedup else 0) + 2 + 2 + (2 if s.dedup else 1) + shared
+        dispatch = 0 if self.fused_dispatch else 1
+        return 1 + 3 + dispatch + 2 + 2 + (2 if s.dedup else 1) + shared
 
     def forward_host(self, logits_h, x_h, residual_h, out_h, dev_inputs=None, stream=None):
         """Whole layer from host buffers: copy the step's inputs host->device,
@@ -565,17 +592,22 @@ class MicrobatchPipeline:
             # vector-unit stages of microbatch m
             moe_route(logits[t0:t1], sm, L.topk_ids, L.topk_w, vec)
             moe_dispatch_layout(L.topk_ids, self.placement, sm, L.layout, L.ws, vec)
-            moe_dispatch(x[t0:t1], L.layout, sm, L.xd, vec)
-            rows = L.xd
-            if s.dedup:
-                moe_expand(L.xd, L.layout, sm, L.xe, vec)
-                rows = L.xe
+            fused = moe_layer_skips_dispatch(sm)
+            if not fused:
+                moe_dispatch(x[t0:t1], L.layout, sm, L.xd, vec)
             a_done[m].record(vec)
             # tensor-core stages of microbatch m
             mat.wait_event(a_done[m])
             if gemm_events is not None:
                 gemm_events[m][0].record(mat)
-            moe_ffn_gate_up(rows, L.layout, sm, self.w[0], self.w[1], L.h, L.ws, mat)
+            if s.dedup:
+                moe_ffn_gate_up_gather(L.xd, L.layout["expand_src"], L.layout, sm, self.w[0],
+                                       self.w[1], L.h, L.ws, mat)
+            elif fused:
+                moe_ffn_gate_up_gather(x[t0:t1], L.layout["row_token"], L.layout, sm, self.w[0],
+                                       self.w[1], L.h, L.ws, mat)
+            else:
+                moe_ffn_gate_up(L.xd, L.layout, sm, self.w[0], self.w[1], L.h, L.ws, mat)
             if gemm_events is not None:
                 gemm_events[m][1].record(mat)
             moe_ffn_down(L.h, L.layout, sm, self.w[2], L.y, L.ws, mat)
@@ -596,4 +628,11 @@ class MicrobatchPipeline:
             L.check_device_errors()
 
     def kernel_launches_per_step(self) -> int:
-        return sum(self.sets[0].kernel_launches_per_step() for _ in self.chunks())
+        total = 0
+        for t0, t1 in self.chunks():
+            s = self.shape
+            sub = Shape(t1 - t0, s.H, s.E, s.k, s.W, s.I, s.dedup)
+            dispatch = 0 if moe_layer_skips_dispatch(sub) else 1
+            total += 1 + 3 + dispatch + 2 + 2 + (2 if s.dedup else 1) + (
+                5 if self.shared is not None else 0)
+        return total

@@ -144,20 +144,25 @@ moe_status moe_dispatch(const uint16_t* x, const moe_layout* layout, const moe_s
  *   y[i, :] = bf16( h[i, :] Wd[e]^T )                          bf16 [N*k, H]
  * with fp32 accumulation on the tensor cores.  Weights in nn.Linear layout:
  * w_gate, w_up bf16 [E, I, H]; w_down bf16 [E, H, I].
- * Plain: xd holds the expert-major rows [N*k, H] and xe is ignored (may be NULL).
- * Dedup: xd holds the dedup rows; they are first expanded into expert-major
- *        order in xe bf16 [N*k, H] (the receiver's "group" step).
+ * Plain: xd holds the expert-major rows [N*k, H].
+ * Dedup: xd holds the dedup rows; the gate/up GEMM reads them in expert-major
+ *        order through layout->expand_src (the receiver's "group" step, done
+ *        by the GEMM's gather warps instead of a copy into xe).
+ * xe is not used and may be NULL (kept so that callers of the materialised
+ * form, moe_expand + moe_ffn_gate_up, can share one buffer set).
  * ws: workspace of moe_workspace_bytes(shape) bytes. */
 moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const moe_shape* shape,
                           const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
                           uint16_t* xe, uint16_t* h, uint16_t* y, void* ws, size_t ws_bytes,
                           void* stream);
 
-/* The three steps of moe_expert_ffn as separate calls (kernel-fusion page,
+/* The steps of moe_expert_ffn as separate calls (kernel-fusion page,
  * "Fusing the layer into one kernel": stage 3 "group", stages 4-5 "MatMul" +
  * "SwiGLU", stage 6 "MatMul").  moe_expert_ffn is exactly
- *   [dedup: moe_expand(xd -> xe)]; moe_ffn_gate_up(rows -> h); moe_ffn_down(h -> y)
- * on one stream.
+ *   plain: moe_ffn_gate_up(xd -> h); moe_ffn_down(h -> y)
+ *   dedup: moe_ffn_gate_up_gather(xd, expand_src -> h); moe_ffn_down(h -> y)
+ * on one stream, and its h equals, bit for bit, that of the materialised form
+ *   moe_expand(xd -> xe); moe_ffn_gate_up(xe -> h).
  * moe_expand:      xe[i, :] = xd[expand_src[i], :] for the N*k expert-major rows
  *                  (dedup only; bit-exact copies).  Returns MOE_ERR_INVALID_ARG
  *                  when shape->dedup == 0.
@@ -180,11 +185,9 @@ moe_status moe_ffn_down(const uint16_t* h, const moe_layout* layout, const moe_s
  * src bf16 [src_rows, H].  With src = the dedup rows and row_index =
  * layout->expand_src this is the dedup expansion; with src = x and row_index
  * = layout->row_token it is the plain dispatch.  Out-of-range indices read
- * row 0.  Results are bit-identical to materialising the rows first.  The
- * producer issues one 4-row TMA gather per lane and stage; on GB300 this is
- * about 3x slower than the 2-D box load of materialised rows for these
- * GEMMs (the gather re-runs for every 64-column k-block), so moe_expert_ffn
- * keeps the materialised expansion. */
+ * row 0.  Results are bit-identical to materialising the rows first.  Four
+ * extra warps of the (single-CTA) GEMM copy the rows' 128-byte k-blocks with
+ * 16-byte cp.async into the swizzled operand tiles; src_rows < 2^31. */
 moe_status moe_ffn_gate_up_gather(const uint16_t* src, const int32_t* row_index, int64_t src_rows,
                                   const moe_layout* layout, const moe_shape* shape,
                                   const uint16_t* w_gate, const uint16_t* w_up, uint16_t* h,
@@ -231,7 +234,10 @@ moe_status moe_combine_shared(const uint16_t* y, const float* topk_w, const moe_
 
 /* The whole layer in order on one stream: moe_route, moe_dispatch_layout,
  * moe_dispatch, moe_expert_ffn, moe_combine, with the buffers documented for
- * each of them. */
+ * each of them -- except that, in the plain form, when
+ * moe_layer_skips_dispatch(shape) is 1 the dispatch copy is fused into the
+ * gate/up GEMM (moe_ffn_gate_up_gather(x, row_token)) and xd is not written.
+ * xe is not used (may be NULL). */
 moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32_t* placement,
                              const uint16_t* w_gate, const uint16_t* w_up,
                              const uint16_t* w_down, const uint16_t* residual,
@@ -239,6 +245,12 @@ moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32
                              const moe_layout* layout, uint16_t* xd, uint16_t* xe, uint16_t* h,
                              uint16_t* y, uint16_t* partial, uint16_t* out, void* ws,
                              size_t ws_bytes, void* stream);
+
+/* 1 when moe_layer_forward, for this shape, gathers the plain rows inside the
+ * gate/up GEMM instead of running moe_dispatch first; 0 otherwise (dedup
+ * form, or a shape whose GEMMs run on the CTA-pair kernel, which has no
+ * gather mode).  Lets a caller that runs the stages itself do the same. */
+int32_t moe_layer_skips_dispatch(const moe_shape* shape);
 
 /* Co-selection counts of "Expert Coupling" Sec. V-A / Appendix A-D Algorithm 1:
  * coselect[e*E + e'] = number of tokens whose topk_ids contain both e and e'

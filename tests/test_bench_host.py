@@ -53,6 +53,10 @@ def test_algorithmic_bytes_of_the_deepseek_layer():
     assert alg["gate_up"]["bytes"] == 2 * 256 * 2048 * 7168 * 2 + 32768 * 7168 * 2 + 32768 * 2048 * 2
     assert alg["gate_up"]["flops"] == 4 * 32768 * 7168 * 2048
     assert alg["dispatch"]["bytes"] == 4096 * 7168 * 2 * (1 + 8)
+    # with the dispatch fused into it, gate/up reads each token row of x once
+    fused = bench.algorithmic(wl, R_d=0, fused_dispatch=True)
+    assert fused["gate_up"]["bytes"] == (2 * 256 * 2048 * 7168 * 2 + 4096 * 7168 * 2 +
+                                         32768 * 2048 * 2)
 
 
 def test_workload_overrides():

@@ -30,18 +30,19 @@ def run_ffn(wl, dedup, ids=None, placement=None):
     moe.moe_dispatch(dev_bf16(x), lay, shape, xd)
     h = torch.empty(shape.R, wl.I, dtype=torch.bfloat16, device="cuda")
     y = torch.empty(shape.R, wl.H, dtype=torch.bfloat16, device="cuda")
-    xe = torch.empty(shape.R, wl.H, dtype=torch.bfloat16, device="cuda") if dedup else None
-    moe.moe_expert_ffn(xd, lay, shape, dev_bf16(wg), dev_bf16(wu), dev_bf16(wd), xe, h, y, ws)
+    moe.moe_expert_ffn(xd, lay, shape, dev_bf16(wg), dev_bf16(wu), dev_bf16(wd), None, h, y, ws)
     torch.cuda.synchronize()
     assert moe.moe_get_error(ws) == 0
     xe_ref = oracle.dispatch(x, ref["row_token"])
     if dedup:
-        assert np.array_equal(host_u16(xe), xe_ref)
-        # the same rows gathered inside the GEMM give the same h, bit for bit
+        # the materialised expansion is a bit-exact copy, and the expansion
+        # done by the GEMM's gather warps (moe_expert_ffn) gives the same h
+        xe = torch.empty(shape.R, wl.H, dtype=torch.bfloat16, device="cuda")
+        moe.moe_expand(xd, lay, shape, xe)
         h2 = torch.empty_like(h)
-        moe.moe_ffn_gate_up_gather(xd, lay["expand_src"], lay, shape, dev_bf16(wg), dev_bf16(wu),
-                                   h2, ws)
+        moe.moe_ffn_gate_up(xe, lay, shape, dev_bf16(wg), dev_bf16(wu), h2, ws)
         torch.cuda.synchronize()
+        assert np.array_equal(host_u16(xe), xe_ref)
         assert torch.equal(h.view(torch.int16), h2.view(torch.int16))
     h_ref, y_ref = oracle.expert_ffn(xe_ref, ref["expert_offsets"], ref["expert_counts"], wg, wu, wd)
     return host_f64(h), host_f64(y), h_ref, y_ref

@@ -75,12 +75,16 @@ def test_full_size_workload(name):
         rows = rng.choice(Rd, size=min(512, Rd), replace=False)
         xd = layer.xd[torch.from_numpy(rows).cuda()]
         assert np.array_equal(host_u16(xd), x[ref["dedup_row_token"][rows]])
-        rows = rng.choice(N * k, size=512, replace=False)
-        xe = layer.xe[torch.from_numpy(rows).cuda()]
-        assert np.array_equal(host_u16(xe), x[ref["row_token"][rows]])
     else:
+        xd_buf = layer.xd
+        if layer.fused_dispatch:
+            # the layer gathered its rows inside the GEMM; the dispatch kernel
+            # itself is checked at this size on its own buffer
+            xd_buf = torch.empty(N * k, wl.H, dtype=torch.bfloat16, device="cuda")
+            moe.moe_dispatch(bf16_host(x).cuda(), layer.layout, layer.shape, xd_buf)
+            torch.cuda.synchronize()
         rows = rng.choice(N * k, size=512, replace=False)
-        xd = layer.xd[torch.from_numpy(rows).cuda()]
+        xd = xd_buf[torch.from_numpy(rows).cuda()]
         assert np.array_equal(host_u16(xd), x[ref["row_token"][rows]])
     # float outputs on sampled tokens (the first, the last and random ones)
     n = SAMPLES[wl.name]

@@ -81,3 +81,41 @@ def test_pair_layer_with_shared_expert(dedup, monkeypatch):
     layer.check_device_errors()
     ref = oracle.layer_forward(L, x, *w, wl.k, wl.W, residual=res, dedup=dedup, shared=sh)
     assert_close(host_f64(out), ref["out"], "out")
+
+
+@pytest.mark.parametrize("dedup", [False, True])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "wide", "odd_h", "deep_k", "e256"])
+def test_gathered_rows_equal_dispatched_rows(name, dedup, monkeypatch):
+    """Both kernels fed by their gather warps (rows of x through row_token, or
+    of the dedup rows through expand_src) give bit for bit the h of the same
+    kernel fed by materialised rows: the gather changes only how A reaches
+    shared memory."""
+    wl = SMALL[name]
+    ids, _ = oracle.route(synth.make_logits(wl), wl.k)
+    x = dev_bf16(synth.make_x(wl))
+    wg, wu = dev_bf16(synth.make_weight(wl, "gate")), dev_bf16(synth.make_weight(wl, "up"))
+    shape = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=dedup)
+    lay = moe.Layout(shape)
+    ws = moe.workspace(shape)
+    moe.moe_dispatch_layout(dev_i32(ids), None, shape, lay, ws)
+    xd = torch.empty(shape.R_d_max if dedup else shape.R, wl.H, dtype=torch.bfloat16,
+                     device="cuda")
+    moe.moe_dispatch(x, lay, shape, xd)
+    if dedup:
+        rows = torch.empty(shape.R, wl.H, dtype=torch.bfloat16, device="cuda")
+        moe.moe_expand(xd, lay, shape, rows)
+        src, index = xd, lay["expand_src"]
+    else:
+        rows, src, index = xd, x, lay["row_token"]
+    outs = {}
+    for pair in ("0", "1"):
+        monkeypatch.setenv("MOE_GEMM_PAIR", pair)
+        h_rows = torch.empty(shape.R, wl.I, dtype=torch.bfloat16, device="cuda")
+        h_gather = torch.empty_like(h_rows)
+        moe.moe_ffn_gate_up(rows, lay, shape, wg, wu, h_rows, ws)
+        moe.moe_ffn_gate_up_gather(src, index, lay, shape, wg, wu, h_gather, ws)
+        torch.cuda.synchronize()
+        assert moe.moe_get_error(ws) == 0
+        assert torch.equal(h_rows.view(torch.int16), h_gather.view(torch.int16)), pair
+        outs[pair] = h_gather
+    assert torch.equal(outs["0"].view(torch.int16), outs["1"].view(torch.int16))
