@@ -12,7 +12,10 @@
 //
 // One warp per output row.  Each lane owns U 16-byte chunks (8 bf16 each) per
 // step along the row; the source rows of a chunk are loaded together, then
-// accumulated in fp32 in j order.
+// accumulated in fp32 in j order.  These are latency-bound chains of loads:
+// the dedup kernels are compiled for at least 3 resident blocks per SM (a
+// register cap that keeps 24 warps per SM in flight), except the owner sum
+// with four chunks per lane, which would spill under that cap and gets 2.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -170,7 +173,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
 // Dedup, expert-rank side: partial[d] = bf16(sum over the j of token t carried
 // by dedup row d of w[t,j] * y[pair_row[t,j]]), j ascending.
 template <int U>
-__global__ void __launch_bounds__(kThreads) rank_reduce_kernel(
+__global__ void __launch_bounds__(kThreads, 3) rank_reduce_kernel(
     const uint4* __restrict__ y, const float* __restrict__ topk_w,
     const int32_t* __restrict__ pair_row, const int32_t* __restrict__ pair_dedup_row,
     const int32_t* __restrict__ dedup_row_token, const int32_t* __restrict__ n_dedup_rows, int N,
@@ -195,7 +198,7 @@ __global__ void __launch_bounds__(kThreads) rank_reduce_kernel(
 // Dedup, owner side: out[t] = bf16(residual[t] + sum of the token's partial
 // rows in ascending rank order).
 template <int U>
-__global__ void __launch_bounds__(kThreads) owner_sum_kernel(
+__global__ void __launch_bounds__(kThreads, U == 4 ? 2 : 3) owner_sum_kernel(
     const uint4* __restrict__ partial, const int32_t* __restrict__ pair_dedup_row, int N, int C,
     int k, int Rd_bound, const uint4* shared, const uint4* residual, uint4* out) {
     const int lane = threadIdx.x & 31;

@@ -146,11 +146,21 @@ def test_dispatch_bit_exact(name, dedup):
         assert np.array_equal(got, oracle.dispatch(x, ref["row_token"]))
 
 
+# long rows whose last step along the row is ragged: H = 2056 (257 16-byte
+# chunks) with k = 5 (one chunk per lane per step: 9 steps, the last 1 chunk),
+# H = 1032 (129 chunks) with k = 2 (four chunks per lane: 2 steps, the last 1)
+LONG_ROWS = {
+    "long_k5": synth.Workload("long_k5", 40, 2056, 10, 5, 128, 2),
+    "long_k2": synth.Workload("long_k2", 30, 1032, 8, 2, 128, 4),
+}
+
+
 @pytest.mark.parametrize("dedup", [False, True])
 @pytest.mark.parametrize("residual", [True, False])
-@pytest.mark.parametrize("name", ["tiny", "ragged", "wide", "k_eq_e", "one_rank", "e256"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "wide", "k_eq_e", "one_rank", "e256",
+                                  "long_k5", "long_k2"])
 def test_combine_matches_oracle(name, dedup, residual):
-    wl = SMALL[name]
+    wl = {**SMALL, **LONG_ROWS}[name]
     L = synth.make_logits(wl)
     ids, w64 = oracle.route(L, wl.k)
     shape = shape_of(wl, dedup)
