@@ -7,8 +7,10 @@
 //
 // One warp per token.  Lane l holds logits l, l+32, l+64, ... (coalesced
 // 128-byte loads).  k rounds of a warp arg-max pick the experts in descending
-// order; ties go to the lower expert index.  Lane j keeps the j-th pick, so
-// the k results are written with one coalesced store per array.
+// order; ties go to the lower expert index.  Each round compares order-
+// preserving integer keys with the warp-wide redux max / min instructions.
+// Lane j keeps the j-th pick, so the k results are written with one coalesced
+// store per array.
 #include <math.h>
 
 #include "moe_internal.cuh"
@@ -16,11 +18,44 @@
 namespace moe {
 namespace {
 
-// a beats b: larger value, or equal value and lower index (idx < 0 = empty).
-__device__ __forceinline__ bool beats(float av, int ai, float bv, int bi) {
-    if (ai < 0) return false;
-    if (bi < 0) return true;
-    return av > bv || (av == bv && ai < bi);
+// Order-preserving map of a finite float to uint32: a < b as floats iff
+// key(a) < key(b).  -0.0 is folded into +0.0 so that the two tie (and the
+// lower index wins, as for any tie).  Every key is at least 0x007FFFFF (the
+// key of -inf), so 0 marks an empty slot.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t b = __float_as_uint(f == 0.f ? 0.f : f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// One round of the warp's selection: the largest key over every lane's slots,
+// ties to the lowest expert index (slot * 32 + lane); the winning slot is
+// emptied.  Lane-local best first (strict '>' over ascending slots keeps the
+// lowest index), then one warp max and one warp min (redux) instead of a
+// shuffle tree.  Requires at least one non-empty slot in the warp.
+template <int VPL>
+__device__ __forceinline__ int take_max(uint32_t (&key)[VPL], int lane, uint32_t& won) {
+    uint32_t best = 0;
+    int bslot = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        if (key[i] > best) {
+            best = key[i];
+            bslot = i;
+        }
+    }
+    const uint32_t m = __reduce_max_sync(0xffffffffu, best);
+    const uint32_t cand = best == m ? (uint32_t)(bslot * 32 + lane) : 0xffffffffu;
+    const uint32_t idx = __reduce_min_sync(0xffffffffu, cand);
+    if ((int)(idx & 31u) == lane) {
+#pragma unroll
+        for (int i = 0; i < VPL; ++i)
+            if (i == (int)(idx >> 5)) key[i] = 0;
+    }
+    won = m;
+    return (int)idx;
 }
 
 // kRenorm: weights are a softmax over the k selected logits; otherwise the
@@ -35,46 +70,23 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
     const float* row = logits + (size_t)t * E;
 
     float v[VPL];
-    uint32_t taken = 0;  // bit i: slot i of this lane is used up or past E
+    uint32_t key[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
         const int e = i * 32 + lane;
-        if (e < E) {
-            v[i] = __ldg(row + e);
-        } else {
-            v[i] = 0.f;
-            taken |= 1u << i;
-        }
+        v[i] = e < E ? __ldg(row + e) : 0.f;
+        key[i] = e < E ? order_key(v[i]) : 0u;
     }
 
+    // k <= E: every round finds a non-empty slot
     int my_id = -1;
     float my_val = 0.f;
     for (int j = 0; j < k; ++j) {
-        float bv = 0.f;
-        int bi = -1;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            // slots are visited in ascending expert index, so a strict '>' keeps
-            // the lower index on ties
-            if (!((taken >> i) & 1u) && (bi < 0 || v[i] > bv)) {
-                bv = v[i];
-                bi = i * 32 + lane;
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (beats(ov, oi, bv, bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        // k <= E guarantees bi >= 0 here
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        uint32_t m;
+        const int idx = take_max<VPL>(key, lane, m);
         if (lane == j) {
-            my_id = bi;
-            my_val = bv;
+            my_id = idx;
+            my_val = key_value(m);
         }
     }
 
@@ -111,48 +123,33 @@ __global__ void __launch_bounds__(256) route_sigmoid_kernel(const float* __restr
     const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
     if (t >= N) return;
     const float* row = logits + (size_t)t * E;
-    float v[VPL], sc[VPL];
-    uint32_t taken = 0;
+    float sc[VPL];
+    uint32_t key[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
         const int e = i * 32 + lane;
         if (e < E) {
             const double L = (double)__ldg(row + e);
             sc[i] = (float)(1.0 / (1.0 + exp(-L)));
-            v[i] = sc[i] + __ldg(bias + e);
+            key[i] = order_key(sc[i] + __ldg(bias + e));
         } else {
             sc[i] = 0.f;
-            v[i] = 0.f;
-            taken |= 1u << i;
+            key[i] = 0u;
         }
     }
     int my_id = -1;
     float my_s = 0.f;
     for (int j = 0; j < k; ++j) {
-        float bv = 0.f, bs = 0.f;
-        int bi = -1;
+        uint32_t m;
+        const int idx = take_max<VPL>(key, lane, m);
+        // the winner's score, from the lane that holds it
+        float s_slot = 0.f;
 #pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            if (!((taken >> i) & 1u) && (bi < 0 || v[i] > bv)) {
-                bv = v[i];
-                bs = sc[i];
-                bi = i * 32 + lane;
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (beats(ov, oi, bv, bi)) {
-                bv = ov;
-                bs = os;
-                bi = oi;
-            }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        for (int i = 0; i < VPL; ++i)
+            if (i == (idx >> 5)) s_slot = sc[i];
+        const float bs = __shfl_sync(0xffffffffu, s_slot, idx & 31);
         if (lane == j) {
-            my_id = bi;
+            my_id = idx;
             my_s = bs;
         }
     }

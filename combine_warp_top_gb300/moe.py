@@ -334,7 +334,8 @@ class MoELayer:
         rows_d = shape.R_d_max if shape.dedup else shape.R
         # plain rows gathered inside the gate/up GEMM need no dispatch buffer
         self.fused_dispatch = moe_layer_skips_dispatch(shape)
-        self.xd = torch.empty(1 if self.fused_dispatch else max(rows_d, 1), H, **bf)
+        self._xd_rows = max(rows_d, 1)
+        self.xd = torch.empty(1 if self.fused_dispatch else self._xd_rows, H, **bf)
         self.xe = None  # the dedup expansion happens inside the gate/up GEMM
         self.h = torch.empty(max(shape.R, 1), I, **bf)
         self.y = torch.empty(max(shape.R, 1), H, **bf)
@@ -342,8 +343,18 @@ class MoELayer:
         self.out = torch.empty(max(N, 1), H, **bf)
         self.ws = workspace(shape, device)
 
+    def refresh_form(self):
+        """Re-read which form the library runs for this shape (the GEMM
+        choice can be forced through MOE_GEMM_PAIR at any time) and give the
+        dispatch buffer its full size when the dispatch is no longer fused."""
+        self.fused_dispatch = moe_layer_skips_dispatch(self.shape)
+        if not self.fused_dispatch and self.xd.shape[0] < self._xd_rows:
+            self.xd = torch.empty(self._xd_rows, self.shape.H, dtype=torch.bfloat16,
+                                  device=self.xd.device)
+
     def forward(self, logits, x, residual=None, out=None, stream=None):
         out = self.out if out is None else out
+        self.refresh_form()
         if self.shared is not None:
             return self.forward_stages(logits, x, residual, out, stream)
         moe_layer_forward(logits, x, self.placement, self.w_gate, self.w_up, self.w_down,
@@ -382,6 +393,7 @@ class MoELayer:
         out = self.out if out is None else out
         st = torch.cuda.current_stream() if stream is None else stream
         s = self.shape
+        self.refresh_form()
 
         def rec(name, i):
             if events is not None and name in events:
@@ -592,6 +604,7 @@ class MicrobatchPipeline:
             # vector-unit stages of microbatch m
             moe_route(logits[t0:t1], sm, L.topk_ids, L.topk_w, vec)
             moe_dispatch_layout(L.topk_ids, self.placement, sm, L.layout, L.ws, vec)
+            L.refresh_form()
             fused = moe_layer_skips_dispatch(sm)
             if not fused:
                 moe_dispatch(x[t0:t1], L.layout, sm, L.xd, vec)

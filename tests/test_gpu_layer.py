@@ -9,7 +9,7 @@ import torch
 import oracle
 from cases import SMALL
 from combine_warp_top_gb300 import moe, synth
-from gpu_util import assert_close, dev_bf16, dev_i32, host_f64
+from gpu_util import assert_close, dev_bf16, dev_i32, host_f64, host_u16
 
 pytestmark = pytest.mark.gpu
 
@@ -190,3 +190,30 @@ def test_cuda_graph_replay_matches_eager(dedup):
         torch.cuda.synchronize()
         assert torch.equal(got.view(torch.int16), want.view(torch.int16))
     layer.check_device_errors()
+
+
+def test_fused_dispatch_and_staged_forms_agree(monkeypatch):
+    """On a shape whose plain dispatch is fused into the gate/up GEMM, the
+    layer gives bit for bit the output of the staged form (dispatch copy, then
+    the CTA-pair GEMMs forced), and switching form after the layer was built
+    gives the dispatch buffer its full size."""
+    wl = SMALL["wide"]
+    monkeypatch.setenv("MOE_GEMM_PAIR", "0")
+    layer, (wg, wu, wd) = build_layer(wl, False)
+    assert layer.fused_dispatch and moe.moe_layer_skips_dispatch(layer.shape)
+    assert layer.xd.shape[0] == 1
+    L = torch.from_numpy(synth.make_logits(wl)).cuda()
+    x, res = dev_bf16(synth.make_x(wl)), dev_bf16(synth.make_residual(wl))
+    fused = layer.forward(L, x, res).clone()
+    monkeypatch.setenv("MOE_GEMM_PAIR", "1")
+    assert not moe.moe_layer_skips_dispatch(layer.shape)
+    staged = layer.forward(L, x, res).clone()
+    torch.cuda.synchronize()
+    layer.check_device_errors()
+    assert layer.xd.shape[0] == layer.shape.R
+    # same K order in both GEMM kernels and the same combine: identical bits
+    assert torch.equal(fused.view(torch.int16), staged.view(torch.int16))
+    # and the dispatched rows the staged form wrote are the oracle's
+    ref = oracle.dispatch_layout(layer.topk_ids.view(wl.N, wl.k).cpu().numpy(),
+                                 np.arange(wl.E), wl.E, wl.W)
+    assert np.array_equal(host_u16(layer.xd), oracle.dispatch(synth.make_x(wl), ref["row_token"]))
