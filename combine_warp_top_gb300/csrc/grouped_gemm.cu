@@ -11,8 +11,10 @@
 //             up columns of the same rows, so the epilogue can apply
 //             h = SiLU(g) * u straight out of TMEM and store bf16 h.
 //   down:     a 128x256 tile of y = h Wd^T, stored as bf16.
-// Roles (192 threads): warp 0 issues TMA loads into a 4-stage shared-memory
-// ring (128B swizzle), warp 1 owns TMEM and issues tcgen05.mma from one thread
+// Roles (192 threads, 320 with gathered rows): warp 0 issues TMA loads into a
+// 4-stage shared-memory ring (128B swizzle; with gathered rows only B, while
+// warps 6-9 copy the A rows in with cp.async), warp 1 owns TMEM and issues
+// tcgen05.mma from one thread
 // (fp32 accumulators, two 256-column buffers so the epilogue of one tile
 // overlaps the main loop of the next), warps 2-5 read the accumulators back
 // with tcgen05.ld, stage 64 output columns of their 32 rows in shared memory
@@ -24,7 +26,6 @@
 // has in flight, frees TMEM and returns.
 #include <cudaTypedefs.h>
 
-#include <cstdlib>
 #include <cstring>
 
 #include "moe_internal.cuh"

@@ -540,8 +540,10 @@ class MicrobatchPipeline:
     route, dispatch and combine its neighbours; buffers are alive per pipeline
     slot, not per microbatch).
 
-    Two streams: `vec` runs route, layout, dispatch, expansion and combine;
-    `mat` runs the gate/up and down GEMMs (and the shared expert).  Microbatch
+    Two streams: `vec` runs route, layout, dispatch and combine; `mat` runs
+    the gate/up and down GEMMs (and the shared expert).  Where the layer
+    gathers rows inside the gate/up GEMM (dedup expansion, fused plain
+    dispatch), the microbatches do the same.  Microbatch
     m uses buffer set m % depth.  Enqueue order on `vec` is A0, A1, C0, A2, C1,
     ... so a set is overwritten only after its previous microbatch's combine
     (which itself waited for that microbatch's GEMMs).  The GEMM CTAs fill the
