@@ -50,6 +50,8 @@ def parse_args(argv=None):
                    help="add a shared expert of SwiGLU width I_S to every step")
     p.add_argument("--microbatch", type=int, default=0, metavar="T",
                    help="run the step as a two-stream pipeline of T-token microbatches")
+    p.add_argument("--fuse-combine", action="store_true",
+                   help="down GEMM with the combine in its epilogue (moe_ffn_down_combine)")
     p.add_argument("--eager", action="store_true",
                    help="launch every step from Python instead of replaying a captured CUDA graph")
     p.add_argument("--e2e-steps", type=int, default=None)
@@ -97,6 +99,10 @@ def algorithmic(wl, R_d, fused_dispatch=False):
         "down": dict(bytes=E * H * I * 2 + R * I * 2 + R * H * 2, flops=2 * R * H * I),
         "combine": dict(bytes=R * H * 2 + 2 * N * H * 2 + R * 8 +
                         (2 * R_d * H * 2 if wl.dedup else 0)),
+        # down GEMM with the combine in its epilogue: weights, h in, residual
+        # in, out; y never leaves the SM
+        "down_combine": dict(bytes=E * H * I * 2 + R * I * 2 + 2 * N * H * 2 + R * 8,
+                             flops=2 * R * H * I),
     }
     return st
 
@@ -371,7 +377,10 @@ def run_ours(args):
         shared = tuple(synth.normal_bf16_device(
             torch.empty(*shp, dtype=torch.bfloat16, device="cuda"), 0, stream_id, std=0.02)
             for stream_id, shp in ((103, (I_s, wl.H)), (104, (I_s, wl.H)), (105, (wl.H, I_s))))
-    layer = moe.MoELayer(shape, w_gate, w_up, w_down, placement_d, shared=shared)
+    if args.fuse_combine and (args.microbatch or args.shared_expert):
+        raise SystemExit("--fuse-combine runs the plain layer: no --microbatch, no --shared-expert")
+    layer = moe.MoELayer(shape, w_gate, w_up, w_down, placement_d, shared=shared,
+                         fuse_combine=args.fuse_combine)
 
     x_h = torch.from_numpy(synth.make_x(wl, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
     r_h = torch.from_numpy(synth.make_residual(wl, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -538,6 +547,7 @@ def run_ours(args):
         "config": {"workload": wl.name, "N": wl.N, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
                    "W": wl.W, "dedup": wl.dedup, "placement": wl.placement,
                    "shared_expert_I": args.shared_expert or None,
+                   "fused_combine": bool(args.fuse_combine),
                    "microbatch": args.microbatch or None,
                    "launch": "one CUDA graph of the K timed steps" if graph is not None
                              else "eager, one C call per stage",

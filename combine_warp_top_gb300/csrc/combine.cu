@@ -235,9 +235,35 @@ __global__ void __launch_bounds__(kThreads, U == 4 ? 2 : 3) owner_sum_kernel(
     }
 }
 
+// out = bf16(acc (+ residual)) for the fp32 accumulator of the combine fused
+// into the down GEMM; one thread per 8 elements, grid-stride.
+__global__ void __launch_bounds__(kThreads) acc_finish_kernel(const float4* __restrict__ acc,
+                                                              const uint4* residual, long long n8,
+                                                              uint4* out) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8;
+         i += (long long)gridDim.x * blockDim.x) {
+        const float4 a0 = acc[2 * i], a1 = acc[2 * i + 1];
+        float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        if (residual) add_bf16x8(a, residual[i]);
+        out[i] = pack_bf16x8(a);
+    }
+}
+
 inline int warps_grid(long long n) { return (int)((n + kThreads / 32 - 1) / (kThreads / 32)); }
 
 }  // namespace
+
+cudaError_t launch_acc_finish(const float* acc, const uint16_t* residual, int N, int H,
+                              uint16_t* out, cudaStream_t st) {
+    const long long n8 = (long long)N * (H / 8);
+    if (n8 == 0) return cudaSuccess;
+    long long blocks = (n8 + kThreads - 1) / kThreads;
+    const long long cap = (long long)sm_count() * 8;
+    acc_finish_kernel<<<(int)(blocks < cap ? blocks : cap), kThreads, 0, st>>>(
+        reinterpret_cast<const float4*>(acc), reinterpret_cast<const uint4*>(residual), n8,
+        reinterpret_cast<uint4*>(out));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& L,
                            const moe_shape& s, uint16_t* partial, const uint16_t* shared,

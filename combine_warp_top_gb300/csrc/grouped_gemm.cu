@@ -87,7 +87,11 @@ using namespace ptx;
 // kGather: A row i of the problem is row a_rows[i] of a_src (rows >= a_total
 // and indices outside [0, a_src_rows) read row 0; such rows are masked on
 // store); otherwise row i of tmA's tensor.
-template <bool kSwiGLU, bool kGather>
+// kCombine (down only): instead of storing y, the epilogue scales row i by its
+// routing weight and adds it into cmb.acc[token of row i] with fp32 vector
+// atomics (the combine of "Kernel fusion for expert parallelism", stage 7,
+// moved into the MatMul's epilogue).
+template <bool kSwiGLU, bool kGather, bool kCombine>
 __global__ void __launch_bounds__(threads_for(kGather), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB0,
@@ -98,7 +102,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1)
                         const int32_t* __restrict__ mblk_prefix, int E, int K, int n_out,
                         __nv_bfloat16* __restrict__ out, int* err,
                         const int32_t* __restrict__ a_rows, int a_total, int a_src_rows,
-                        const uint16_t* __restrict__ a_src) {
+                        const uint16_t* __restrict__ a_src, const CombineArgs cmb) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* tiles = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1)
         if (!kGather) prefetch_map(&tmA);
         prefetch_map(&tmB0);
         if (kSwiGLU) prefetch_map(&tmB1);
-        prefetch_map(&tmOut);
+        if (!kCombine) prefetch_map(&tmOut);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
@@ -261,6 +265,54 @@ __global__ void __launch_bounds__(threads_for(kGather), 1)
             if (!ready) break;
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kMmaN);
+            if constexpr (kCombine) {
+                // this lane's row: its token and routing weight (the j with
+                // pair_row[t, j] == row)
+                const int i = row_base + lane;
+                int t = 0;
+                float wr = 0.f;
+                if (lane < rows_valid) {
+                    const int tt = cmb.row_token[i];
+                    t = (unsigned)tt < (unsigned)cmb.N ? tt : 0;
+                    for (int j = 0; j < cmb.k; ++j) {
+                        if (cmb.pair_row[(size_t)t * cmb.k + j] == i) {
+                            wr = cmb.topk_w[(size_t)t * cmb.k + j];
+                            break;
+                        }
+                    }
+                }
+                // 32 columns at a time: each lane stages its scaled row (128 B,
+                // swizzled), then 8 lanes per row add whole 128-byte lines
+                const int qq = lane & 7;
+#pragma unroll 1
+                for (int c = 0; c < BNo / 32; ++c) {
+                    uint32_t g[32];
+                    tmem_ld32(tbase + (uint32_t)(c * 32), g);
+                    tmem_wait_ld();
+                    __syncwarp();  // the previous slice's reads of the staging tile are done
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const float4 v = make_float4(wr * __uint_as_float(g[4 * ch]),
+                                                     wr * __uint_as_float(g[4 * ch + 1]),
+                                                     wr * __uint_as_float(g[4 * ch + 2]),
+                                                     wr * __uint_as_float(g[4 * ch + 3]));
+                        *reinterpret_cast<float4*>(my_row + ((ch ^ sw) << 4)) = v;
+                    }
+                    __syncwarp();
+                    const int col = n0 + c * 32 + qq * 4;  // n_out % 8 == 0: 4 columns in or out
+#pragma unroll
+                    for (int pp = 0; pp < 8; ++pp) {
+                        const int rr = pp * 4 + (lane >> 3);
+                        const int tr = __shfl_sync(0xffffffffu, t, rr);
+                        if (rr < rows_valid && col < n_out) {
+                            const float4 v = *reinterpret_cast<const float4*>(
+                                stage + rr * 128 + ((qq ^ (rr & 7)) << 4));
+                            atomicAdd(reinterpret_cast<float4*>(cmb.acc + (size_t)tr * n_out + col),
+                                      v);
+                        }
+                    }
+                }
+            } else {
 #pragma unroll 1
             for (int c = 0; c < BNo / kStageCols; ++c) {
                 // the staging tile is free once the previous TMA store has read it
@@ -322,6 +374,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1)
                     __syncwarp();
                 }
             }
+            }  // kCombine
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
@@ -474,13 +527,16 @@ cudaError_t launch_schedule(const int32_t* counts, int E, int bm, int32_t* prefi
 namespace {
 
 bool set_smem_attr() {
-    return cudaFuncSetAttribute(grouped_gemm_kernel<true, false>,
+    return cudaFuncSetAttribute(grouped_gemm_kernel<true, false, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kSmemBytes) == cudaSuccess &&
-           cudaFuncSetAttribute(grouped_gemm_kernel<true, true>,
+           cudaFuncSetAttribute(grouped_gemm_kernel<true, true, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kSmemBytes) == cudaSuccess &&
-           cudaFuncSetAttribute(grouped_gemm_kernel<false, false>,
+           cudaFuncSetAttribute(grouped_gemm_kernel<false, false, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kSmemBytes) == cudaSuccess &&
+           cudaFuncSetAttribute(grouped_gemm_kernel<false, false, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kSmemBytes) == cudaSuccess;
 }
@@ -519,13 +575,13 @@ moe_status launch_gate_up(const uint16_t* rows, const GemmGroup& g, int H, int I
     if (ss != MOE_OK) return ss;
     __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(h);
     if (gather)
-        grouped_gemm_kernel<true, true><<<grid, threads_for(true), kSmemBytes, st>>>(
+        grouped_gemm_kernel<true, true, false><<<grid, threads_for(true), kSmemBytes, st>>>(
             a, bg, bu, o, g.offsets, g.counts, g.prefix, g.E, H, I, hb, g.err, gather, (int)g.R,
-            (int)src_rows, rows);
+            (int)src_rows, rows, CombineArgs{});
     else
-        grouped_gemm_kernel<true, false><<<grid, kThreads, kSmemBytes, st>>>(
+        grouped_gemm_kernel<true, false, false><<<grid, kThreads, kSmemBytes, st>>>(
             a, bg, bu, o, g.offsets, g.counts, g.prefix, g.E, H, I, hb, g.err, nullptr, 0, 0,
-            nullptr);
+            nullptr, CombineArgs{});
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -540,9 +596,26 @@ moe_status launch_down(const uint16_t* h, const GemmGroup& g, int H, int I, cons
     int grid;
     const moe_status ss = schedule(g, (H + kMmaN - 1) / kMmaN, st, &grid);
     if (ss != MOE_OK) return ss;
-    grouped_gemm_kernel<false, false><<<grid, kThreads, kSmemBytes, st>>>(
+    grouped_gemm_kernel<false, false, false><<<grid, kThreads, kSmemBytes, st>>>(
         a, bd, bd, o, g.offsets, g.counts, g.prefix, g.E, I, H,
-        reinterpret_cast<__nv_bfloat16*>(y), g.err, nullptr, 0, 0, nullptr);
+        reinterpret_cast<__nv_bfloat16*>(y), g.err, nullptr, 0, 0, nullptr, CombineArgs{});
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status launch_down_combine(const uint16_t* h, const GemmGroup& g, int H, int I,
+                               const uint16_t* wd, const CombineArgs& cmb, cudaStream_t st) {
+    if (g.R == 0) return MOE_OK;
+    CUtensorMap a, bd, o;
+    memset(&o, 0, sizeof(o));  // unused: the epilogue adds into cmb.acc
+    if (!map_2d(&a, h, g.R, I, BM) || !map_3d(&bd, wd, g.E, H, I, kMmaN))
+        return MOE_ERR_UNSUPPORTED;
+    if (!set_smem_attr()) return MOE_ERR_CUDA;
+    int grid;
+    const moe_status ss = schedule(g, (H + kMmaN - 1) / kMmaN, st, &grid);
+    if (ss != MOE_OK) return ss;
+    grouped_gemm_kernel<false, false, true><<<grid, kThreads, kSmemBytes, st>>>(
+        a, bd, bd, o, g.offsets, g.counts, g.prefix, g.E, I, H, nullptr, g.err, nullptr, 0, 0,
+        nullptr, cmb);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -551,10 +624,8 @@ moe_status launch_down(const uint16_t* h, const GemmGroup& g, int H, int I, cons
 // give up, record MOE_ERR_TIMEOUT and let the kernel return.
 __global__ void wait_selftest_kernel(long long limit_cycles, int* err) {
     __shared__ uint64_t bar;
-    __shared__ int abort_flag;
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bar), 1);
-        abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -562,7 +633,6 @@ __global__ void wait_selftest_kernel(long long limit_cycles, int* err) {
         const long long t0 = clock64();
         while (!mbar_try_wait(smem_u32(&bar), 0)) {
             if (clock64() - t0 > limit_cycles) {
-                abort_flag = 1;
                 set_error(err, MOE_ERR_TIMEOUT);
                 break;
             }

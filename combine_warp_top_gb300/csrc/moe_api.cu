@@ -194,6 +194,24 @@ moe_status moe_ffn_down(const uint16_t* h, const moe_layout* layout, const moe_s
     return launch_down(h, g, shape->H, shape->I, w_down, y, as_stream(stream));
 }
 
+moe_status moe_ffn_down_combine(const uint16_t* h, const float* topk_w, const moe_layout* layout,
+                                const moe_shape* shape, const uint16_t* w_down,
+                                const uint16_t* residual, float* acc, uint16_t* out, void* ws,
+                                size_t ws_bytes, void* stream) {
+    MOE_TRY(check_shape(shape));
+    MOE_TRY(check_layout(layout, shape));
+    MOE_TRY(check_ws(shape, ws, ws_bytes));
+    if (shape->N == 0) return MOE_OK;
+    if (!h || !topk_w || !w_down || !acc || !out) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = as_stream(stream);
+    if (cudaMemsetAsync(acc, 0, (size_t)shape->N * shape->H * sizeof(float), st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const CombineArgs cmb{layout->row_token, layout->pair_row, topk_w, acc, shape->N, shape->k};
+    MOE_TRY(launch_down_combine(h, routed_group(*layout, *shape, ws), shape->H, shape->I, w_down,
+                                cmb, st));
+    return cuda_status(launch_acc_finish(acc, residual, shape->N, shape->H, out, st));
+}
+
 moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const moe_shape* shape,
                           const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
                           uint16_t* xe, uint16_t* h, uint16_t* y, void* ws, size_t ws_bytes,

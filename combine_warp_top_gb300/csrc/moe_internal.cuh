@@ -90,6 +90,17 @@ struct GemmGroup {
     int* err;
 };
 
+// Inputs of the combine fused into the down GEMM's epilogue: row i of y is
+// added, times its routing weight, into acc[row_token[i], :] (fp32 [N, H]).
+struct CombineArgs {
+    const int32_t* row_token;  // [N*k]
+    const int32_t* pair_row;   // [N*k]
+    const float* topk_w;       // [N*k]
+    float* acc;                // [N, H]
+    int N;
+    int k;
+};
+
 // Return MOE_OK, or an error status when a host-side step (tensor-map
 // encoding, launch) failed.
 // gather != nullptr: problem row i is row gather[i] of `rows` ([src_rows, H]),
@@ -97,6 +108,10 @@ struct GemmGroup {
 moe_status launch_gate_up(const uint16_t* rows, const GemmGroup& g, int H, int I,
                           const uint16_t* wg, const uint16_t* wu, uint16_t* h, cudaStream_t st,
                           const int32_t* gather = nullptr, long long src_rows = 0);
+moe_status launch_down_combine(const uint16_t* h, const GemmGroup& g, int H, int I,
+                               const uint16_t* wd, const CombineArgs& cmb, cudaStream_t st);
+cudaError_t launch_acc_finish(const float* acc, const uint16_t* residual, int N, int H,
+                              uint16_t* out, cudaStream_t st);
 moe_status launch_down(const uint16_t* h, const GemmGroup& g, int H, int I, const uint16_t* wd,
                        uint16_t* y, cudaStream_t st);
 // One warp waits on an mbarrier that never completes, up to limit_cycles.

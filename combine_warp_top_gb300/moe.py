@@ -64,6 +64,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_ffn_down": (I32, [P, lay, shp, P, P, P, S, P]),
         "moe_ffn_gate_up_gather": (I32, [P, P, ctypes.c_int64, lay, shp, P, P, P, P, S, P]),
         "moe_combine": (I32, [P, P, lay, shp, P, P, P, P]),
+        "moe_ffn_down_combine": (I32, [P, P, lay, shp, P, P, P, P, P, S, P]),
         "moe_layer_forward": (I32, [P, P, P, P, P, P, P, shp, P, P, lay, P, P, P, P, P, P, P, S,
                                     P]),
         "moe_dispatch_layout_noalloc": (I32, [P, P, shp, lay, P]),
@@ -230,6 +231,14 @@ def moe_ffn_gate_up_gather(src, row_index, layout: Layout, shape: Shape, w_gate,
                                          _stream(stream)), "moe_ffn_gate_up_gather")
 
 
+def moe_ffn_down_combine(h, topk_w, layout: Layout, shape: Shape, w_down, residual, acc, out,
+                         ws, stream=None):
+    _check(load().moe_ffn_down_combine(_ptr(h), _ptr(topk_w), ctypes.byref(layout.c),
+                                       ctypes.byref(shape.c()), _ptr(w_down), _ptr(residual),
+                                       _ptr(acc), _ptr(out), _ptr(ws), ws.numel(),
+                                       _stream(stream)), "moe_ffn_down_combine")
+
+
 def moe_layer_skips_dispatch(shape: Shape) -> bool:
     """True when the layer gathers its plain rows inside the gate/up GEMM
     (no moe_dispatch copy) for this shape."""
@@ -314,10 +323,15 @@ class MoELayer:
     up) and [E, H, I] (down); placement int32 [E] or None."""
 
     def __init__(self, shape: Shape, w_gate, w_up, w_down, placement=None, device="cuda",
-                 shared=None):
+                 shared=None, fuse_combine=False):
         """shared: optional (w_gate_s [I_s, H], w_up_s [I_s, H], w_down_s [H, I_s])
-        of a shared expert run on every token."""
+        of a shared expert run on every token.  fuse_combine: run the down GEMM
+        with the combine in its epilogue (moe_ffn_down_combine, fp32
+        accumulator) instead of moe_ffn_down + moe_combine."""
+        if fuse_combine and shared is not None:
+            raise ValueError("the combine fused into the down GEMM adds no shared expert")
         self.shape = shape
+        self.fuse_combine = fuse_combine
         self.w_gate, self.w_up, self.w_down = w_gate, w_up, w_down
         self.placement = placement
         self.shared = shared
@@ -341,6 +355,8 @@ class MoELayer:
         self.y = torch.empty(max(shape.R, 1), H, **bf)
         self.partial = torch.empty(max(shape.R_d_max, 1), H, **bf) if shape.dedup else None
         self.out = torch.empty(max(N, 1), H, **bf)
+        self.acc = (torch.empty(max(N, 1), H, dtype=torch.float32, device=device)
+                    if fuse_combine else None)
         self.ws = workspace(shape, device)
 
     def refresh_form(self):
@@ -355,7 +371,7 @@ class MoELayer:
     def forward(self, logits, x, residual=None, out=None, stream=None):
         out = self.out if out is None else out
         self.refresh_form()
-        if self.shared is not None:
+        if self.shared is not None or self.fuse_combine:
             return self.forward_stages(logits, x, residual, out, stream)
         moe_layer_forward(logits, x, self.placement, self.w_gate, self.w_up, self.w_down,
                           residual, self.shape, self.topk_ids, self.topk_w, self.layout,
@@ -376,15 +392,18 @@ class MoELayer:
             self.forward(logits, x, residual, out)
         return g
 
-    STAGES = ("route", "layout", "dispatch", "gate_up", "down", "shared", "combine")
+    STAGES = ("route", "layout", "dispatch", "gate_up", "down", "shared", "combine",
+              "down_combine")
 
     def stage_names(self):
         """The stages forward_stages() runs for this layer, in order: no
         separate dispatch when the gate/up GEMM gathers the plain rows from x,
         no shared expert unless one is set."""
+        fused = ("down_combine",) if self.fuse_combine else ("down", "combine")
         return [n for n in self.STAGES
                 if (n != "dispatch" or not self.fused_dispatch)
-                and (n != "shared" or self.shared is not None)]
+                and (n != "shared" or self.shared is not None)
+                and (n not in ("down", "combine", "down_combine") or n in fused)]
 
     def forward_stages(self, logits, x, residual=None, out=None, stream=None, events=None):
         """The same kernels as forward(), one C call per stage of the pages'
@@ -412,6 +431,12 @@ class MoELayer:
         rec("gate_up", 0)
         self._gate_up(x, st)
         rec("gate_up", 1)
+        if self.fuse_combine:
+            rec("down_combine", 0)
+            moe_ffn_down_combine(self.h, self.topk_w, self.layout, s, self.w_down, residual,
+                                 self.acc, out, self.ws, st)
+            rec("down_combine", 1)
+            return out
         rec("down", 0)
         moe_ffn_down(self.h, self.layout, s, self.w_down, self.y, self.ws, st)
         rec("down", 1)
@@ -451,7 +476,9 @@ class MoELayer:
             return 0
         shared = 5 if self.shared is not None else 0  # dense segment + 2 x (schedule + GEMM)
         dispatch = 0 if self.fused_dispatch else 1
-        return 1 + 3 + dispatch + 2 + 2 + (2 if s.dedup else 1) + shared
+        # fused combine: schedule + GEMM + finish (the accumulator memset is a copy-engine op)
+        down_combine = 3 if self.fuse_combine else 2 + (2 if s.dedup else 1)
+        return 1 + 3 + dispatch + 2 + down_combine + shared
 
     def forward_host(self, logits_h, x_h, residual_h, out_h, dev_inputs=None, stream=None):
         """Whole layer from host buffers: copy the step's inputs host->device,

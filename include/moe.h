@@ -193,6 +193,24 @@ moe_status moe_ffn_gate_up_gather(const uint16_t* src, const int32_t* row_index,
                                   const uint16_t* w_gate, const uint16_t* w_up, uint16_t* h,
                                   void* ws, size_t ws_bytes, void* stream);
 
+/* moe_ffn_down followed by moe_combine, fused: the down GEMM's epilogue scales
+ * each output row by its routing weight and adds it into an fp32 accumulator
+ * instead of storing y (the kernel-fusion page's MegaKernel direction, with the
+ * stage-7 "reduce" moved into the MatMul), then
+ *   out[t, :] = bf16( residual[t, :] + acc[t, :] ),
+ *   acc[t, :] = sum_j topk_w[t, j] * (h[pair_row[t, j], :] Wd[e_j]^T)    fp32
+ * acc: caller-owned fp32 [N, H] scratch, zeroed by this call.  residual is
+ * nullable; out may equal residual.  The k terms of a token are added by
+ * fp32 atomics in whatever order the tiles finish, so the result equals
+ * moe_ffn_down + moe_combine up to fp32 reassociation and y's bf16 rounding
+ * (y is never rounded here) and is not bit-reproducible from run to run.
+ * The dedup form gives the same sums (its two-level order is not kept).
+ * Always runs the single-CTA GEMM. */
+moe_status moe_ffn_down_combine(const uint16_t* h, const float* topk_w, const moe_layout* layout,
+                                const moe_shape* shape, const uint16_t* w_down,
+                                const uint16_t* residual, float* acc, uint16_t* out, void* ws,
+                                size_t ws_bytes, void* stream);
+
 /* Combine (kernel-fusion page, "Expert parallelism: dispatch and combine" and
  * stage 7 "reduce"; residual add of FarSkip-Collective Sec. 3).
  * Plain: out[t, :] = bf16( residual[t, :] + sum_j topk_w[t, j] * y[pair_row[t, j], :] ),
