@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1)
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
                 int e, mb, nb;
-                decode_tile(ctl->prefix, E, NB, tile, e, mb, nb);
+                decode_tile(ctl->prefix, E, NB, BM, kMmaN, tile, e, mb, nb);
                 const int row0 = ctl->offs[e] + mb * BM;
                 const int n0 = nb * BNo;
                 for (int kb = 0; kb < KB; ++kb) {
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1)
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             int e, mb, nb;
-            decode_tile(ctl->prefix, E, NB, tile, e, mb, nb);
+            decode_tile(ctl->prefix, E, NB, BM, kMmaN, tile, e, mb, nb);
             const int row_base = ctl->offs[e] + mb * BM + q * 32;  // this warp's first row
             int rows_valid = ctl->offs[e] + ctl->cnts[e] - row_base;
             rows_valid = rows_valid < 0 ? 0 : (rows_valid > 32 ? 32 : rows_valid);
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1)
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
             int e, mb, nb;
-            decode_tile(ctl->prefix, E, NB, tile, e, mb, nb);
+            decode_tile(ctl->prefix, E, NB, BM, kMmaN, tile, e, mb, nb);
             const int row0 = ctl->offs[e] + mb * BM;
             const uint16_t* src[BM / 16];
 #pragma unroll

@@ -137,7 +137,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int tile = pair; ok && tile < total; tile += npairs) {
                 int e, mb, nb;
-                decode_tile(ctl->prefix, E, NB, tile, e, mb, nb);
+                decode_tile(ctl->prefix, E, NB, BMP, kMmaN, tile, e, mb, nb);
                 const int row0 = ctl->offs[e] + mb * BMP + (int)rank * BMC;
                 const int n0 = nb * BNo;
                 for (int kb = 0; kb < KB; ++kb) {
@@ -234,7 +234,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t acc_phase = 0;
         for (int tile = pair; tile < total; tile += npairs) {
             int e, mb, nb;
-            decode_tile(ctl->prefix, E, NB, tile, e, mb, nb);
+            decode_tile(ctl->prefix, E, NB, BMP, kMmaN, tile, e, mb, nb);
             const int row_base = ctl->offs[e] + mb * BMP + (int)rank * BMC + q * 32;
             int rows_valid = ctl->offs[e] + ctl->cnts[e] - row_base;
             rows_valid = rows_valid < 0 ? 0 : (rows_valid > 32 ? 32 : rows_valid);

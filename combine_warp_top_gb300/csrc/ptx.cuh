@@ -318,11 +318,14 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// tile -> (expert, m-block, n-block).  Tiles are numbered expert by expert;
-// inside an expert the m-blocks vary fastest, so CTAs running side by side
-// share the same weight block through L2.
-__device__ __forceinline__ void decode_tile(const int* prefix, int E, int NB, int tile, int& e,
-                                            int& mb, int& nb) {
+// tile -> (expert, m-block, n-block).  Tiles are numbered expert by expert.
+// Inside an expert the order re-reads the smaller operand: when the expert's
+// A rows (MB m-blocks of bm rows) outnumber its weight rows (NB n-blocks of
+// bn_w rows), the n-blocks vary fastest, so each m-block's rows are read once
+// while the expert's weight blocks stay in L2; otherwise the m-blocks vary
+// fastest and CTAs running side by side share a weight block through L2.
+__device__ __forceinline__ void decode_tile(const int* prefix, int E, int NB, int bm, int bn_w,
+                                            int tile, int& e, int& mb, int& nb) {
     const int q = tile / NB;
     int lo = 0, hi = E;  // prefix[lo] <= q < prefix[hi]
     while (hi - lo > 1) {
@@ -333,8 +336,13 @@ __device__ __forceinline__ void decode_tile(const int* prefix, int E, int NB, in
     e = lo;
     const int MB = prefix[e + 1] - prefix[e];
     const int local = tile - NB * prefix[e];
-    nb = local / MB;
-    mb = local - nb * MB;
+    if ((long long)MB * bm > (long long)NB * bn_w) {
+        mb = local / NB;
+        nb = local - mb * NB;
+    } else {
+        nb = local / MB;
+        mb = local - nb * MB;
+    }
 }
 
 }  // namespace ptx

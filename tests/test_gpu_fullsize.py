@@ -31,14 +31,14 @@ def runs():
     return {}
 
 
-def run_full(name):
+def run_full(name, fuse_combine=False):
     wl = synth.WORKLOADS[name]
     shape = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=wl.dedup)
     placement = synth.make_placement(wl)
     pl_d = None if wl.placement == "contiguous" else dev_i32(placement)
     layer = moe.MoELayer(shape, synth.make_weight_device(wl, "gate"),
                          synth.make_weight_device(wl, "up"), synth.make_weight_device(wl, "down"),
-                         pl_d)
+                         pl_d, fuse_combine=fuse_combine)
     L = synth.make_logits(wl)
     x = synth.make_x(wl)
     res = synth.make_residual(wl)
@@ -109,6 +109,27 @@ def test_full_size_workload(name):
     pr = ref["pair_row"][toks].reshape(-1)
     y_got = host_f64(layer.y[torch.from_numpy(pr.astype(np.int64)).cuda()])
     assert_close(y_got, y_want.reshape(-1, wl.H), f"{name} y rows")
+
+
+@pytest.mark.parametrize("name", ["deepseek_v3", "correlated_placed"])
+def test_full_size_fused_combine(name):
+    """The combine fused into the down GEMM's epilogue at full size, on
+    sampled tokens recomputed by the oracle."""
+    wl, layer, L, x, res, placement, out = run_full(name, fuse_combine=True)
+    N, k = wl.N, wl.k
+    ids = layer.topk_ids.view(N, k).cpu().numpy()
+    w = layer.topk_w.view(N, k).cpu().numpy()
+    ref_ids, ref_w = oracle.route(L, k)
+    assert np.array_equal(ids, ref_ids)
+    rng = np.random.default_rng(11)
+    n = SAMPLES[wl.name]
+    toks = np.unique(np.concatenate([[0, N - 1], rng.choice(N, size=n - 2, replace=False)]))
+
+    def weights_of(e):
+        return tuple(synth.make_weight(wl, m, experts=[e])[0] for m in ("gate", "up", "down"))
+
+    want, _ = oracle.token_outputs(x[toks], ref_ids[toks], ref_w[toks], weights_of, res[toks])
+    assert_close(host_f64(out[torch.from_numpy(toks).cuda()]), want, f"{name} fused-combine out")
 
 
 def test_device_weight_generator_matches_host():
