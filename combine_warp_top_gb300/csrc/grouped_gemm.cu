@@ -444,7 +444,8 @@ __global__ void __launch_bounds__(threads_for(kGather), 1)
     }
 }
 
-// m-blocks per expert, exclusive prefix over expert ids: mblk_prefix[E+1].
+// m-blocks per expert, exclusive prefix over expert ids: mblk_prefix[E+1];
+// one more entry, mblk_prefix[E+1], is reset to 0 for the tile counter.
 __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* __restrict__ counts, int E,
                                                         int bm, int32_t* __restrict__ mblk_prefix) {
     __shared__ int warp_sums[32];
@@ -471,7 +472,10 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* __restric
     __syncthreads();
     const int excl = warp_sums[warp] + incl - v;
     if (e < E) mblk_prefix[e] = excl;
-    if (e == E - 1) mblk_prefix[E] = excl + v;
+    if (e == E - 1) {
+        mblk_prefix[E] = excl + v;
+        mblk_prefix[E + 1] = 0;  // tile counter of a dynamically scheduled GEMM
+    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

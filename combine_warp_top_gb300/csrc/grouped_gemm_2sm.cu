@@ -11,7 +11,7 @@
 // 128 rows), so 32 KB per CTA and k-block feed a 256x256 MMA.  That halves
 // the B traffic per flop and leaves room for six pipeline stages.
 //
-// Roles per CTA (192 threads): warp 0 loads this CTA's A rows and B half by
+// Roles per CTA (224 threads): warp 0 loads this CTA's A rows and B half by
 // TMA, counting the bytes on the LEADER's full barrier; warp 1 allocates TMEM
 // (collectively for the pair) and, in the leader only, issues
 // tcgen05.mma.cta_group::2 (M=256, N=256) and commits each stage to the empty
@@ -19,6 +19,18 @@
 // each CTA drain its own 128 accumulator rows (as in the single-CTA kernel)
 // and release the accumulator on the leader's tmem-empty barrier (8 arrivals:
 // 4 local, 4 from the peer).  Every wait is bounded.
+//
+// Tiles are handed out dynamically: a scheduler warp of the leader (warp 6)
+// takes tile indices from a global counter and publishes them in a small
+// queue in both CTAs' shared memory, one tile ahead of the leader's producer
+// (so the tiles in flight over the whole GPU stay about two per pair).  In the leader the producer, the MMA thread and the epilogue warps
+// read that queue; in the peer only the producer does, and it forwards each
+// tile to its epilogue warps through a second, CTA-local queue, so a tile
+// costs one cluster-scope release each way and none on a loading thread.
+// Pairs that run faster simply take more tiles, so the tiles in flight stay
+// close to consecutive in the schedule's order and blocks that neighbouring
+// tiles share are still in L2 when they are needed (a static round-robin
+// assignment lets pairs drift apart over a long launch).
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 
@@ -38,9 +50,13 @@ constexpr int kTmemCols = kMmaN * kAccs;
 constexpr int A_BYTES = BMC * BK * 2;          // 16 KB
 constexpr int B_BYTES = (kMmaN / 2) * BK * 2;  // 16 KB: this CTA's half of N
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;  // 6 warps + the tile scheduler warp
 constexpr int kEpilogueWarps = 4;
 constexpr int kStageCols = 64;
+constexpr int kQ = 8;  // slots of the tile queues
+// Readers of each slot of the leader's queue: its producer, MMA thread and 4
+// epilogue warps, and the peer's producer.
+constexpr int kQueueReaders = 2 + kEpilogueWarps + 1;
 constexpr int kStageWarpBytes = 32 * kStageCols * 2;
 
 struct Ctl {
@@ -49,6 +65,13 @@ struct Ctl {
     uint64_t tfull[kAccs];     // each CTA: accumulator ready
     uint64_t tempty[kAccs];    // leader: accumulator drained by both CTAs
     uint64_t done;             // leader: every issued MMA retired
+    uint64_t tq_full[kQ];      // each CTA: queue slot written
+    uint64_t tq_empty[kQ];     // leader: queue slot read by every reader of both CTAs
+    int tile_q[kQ];            // each CTA: tile index (-1: no more tiles)
+    uint64_t tq_taken[kQ];     // leader: its producer has taken the slot's tile
+    uint64_t lq_full[kQ];      // peer: local queue slot written by its producer
+    uint64_t lq_empty[kQ];     // peer: local queue slot read by its 4 epilogue warps
+    int local_q[kQ];           // peer: the tiles forwarded to its epilogue
     uint32_t tmem_base;
     int abort;
     int prefix[kMaxE + 1];
@@ -59,6 +82,66 @@ struct Ctl {
 constexpr size_t kCtlBytes = (sizeof(Ctl) + 15) & ~size_t(15);
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * STAGE_BYTES +
                               (size_t)kEpilogueWarps * kStageWarpBytes + kCtlBytes;
+
+// Leader's scheduler thread: wait until queue slot i % kQ is free in both CTAs, take
+// the next tile from the counter (-1 once every tile is taken) and publish it
+// to both CTAs.  Returns the tile, or -2 if the wait gave up.
+__device__ __forceinline__ int queue_publish(Ctl* ctl, int i, int* counter, int total,
+                                             volatile int* abort, int* err) {
+    const int slot = i % kQ;
+    const uint32_t ph = (uint32_t)(i / kQ) & 1u;
+    if (!wait_bar(smem_u32(&ctl->tq_empty[slot]), ph ^ 1u, abort, err)) return -2;
+    int t = atomicAdd(counter, 1);
+    if (t >= total) t = -1;
+    ctl->tile_q[slot] = t;
+    st_shared_cluster(mapa_shared(smem_u32(&ctl->tile_q[slot]), 1), t);
+    mbar_arrive(smem_u32(&ctl->tq_full[slot]));
+    // release.cluster: the store into the peer's slot is visible before its arrival
+    mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tq_full[slot]), 1));
+    return t;
+}
+
+// Peer's producer: forward tile t to the peer's epilogue warps (local queue).
+// Returns false if the wait gave up.
+__device__ __forceinline__ bool local_publish(Ctl* ctl, int i, int t, volatile int* abort,
+                                              int* err) {
+    const int slot = i % kQ;
+    const uint32_t ph = (uint32_t)(i / kQ) & 1u;
+    if (!wait_bar(smem_u32(&ctl->lq_empty[slot]), ph ^ 1u, abort, err)) return false;
+    ctl->local_q[slot] = t;
+    mbar_arrive(smem_u32(&ctl->lq_full[slot]));
+    return true;
+}
+
+// Peer's epilogue warp (lane 0): the tile in local queue slot i % kQ.
+__device__ __forceinline__ int local_take(Ctl* ctl, int i, volatile int* abort, int* err) {
+    const int slot = i % kQ;
+    const uint32_t ph = (uint32_t)(i / kQ) & 1u;
+    if (!wait_bar(smem_u32(&ctl->lq_full[slot]), ph, abort, err)) return -2;
+    const int t = *reinterpret_cast<volatile int*>(&ctl->local_q[slot]);
+    mbar_arrive(smem_u32(&ctl->lq_empty[slot]));
+    return t;
+}
+
+// Reader of the leader's queue (the leader's producer, MMA thread and
+// epilogue warps, the peer's producer): the tile in slot i % kQ (-1: none left), after which
+// the slot is released to the leader.  Returns -2 if the wait gave up.
+__device__ __forceinline__ int queue_take(Ctl* ctl, int i, bool leader, volatile int* abort,
+                                          int* err) {
+    const int slot = i % kQ;
+    const uint32_t ph = (uint32_t)(i / kQ) & 1u;
+    const uint32_t full = smem_u32(&ctl->tq_full[slot]);
+    // the peer's copy was written by the leader: acquire at cluster scope
+    if (!(leader ? wait_bar(full, ph, abort, err) : wait_bar_cluster(full, ph, abort, err)))
+        return -2;
+    const int t = *reinterpret_cast<volatile int*>(&ctl->tile_q[slot]);
+    const uint32_t empty = smem_u32(&ctl->tq_empty[slot]);
+    if (leader)
+        mbar_arrive(empty);
+    else
+        mbar_arrive_cluster(mapa_shared(empty, 0));
+    return t;
+}
 
 // Spin for about `cycles` SM clocks (lets copies in flight land on abort).
 __device__ __forceinline__ void spin(long long cycles) {
@@ -76,7 +159,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                              const int32_t* __restrict__ expert_offsets,
                              const int32_t* __restrict__ expert_counts,
                              const int32_t* __restrict__ mblk_prefix, int E, int K, int n_out,
-                             __nv_bfloat16* __restrict__ out, int* err) {
+                             __nv_bfloat16* __restrict__ out, int* err, int* tile_counter) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* tiles = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -91,7 +174,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr int BNo = kSwiGLU ? kMmaN / 2 : kMmaN;  // output columns per tile
     const int NB = (n_out + BNo - 1) / BNo;
     const int KB = (K + BK - 1) / BK;
-    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
     for (int i = threadIdx.x; i <= E; i += blockDim.x) ctl->prefix[i] = mblk_prefix[i];
     for (int i = threadIdx.x; i < E; i += blockDim.x) {
@@ -108,6 +190,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&ctl->tempty[a]), 2 * kEpilogueWarps);
         }
         mbar_init(smem_u32(&ctl->done), 1);
+        for (int q = 0; q < kQ; ++q) {
+            mbar_init(smem_u32(&ctl->tq_full[q]), 1);
+            mbar_init(smem_u32(&ctl->tq_empty[q]), kQueueReaders);
+            mbar_init(smem_u32(&ctl->lq_full[q]), 1);
+            mbar_init(smem_u32(&ctl->tq_taken[q]), 1);
+            mbar_init(smem_u32(&ctl->lq_empty[q]), kEpilogueWarps);
+        }
         ctl->abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -135,7 +224,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
             bool ok = true;
-            for (int tile = pair; ok && tile < total; tile += npairs) {
+            for (int i = 0; ok; ++i) {
+                int tile = queue_take(ctl, i, leader, abort_flag, err);
+                if (leader && tile != -2) mbar_arrive(smem_u32(&ctl->tq_taken[i % kQ]));
+                if (!leader && tile != -2 && !local_publish(ctl, i, tile, abort_flag, err))
+                    tile = -2;
+                if (tile == -2) ok = false;
+                if (tile < 0) break;
                 int e, mb, nb;
                 decode_tile(ctl->prefix, E, NB, BMP, kMmaN, tile, e, mb, nb);
                 const int row0 = ctl->offs[e] + mb * BMP + (int)rank * BMC;
@@ -187,7 +282,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int tile = pair; ok && tile < total; tile += npairs) {
+            for (int i = 0; ok; ++i) {
+                if (queue_take(ctl, i, true, abort_flag, err) < 0) break;
                 if (!wait_bar(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u, abort_flag, err)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(acc * kMmaN);
@@ -221,7 +317,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             umma_commit_pair_multicast(smem_u32(&ctl->done), 0x1);
             wait_bar_drain(smem_u32(&ctl->done), 0);
         }
-    } else {
+    } else if (warp < 2 + kEpilogueWarps) {
         // ---------------- epilogue (both CTAs): own 128 rows ----------------
         const int q = warp & 3;
         uint8_t* stage = stage_area + (size_t)(warp - 2) * kStageWarpBytes;
@@ -232,7 +328,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t tempty_leader1 = mapa_shared(smem_u32(&ctl->tempty[1]), 0);
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = pair; tile < total; tile += npairs) {
+        for (int i = 0;; ++i) {
+            int tile = 0;
+            if (lane == 0)
+                tile = leader ? queue_take(ctl, i, true, abort_flag, err)
+                              : local_take(ctl, i, abort_flag, err);
+            tile = __shfl_sync(0xffffffffu, tile, 0);
+            if (tile < 0) break;
             int e, mb, nb;
             decode_tile(ctl->prefix, E, NB, BMP, kMmaN, tile, e, mb, nb);
             const int row_base = ctl->offs[e] + mb * BMP + (int)rank * BMC + q * 32;
@@ -311,6 +413,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
+    } else if (leader && lane == 0) {
+        // ---------------- tile scheduler (leader) ----------------
+        // index i is published once the producer has taken index i - 1
+        for (int i = 0;; ++i) {
+            if (i > 0) {
+                const int j = i - 1;
+                if (!wait_bar(smem_u32(&ctl->tq_taken[j % kQ]), (uint32_t)(j / kQ) & 1u,
+                              abort_flag, err))
+                    break;
+            }
+            if (queue_publish(ctl, i, tile_counter, total, abort_flag, err) < 0) break;
+        }
     }
 
     tc_fence_before();
@@ -357,7 +471,7 @@ moe_status launch_gate_up_pair(const uint16_t* rows, const GemmGroup& g, int H, 
     if (ss != MOE_OK) return ss;
     grouped_gemm_pair_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(
         a, bg, bu, o, g.offsets, g.counts, g.prefix, g.E, H, I,
-        reinterpret_cast<__nv_bfloat16*>(h), g.err);
+        reinterpret_cast<__nv_bfloat16*>(h), g.err, g.prefix + g.E + 1);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -374,7 +488,7 @@ moe_status launch_down_pair(const uint16_t* h, const GemmGroup& g, int H, int I,
     if (ss != MOE_OK) return ss;
     grouped_gemm_pair_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(
         a, bd, bd, o, g.offsets, g.counts, g.prefix, g.E, I, H,
-        reinterpret_cast<__nv_bfloat16*>(y), g.err);
+        reinterpret_cast<__nv_bfloat16*>(y), g.err, g.prefix + g.E + 1);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

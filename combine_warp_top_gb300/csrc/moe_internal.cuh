@@ -24,7 +24,7 @@ struct Workspace {
     size_t blk_counts;   // int32 [nblk][E]  per-block counts by placement slot
     size_t blk_rcounts;  // int32 [nblk][W]  per-block dedup counts by rank
     size_t slot_start;   // int32 [E+1]      first row of each slot
-    size_t mblk_prefix;  // int32 [E+1]      GEMM m-blocks before expert e
+    size_t mblk_prefix;  // int32 [E+2]      GEMM m-blocks before expert e; [E+1]: tile counter
     size_t dense;        // int32 [8]        shared expert: count, offsets, schedule
     size_t total;
 };
@@ -41,7 +41,7 @@ inline Workspace workspace_layout(const moe_shape& s) {
     w.blk_counts = o;  o = align256(o + nb * s.E * 4);
     w.blk_rcounts = o; o = align256(o + nb * s.W * 4);
     w.slot_start = o;  o = align256(o + (size_t)(s.E + 1) * 4);
-    w.mblk_prefix = o; o = align256(o + (size_t)(s.E + 1) * 4);
+    w.mblk_prefix = o; o = align256(o + (size_t)(s.E + 2) * 4);
     w.dense = o;       o = align256(o + 8 * 4);
     w.total = o;
     return w;
@@ -80,7 +80,8 @@ cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& 
 
 // One grouped GEMM problem: R rows in E expert segments (device arrays
 // counts[E], offsets[E] of the segments), plus device scratch for its tile
-// schedule (prefix[E+1]) and the error word.
+// schedule (prefix[0..E], and prefix[E+1] as a tile counter) and the error
+// word.
 struct GemmGroup {
     const int32_t* counts;
     const int32_t* offsets;

@@ -61,6 +61,35 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     return true;
 }
 
+// Bounded wait with cluster-scope acquire, for a barrier that a thread of the
+// other CTA of a cluster arrives on with release.cluster semantics (so that
+// what that thread wrote before arriving is visible after the wait).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity,
+                                                 volatile int* abort, int* err) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait_cluster(bar, parity)) {
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitLimit) {
+            *abort = 1;
+            set_error(err, MOE_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
 // Bounded wait that ignores the abort flag (used only while draining).
 __device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity) {
     const long long t0 = clock64();
@@ -239,6 +268,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
+}
+
+// 32-bit store into another CTA's shared memory (shared::cluster address).
+__device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, int v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {
