@@ -116,22 +116,36 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def recorded_traffic(wl):
-    """DRAM bytes per launch of the gate/up GEMM from the committed ncu capture
-    (profiles/), scaled to this workload; None if the capture does not cover
-    this workload or the kernel source changed since it was taken."""
+TRAFFIC_SOURCES = ("combine_warp_top_gb300/csrc/grouped_gemm.cu",
+                   "combine_warp_top_gb300/csrc/grouped_gemm_2sm.cu",
+                   "combine_warp_top_gb300/csrc/ptx.cuh")
+
+
+def sources_digest():
+    """sha256 prefix over the grouped-GEMM sources (both kernels and their PTX
+    wrappers): a recorded DRAM traffic figure holds only for these bytes."""
     import hashlib
+    h = hashlib.sha256()
+    for rel in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(wl):
+    """DRAM bytes (read + write) of one gate/up GEMM launch of this workload,
+    from the committed ncu capture (profiles/gemm_traffic.json: one full-size
+    capture per workload); None if the capture does not cover this workload
+    or the GEMM sources changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "gemm_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        rec = json.load(f).get("grouped_gemm_kernel<SwiGLU>")
-    if not rec or rec.get("workload") != wl.name:
+        rec = json.load(f)
+    if rec.get("sources_sha256_prefix") != sources_digest():
         return None
-    with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest()[:16] != rec["sha256_prefix"]:
-            return None
-    return rec["traffic_bytes_per_full_launch"]
+    entry = rec.get("gate_up", {}).get(wl.name)
+    return None if entry is None else entry["dram_bytes"]
 
 
 # ---------------------------------------------------------------------------- clocks

@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1)
                         const int32_t* __restrict__ mblk_prefix, int E, int K, int n_out,
                         __nv_bfloat16* __restrict__ out, int* err,
                         const int32_t* __restrict__ a_rows, int a_total, int a_src_rows,
-                        const uint16_t* __restrict__ a_src, const CombineArgs cmb) {
+                        const uint16_t* __restrict__ a_src, int a_keep, const CombineArgs cmb) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* tiles = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -419,11 +419,23 @@ __global__ void __launch_bounds__(threads_for(kGather), 1)
                 const uint32_t a_s = tiles_addr + stage * STAGE_BYTES;
                 const int col = kb * BK + chunk * 8;
                 const bool in = col < K;  // K % 8 == 0: a chunk is wholly in or out
+                if (a_keep) {
+                    // a source small enough to stay in L2 is read there by the
+                    // later experts of each token, not from HBM again
+                    const uint64_t pol = policy_evict_last(1.0f);
+#pragma unroll
+                    for (int i = 0; i < BM / 16; ++i) {
+                        const int r = i * 16 + rsub;
+                        cp_async_16_hint(a_s + r * 128 + ((chunk ^ (r & 7)) << 4),
+                                         src[i] + (in ? col : 0), in ? 16u : 0u, pol);
+                    }
+                } else {
 #pragma unroll
                 for (int i = 0; i < BM / 16; ++i) {
                     const int r = i * 16 + rsub;
                     cp_async_16(a_s + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + (in ? col : 0),
                                 in ? 16u : 0u);
+                }
                 }
                 cp_async_arrive_noinc(smem_u32(&ctl->full[stage]));
                 if (++stage == kStages) {
@@ -566,6 +578,10 @@ moe_status launch_gate_up(const uint16_t* rows, const GemmGroup& g, int H, int I
     if (g.R == 0) return MOE_OK;
     CUtensorMap a, bg, bu, o;
     bool ok_a = true;
+    // gathered rows are re-read by every expert of their token: ask L2 to keep
+    // the source when it is at most half of L2 (x of the DeepSeek-V3 shape:
+    // 59 MB), never for the larger dedup sources
+    const bool keep_src = gather && src_rows * (long long)H * 2 <= (64LL << 20);
     if (gather)
         memset(&a, 0, sizeof(a));  // unused: the gather warps read `rows` directly
     else
@@ -581,11 +597,11 @@ moe_status launch_gate_up(const uint16_t* rows, const GemmGroup& g, int H, int I
     if (gather)
         grouped_gemm_kernel<true, true, false><<<grid, threads_for(true), kSmemBytes, st>>>(
             a, bg, bu, o, g.offsets, g.counts, g.prefix, g.E, H, I, hb, g.err, gather, (int)g.R,
-            (int)src_rows, rows, CombineArgs{});
+            (int)src_rows, rows, keep_src ? 1 : 0, CombineArgs{});
     else
         grouped_gemm_kernel<true, false, false><<<grid, kThreads, kSmemBytes, st>>>(
             a, bg, bu, o, g.offsets, g.counts, g.prefix, g.E, H, I, hb, g.err, nullptr, 0, 0,
-            nullptr, CombineArgs{});
+            nullptr, 0, CombineArgs{});
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -602,7 +618,7 @@ moe_status launch_down(const uint16_t* h, const GemmGroup& g, int H, int I, cons
     if (ss != MOE_OK) return ss;
     grouped_gemm_kernel<false, false, false><<<grid, kThreads, kSmemBytes, st>>>(
         a, bd, bd, o, g.offsets, g.counts, g.prefix, g.E, I, H,
-        reinterpret_cast<__nv_bfloat16*>(y), g.err, nullptr, 0, 0, nullptr, CombineArgs{});
+        reinterpret_cast<__nv_bfloat16*>(y), g.err, nullptr, 0, 0, nullptr, 0, CombineArgs{});
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -619,7 +635,7 @@ moe_status launch_down_combine(const uint16_t* h, const GemmGroup& g, int H, int
     if (ss != MOE_OK) return ss;
     grouped_gemm_kernel<false, false, true><<<grid, kThreads, kSmemBytes, st>>>(
         a, bd, bd, o, g.offsets, g.counts, g.prefix, g.E, I, H, nullptr, g.err, nullptr, 0, 0,
-        nullptr, cmb);
+        nullptr, 0, cmb);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

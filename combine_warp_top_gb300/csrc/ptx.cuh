@@ -147,6 +147,18 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
                  "r"(src_bytes)
                  : "memory");
 }
+// The same with an L2 eviction-priority policy (createpolicy).
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void* src,
+                                                 uint32_t src_bytes, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst),
+                 "l"(src), "r"(src_bytes), "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_last(float fraction) {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, %1;" : "=l"(p) : "f"(fraction));
+    return p;
+}
 // One arrival on `bar` (counted in its expected arrivals) once every cp.async
 // this thread has issued so far has landed.
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {

@@ -62,3 +62,25 @@ def test_algorithmic_bytes_of_the_deepseek_layer():
 def test_workload_overrides():
     wl = bench.workload(bench.parse_args(["--tokens", "512", "--experts", "32"]))
     assert (wl.N, wl.E, wl.W, wl.H) == (512, 32, 8, 7168)
+
+
+def test_recorded_traffic_follows_the_gemm_sources(tmp_path, monkeypatch):
+    """roofline.traffic is reported only while the GEMM sources keep the bytes
+    the capture was taken on, and only for the captured workload."""
+    import json
+    import shutil
+    for rel in bench.TRAFFIC_SOURCES:
+        dst = tmp_path / rel
+        dst.parent.mkdir(parents=True, exist_ok=True)
+        shutil.copy(os.path.join(bench.ROOT, rel), dst)
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    rec = {"sources_sha256_prefix": bench.sources_digest(),
+           "gate_up": {"mixtral": {"dram_bytes": 123}}}
+    (tmp_path / "profiles" / "gemm_traffic.json").write_text(json.dumps(rec))
+    args = bench.parse_args(["--workload", "mixtral"])
+    assert bench.recorded_traffic(bench.workload(args)) == 123
+    assert bench.recorded_traffic(bench.workload(bench.parse_args([]))) is None
+    with open(tmp_path / bench.TRAFFIC_SOURCES[2], "a") as f:
+        f.write("// changed\n")
+    assert bench.recorded_traffic(bench.workload(args)) is None
