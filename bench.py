@@ -97,8 +97,8 @@ def algorithmic(wl, R_d, fused_dispatch=False):
         "dispatch": dict(bytes=N * H * 2 + rows_d * H * 2),
         "gate_up": dict(bytes=2 * E * I * H * 2 + a_rows * H * 2 + R * I * 2, flops=4 * R * H * I),
         "down": dict(bytes=E * H * I * 2 + R * I * 2 + R * H * 2, flops=2 * R * H * I),
-        "combine": dict(bytes=R * H * 2 + 2 * N * H * 2 + R * 8 +
-                        (2 * R_d * H * 2 if wl.dedup else 0)),
+        # dedup: the partial rows stay in registers (one-pass dedup combine)
+        "combine": dict(bytes=R * H * 2 + 2 * N * H * 2 + R * 8),
         # down GEMM with the combine in its epilogue: weights, h in, residual
         # in, out; y never leaves the SM
         "down_combine": dict(bytes=E * H * I * 2 + R * I * 2 + 2 * N * H * 2 + R * 8,

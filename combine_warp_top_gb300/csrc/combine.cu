@@ -12,10 +12,9 @@
 //
 // One warp per output row.  Each lane owns U 16-byte chunks (8 bf16 each) per
 // step along the row; the source rows of a chunk are loaded together, then
-// accumulated in fp32 in j order.  These are latency-bound chains of loads:
-// the dedup kernels are compiled for at least 3 resident blocks per SM (a
-// register cap that keeps 24 warps per SM in flight), except the owner sum
-// with four chunks per lane, which would spill under that cap and gets 2.
+// accumulated in fp32 in j order.  These are latency-bound chains of loads,
+// so the dedup kernels are compiled with register caps that keep 24-32 warps
+// per SM in flight where that costs no spills.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -235,6 +234,89 @@ __global__ void __launch_bounds__(kThreads, U == 4 ? 2 : 3) owner_sum_kernel(
     }
 }
 
+// Dedup combine in one pass: the two levels of rank_reduce_kernel and
+// owner_sum_kernel with the partial rows kept in registers.  For each of the
+// token's dedup rows d in ascending order (= ascending rank), the partial is
+// the fp32 sum of w[t, j] * y[pair_row[t, j]] over the j carried by d (j
+// ascending), rounded to bf16 as the materialised partial would be; the
+// partials are summed in fp32 in that order, then the shared row and the
+// residual are added.  Bit-identical to the two-kernel form, without writing
+// the partials out and reading them back.
+template <int U>
+__global__ void __launch_bounds__(kThreads, U == 1 ? 4 : (U == 2 ? 2 : 1)) dedup_combine_kernel(
+    const uint4* __restrict__ y, const float* __restrict__ topk_w,
+    const int32_t* __restrict__ pair_row, const int32_t* __restrict__ pair_dedup_row, int N,
+    int C, int k, int R, int Rd_bound, const uint4* shared, const uint4* residual, uint4* out) {
+    constexpr int kRows = kBatch / U;  // source rows kept in registers per step
+    const int lane = threadIdx.x & 31;
+    const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    if (t >= N) return;
+    const int my_row = lane < k ? clamp_row(pair_row[(size_t)t * k + lane], R) : 0;
+    const float my_w = lane < k ? topk_w[(size_t)t * k + lane] : 0.f;
+    const int my_d = lane < k ? clamp_row(pair_dedup_row[(size_t)t * k + lane], Rd_bound) : -1;
+    // group of lane j = number of distinct dedup rows below my_d
+    bool first = lane < k;
+    for (int jj = 0; jj < k; ++jj) {
+        const int o = __shfl_sync(0xffffffffu, my_d, jj);
+        if (jj < lane && o == my_d) first = false;
+    }
+    const uint32_t firsts = __ballot_sync(0xffffffffu, first);
+    int group = 0;
+    for (int jj = 0; jj < k; ++jj) {
+        const int o = __shfl_sync(0xffffffffu, my_d, jj);
+        if (((firsts >> jj) & 1u) && o < my_d) ++group;
+    }
+    const int ngroups = __popc(firsts);
+    for (int c0 = 0; c0 < C; c0 += 32 * U) {
+        float acc[U][8];
+        zero(acc);
+        if (k <= kRows) {
+            // every source row of this step loaded together, then summed group by group
+            uint4 v[kRows][U];
+#pragma unroll
+            for (int b = 0; b < kRows; ++b) {
+                if (b < k) {
+                    const int r = __shfl_sync(0xffffffffu, my_row, b);
+                    const uint4* src = y + (size_t)r * C;
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int c = c0 + u * 32 + lane;
+                        if (c < C) v[b][u] = src[c];
+                    }
+                }
+            }
+            for (int g = 0; g < ngroups; ++g) {
+                const uint32_t members = __ballot_sync(0xffffffffu, lane < k && group == g);
+                float part[U][8];
+                zero(part);
+#pragma unroll
+                for (int b = 0; b < kRows; ++b) {
+                    const float w = __shfl_sync(0xffffffffu, my_w, b);
+                    if ((members >> b) & 1u) {
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            const int c = c0 + u * 32 + lane;
+                            if (c < C) acc_bf16x8(part[u], v[b][u], w);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) add_bf16x8(acc[u], pack_bf16x8(part[u]));
+            }
+        } else {
+            for (int g = 0; g < ngroups; ++g) {
+                const uint32_t members = __ballot_sync(0xffffffffu, lane < k && group == g);
+                float part[U][8];
+                zero(part);
+                gather_weighted<U>(part, y, C, c0, members, my_row, my_w);
+#pragma unroll
+                for (int u = 0; u < U; ++u) add_bf16x8(acc[u], pack_bf16x8(part[u]));
+            }
+        }
+        finish<U>(acc, shared, residual, out, (size_t)t * C, C, c0);
+    }
+}
+
 // out = bf16(acc (+ residual)) for the fp32 accumulator of the combine fused
 // into the down GEMM; one thread per 8 elements, grid-stride.
 __global__ void __launch_bounds__(kThreads) acc_finish_kernel(const float4* __restrict__ acc,
@@ -289,6 +371,20 @@ cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& 
     }
     const int Rd_max = s.N * (s.k < s.W ? s.k : s.W);
     const uint4* yy = reinterpret_cast<const uint4*>(y);
+    if (!partial) {
+        // one pass, partials in registers (bit-identical to the two kernels below)
+        uint4* o = reinterpret_cast<uint4*>(out);
+        if (U == 4)
+            dedup_combine_kernel<4><<<warps_grid(s.N), kThreads, 0, st>>>(
+                yy, w, L.pair_row, L.pair_dedup_row, s.N, C, s.k, R, Rd_max, sh, res, o);
+        else if (U == 2)
+            dedup_combine_kernel<2><<<warps_grid(s.N), kThreads, 0, st>>>(
+                yy, w, L.pair_row, L.pair_dedup_row, s.N, C, s.k, R, Rd_max, sh, res, o);
+        else
+            dedup_combine_kernel<1><<<warps_grid(s.N), kThreads, 0, st>>>(
+                yy, w, L.pair_row, L.pair_dedup_row, s.N, C, s.k, R, Rd_max, sh, res, o);
+        return cudaGetLastError();
+    }
     uint4* pp = reinterpret_cast<uint4*>(partial);
     // a dedup row carries the token's experts on one rank: at most min(k, E/W) rows
     const int per_rank = s.E / s.W;

@@ -241,7 +241,6 @@ moe_status moe_combine(const uint16_t* y, const float* topk_w, const moe_layout*
     MOE_TRY(check_layout(layout, shape));
     if (shape->N == 0) return MOE_OK;
     if (!y || !topk_w || !out) return MOE_ERR_INVALID_ARG;
-    if (shape->dedup && !partial) return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_combine(y, topk_w, *layout, *shape, partial, nullptr, residual, out,
                                       as_stream(stream)));
 }
@@ -275,7 +274,6 @@ moe_status moe_combine_shared(const uint16_t* y, const float* topk_w, const moe_
     MOE_TRY(check_layout(layout, shape));
     if (shape->N == 0) return MOE_OK;
     if (!y || !topk_w || !out || !y_shared) return MOE_ERR_INVALID_ARG;
-    if (shape->dedup && !partial) return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_combine(y, topk_w, *layout, *shape, partial, y_shared, residual, out,
                                       as_stream(stream)));
 }
@@ -294,7 +292,6 @@ moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32
     if (!logits || !x || !w_gate || !w_up || !w_down || !topk_ids || !topk_w || !xd || !h ||
         !y || !out)
         return MOE_ERR_INVALID_ARG;
-    if (shape->dedup && !partial) return MOE_ERR_INVALID_ARG;
     MOE_TRY(moe_route(logits, shape, topk_ids, topk_w, stream));
     MOE_TRY(moe_dispatch_layout(topk_ids, placement, shape, layout, ws, ws_bytes, stream));
     if (moe_layer_skips_dispatch(shape)) {

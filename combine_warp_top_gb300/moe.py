@@ -353,7 +353,9 @@ class MoELayer:
         self.xe = None  # the dedup expansion happens inside the gate/up GEMM
         self.h = torch.empty(max(shape.R, 1), I, **bf)
         self.y = torch.empty(max(shape.R, 1), H, **bf)
-        self.partial = torch.empty(max(shape.R_d_max, 1), H, **bf) if shape.dedup else None
+        # the dedup combine keeps its partial rows in registers (moe_combine with
+        # partial = NULL); a caller who wants them written passes its own buffer
+        self.partial = None
         self.out = torch.empty(max(N, 1), H, **bf)
         self.acc = (torch.empty(max(N, 1), H, dtype=torch.float32, device=device)
                     if fuse_combine else None)
@@ -470,14 +472,14 @@ class MoELayer:
     def kernel_launches_per_step(self) -> int:
         """Kernels of this library launched by one forward (route 1, layout 3,
         dispatch 1 unless fused into the gate/up GEMM, each GEMM 2 with its
-        schedule, combine 1 or 2 with dedup, shared expert 5)."""
+        schedule, combine 1, shared expert 5)."""
         s = self.shape
         if s.N == 0:
             return 0
         shared = 5 if self.shared is not None else 0  # dense segment + 2 x (schedule + GEMM)
         dispatch = 0 if self.fused_dispatch else 1
         # fused combine: schedule + GEMM + finish (the accumulator memset is a copy-engine op)
-        down_combine = 3 if self.fuse_combine else 2 + (2 if s.dedup else 1)
+        down_combine = 3 if self.fuse_combine else 2 + 1
         return 1 + 3 + dispatch + 2 + down_combine + shared
 
     def forward_host(self, logits_h, x_h, residual_h, out_h, dev_inputs=None, stream=None):
@@ -675,6 +677,6 @@ class MicrobatchPipeline:
             s = self.shape
             sub = Shape(t1 - t0, s.H, s.E, s.k, s.W, s.I, s.dedup)
             dispatch = 0 if moe_layer_skips_dispatch(sub) else 1
-            total += 1 + 3 + dispatch + 2 + 2 + (2 if s.dedup else 1) + (
+            total += 1 + 3 + dispatch + 2 + 2 + 1 + (
                 5 if self.shared is not None else 0)
         return total

@@ -219,7 +219,11 @@ moe_status moe_ffn_down_combine(const uint16_t* h, const float* topk_w, const mo
  *        (token, rank), partial[d, :] = bf16( sum over the token's j carried by
  *        row d of topk_w[t, j] * y[pair_row[t, j], :] ) (j order), bf16
  *        [N*min(k,W), H]; the owner then sums the token's partials in ascending
- *        rank order and adds the residual.
+ *        rank order and adds the residual.  With partial == NULL one kernel
+ *        forms each token's partials in registers (same bf16 rounding, same
+ *        orders: bit-identical out) and nothing is written but out; with a
+ *        partial buffer the rank side writes the partial rows there (the
+ *        message a multi-GPU layer would send) and the owner side reads them.
  * residual may be NULL (out is then the MoE output alone) and out may equal
  * residual (in-place add into the residual stream).  partial is ignored when
  * dedup == 0. */

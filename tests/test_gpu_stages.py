@@ -203,3 +203,32 @@ def test_combine_in_place_on_residual():
     torch.cuda.synchronize()
     want = oracle.combine(oracle.widen_bf16(y), w32.astype(np.float64), ref["pair_row"], res)
     assert_close(host_f64(stream_buf), want, "in-place combine")
+
+
+@pytest.mark.parametrize("residual", [True, False])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "wide", "k_eq_e", "one_rank", "e256", "odd_h",
+                                  "deep_k", "long_k5", "long_k2"])
+def test_dedup_combine_one_pass_equals_two_level(name, residual):
+    """The one-pass dedup combine (partial = NULL: partials in registers) gives
+    the two-level form's output bit for bit, and both match the oracle."""
+    wl = {**SMALL, **LONG_ROWS}[name]
+    ids, w64 = oracle.route(synth.make_logits(wl), wl.k)
+    shape = shape_of(wl, True)
+    ref = oracle.dispatch_layout(ids, np.arange(wl.E), wl.E, wl.W)
+    y = synth.normal_bf16(0, 63, (shape.R, wl.H))
+    res = synth.make_residual(wl) if residual else None
+    lay = moe.Layout(shape)
+    ws = moe.workspace(shape)
+    moe.moe_dispatch_layout(dev_i32(ids), None, shape, lay, ws)
+    w32 = torch.from_numpy(w64.astype(np.float32)).cuda()
+    partial = torch.empty(shape.R_d_max, wl.H, dtype=torch.bfloat16, device="cuda")
+    out2 = torch.empty(wl.N, wl.H, dtype=torch.bfloat16, device="cuda")
+    out1 = torch.empty_like(out2)
+    r = None if res is None else dev_bf16(res)
+    moe.moe_combine(dev_bf16(y), w32, lay, shape, partial, r, out2)
+    moe.moe_combine(dev_bf16(y), w32, lay, shape, None, r, out1)
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    _, want = oracle.combine_dedup(oracle.widen_bf16(y), w64.astype(np.float32).astype(np.float64),
+                                   ref["pair_row"], ref["pair_dedup_row"], ref["n_dedup_rows"], res)
+    assert_close(host_f64(out1), want, "one-pass dedup combine")
