@@ -47,14 +47,26 @@ def run_layer(wl, dedup=False):
     assert_close(host_f64(out), ref["out"], "out")
 
 
-@pytest.mark.parametrize("dedup", [False, True])
-@pytest.mark.parametrize("wl", [
+EDGE = [
     synth.Workload("one_expert", 300, 128, 1, 1, 128, 1),
     synth.Workload("one_token", 1, 256, 8, 2, 128, 2),
     synth.Workload("one_token_one_expert", 1, 64, 1, 1, 64, 1),
     synth.Workload("narrow16", 200, 16, 4, 2, 16, 2),
     synth.Workload("narrow8", 130, 8, 4, 2, 8, 4),
     synth.Workload("wide_i_small_h", 300, 64, 4, 2, 1000, 2),
-], ids=lambda w: w.name)
+]
+
+
+@pytest.mark.parametrize("dedup", [False, True])
+@pytest.mark.parametrize("wl", EDGE, ids=lambda w: w.name)
 def test_layer_edge_shapes(wl, dedup):
+    run_layer(wl, dedup)
+
+
+@pytest.mark.parametrize("dedup", [False, True])
+@pytest.mark.parametrize("wl", EDGE, ids=lambda w: w.name)
+def test_layer_edge_shapes_on_cta_pairs(wl, dedup, monkeypatch):
+    """The same shapes on the CTA-pair GEMMs (forced): fewer tiles than pairs,
+    so most pairs find the tile queue exhausted at once; tiles of one row."""
+    monkeypatch.setenv("MOE_GEMM_PAIR", "1")
     run_layer(wl, dedup)
