@@ -121,14 +121,26 @@ TRAFFIC_SOURCES = ("combine_warp_top_gb300/csrc/grouped_gemm.cu",
                    "combine_warp_top_gb300/csrc/ptx.cuh")
 
 
+def code_lines(text):
+    """The lines of a C++/CUDA source that are code: // comments, trailing
+    blanks and empty lines removed (the sources hold no '//' inside strings)."""
+    out = []
+    for line in text.splitlines():
+        code = line.split("//", 1)[0].rstrip()
+        if code:
+            out.append(code)
+    return "\n".join(out)
+
+
 def sources_digest():
-    """sha256 prefix over the grouped-GEMM sources (both kernels and their PTX
-    wrappers): a recorded DRAM traffic figure holds only for these bytes."""
+    """sha256 prefix over the code of the grouped-GEMM sources (both kernels and
+    their PTX wrappers, comments ignored): a recorded DRAM traffic figure holds
+    only for this code."""
     import hashlib
     h = hashlib.sha256()
     for rel in TRAFFIC_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            h.update(code_lines(f.read()).encode())
     return h.hexdigest()[:16]
 
 

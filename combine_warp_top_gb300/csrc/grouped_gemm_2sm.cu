@@ -23,10 +23,11 @@
 // Tiles are handed out dynamically: a scheduler warp of the leader (warp 6)
 // takes tile indices from a global counter and publishes them in a small
 // queue in both CTAs' shared memory, one tile ahead of the leader's producer
-// (so the tiles in flight over the whole GPU stay about two per pair).  In the leader the producer, the MMA thread and the epilogue warps
-// read that queue; in the peer only the producer does, and it forwards each
-// tile to its epilogue warps through a second, CTA-local queue, so a tile
-// costs one cluster-scope release each way and none on a loading thread.
+// (so the tiles in flight over the whole GPU stay about two per pair).  In the
+// leader the producer, the MMA thread and the epilogue warps read that queue;
+// in the peer only the producer does, and it forwards each tile to its
+// epilogue warps through a second, CTA-local queue, so a tile costs one
+// cluster-scope release each way and none on a loading thread.
 // Pairs that run faster simply take more tiles, so the tiles in flight stay
 // close to consecutive in the schedule's order and blocks that neighbouring
 // tiles share are still in L2 when they are needed (a static round-robin

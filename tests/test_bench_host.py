@@ -81,6 +81,10 @@ def test_recorded_traffic_follows_the_gemm_sources(tmp_path, monkeypatch):
     args = bench.parse_args(["--workload", "mixtral"])
     assert bench.recorded_traffic(bench.workload(args)) == 123
     assert bench.recorded_traffic(bench.workload(bench.parse_args([]))) is None
+    # a comment does not change the code the capture was taken on; code does
     with open(tmp_path / bench.TRAFFIC_SOURCES[2], "a") as f:
-        f.write("// changed\n")
+        f.write("// a comment\n")
+    assert bench.recorded_traffic(bench.workload(args)) == 123
+    with open(tmp_path / bench.TRAFFIC_SOURCES[2], "a") as f:
+        f.write("static int changed_code;\n")
     assert bench.recorded_traffic(bench.workload(args)) is None
