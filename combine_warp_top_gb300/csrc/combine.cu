@@ -362,11 +362,14 @@ cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& 
         const uint4* yy = reinterpret_cast<const uint4*>(y);
         uint4* o = reinterpret_cast<uint4*>(out);
         if (U == 4)
-            combine_kernel<4><<<warps_grid(s.N), kThreads, 0, st>>>(yy, w, L.pair_row, s.N, C, s.k, R, sh, res, o);
+            combine_kernel<4><<<warps_grid(s.N), kThreads, 0, st>>>(yy, w, L.pair_row, s.N, C,
+                                                                     s.k, R, sh, res, o);
         else if (U == 2)
-            combine_kernel<2><<<warps_grid(s.N), kThreads, 0, st>>>(yy, w, L.pair_row, s.N, C, s.k, R, sh, res, o);
+            combine_kernel<2><<<warps_grid(s.N), kThreads, 0, st>>>(yy, w, L.pair_row, s.N, C,
+                                                                     s.k, R, sh, res, o);
         else
-            combine_kernel<1><<<warps_grid(s.N), kThreads, 0, st>>>(yy, w, L.pair_row, s.N, C, s.k, R, sh, res, o);
+            combine_kernel<1><<<warps_grid(s.N), kThreads, 0, st>>>(yy, w, L.pair_row, s.N, C,
+                                                                     s.k, R, sh, res, o);
         return cudaGetLastError();
     }
     const int Rd_max = s.N * (s.k < s.W ? s.k : s.W);
@@ -392,23 +395,29 @@ cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& 
     const int Ur = kr <= 2 ? 4 : (kr <= 4 ? 2 : 1);
     if (Ur == 4)
         rank_reduce_kernel<4><<<warps_grid(Rd_max), kThreads, 0, st>>>(
-            yy, w, L.pair_row, L.pair_dedup_row, L.dedup_row_token, L.n_dedup_rows, s.N, C, s.k, R, pp);
+            yy, w, L.pair_row, L.pair_dedup_row, L.dedup_row_token, L.n_dedup_rows, s.N, C, s.k,
+            R, pp);
     else if (Ur == 2)
         rank_reduce_kernel<2><<<warps_grid(Rd_max), kThreads, 0, st>>>(
-            yy, w, L.pair_row, L.pair_dedup_row, L.dedup_row_token, L.n_dedup_rows, s.N, C, s.k, R, pp);
+            yy, w, L.pair_row, L.pair_dedup_row, L.dedup_row_token, L.n_dedup_rows, s.N, C, s.k,
+            R, pp);
     else
         rank_reduce_kernel<1><<<warps_grid(Rd_max), kThreads, 0, st>>>(
-            yy, w, L.pair_row, L.pair_dedup_row, L.dedup_row_token, L.n_dedup_rows, s.N, C, s.k, R, pp);
+            yy, w, L.pair_row, L.pair_dedup_row, L.dedup_row_token, L.n_dedup_rows, s.N, C, s.k,
+            R, pp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     uint4* o = reinterpret_cast<uint4*>(out);
     const uint4* cp = reinterpret_cast<const uint4*>(partial);
     if (U == 4)
-        owner_sum_kernel<4><<<warps_grid(s.N), kThreads, 0, st>>>(cp, L.pair_dedup_row, s.N, C, s.k, Rd_max, sh, res, o);
+        owner_sum_kernel<4><<<warps_grid(s.N), kThreads, 0, st>>>(
+            cp, L.pair_dedup_row, s.N, C, s.k, Rd_max, sh, res, o);
     else if (U == 2)
-        owner_sum_kernel<2><<<warps_grid(s.N), kThreads, 0, st>>>(cp, L.pair_dedup_row, s.N, C, s.k, Rd_max, sh, res, o);
+        owner_sum_kernel<2><<<warps_grid(s.N), kThreads, 0, st>>>(
+            cp, L.pair_dedup_row, s.N, C, s.k, Rd_max, sh, res, o);
     else
-        owner_sum_kernel<1><<<warps_grid(s.N), kThreads, 0, st>>>(cp, L.pair_dedup_row, s.N, C, s.k, Rd_max, sh, res, o);
+        owner_sum_kernel<1><<<warps_grid(s.N), kThreads, 0, st>>>(
+            cp, L.pair_dedup_row, s.N, C, s.k, Rd_max, sh, res, o);
     return cudaGetLastError();
 }
 

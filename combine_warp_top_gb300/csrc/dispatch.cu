@@ -35,11 +35,10 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 
 // dest_of_pair: pair_row (plain) or pair_dedup_row (dedup), [N*k].  Warp g
 // copies slice g % slices of token g / slices.
-__global__ void __launch_bounds__(kThreads) dispatch_kernel(const uint4* __restrict__ x, int N,
-                                                            int C, int k,
-                                                            const int32_t* __restrict__ dest_of_pair,
-                                                            int dedup, int row_bound,
-                                                            uint4* __restrict__ xd) {
+__global__ void __launch_bounds__(kThreads)
+    dispatch_kernel(const uint4* __restrict__ x, int N, int C, int k,
+                    const int32_t* __restrict__ dest_of_pair, int dedup, int row_bound,
+                    uint4* __restrict__ xd) {
     const int lane = threadIdx.x & 31;
     const long long g = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
     const int slices = (C + 32 * kUnroll - 1) / (32 * kUnroll);
