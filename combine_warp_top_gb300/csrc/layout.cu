@@ -150,28 +150,41 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
     return r;
 }
 
-// Exclusive column scan over the layout blocks of column c of a [nb][ncol]
-// table, in place; returns the column total.
-__device__ int column_scan(int32_t* __restrict__ tab, int nb, int ncol, int c) {
-    int run = 0;
-    int b = 0;
-    for (; b + 4 <= nb; b += 4) {
-        const int c0 = tab[(size_t)(b + 0) * ncol + c];
-        const int c1 = tab[(size_t)(b + 1) * ncol + c];
-        const int c2 = tab[(size_t)(b + 2) * ncol + c];
-        const int c3 = tab[(size_t)(b + 3) * ncol + c];
-        tab[(size_t)(b + 0) * ncol + c] = run;
-        tab[(size_t)(b + 1) * ncol + c] = run + c0;
-        tab[(size_t)(b + 2) * ncol + c] = run + c0 + c1;
-        tab[(size_t)(b + 3) * ncol + c] = run + c0 + c1 + c2;
-        run += c0 + c1 + c2 + c3;
+// Exclusive scan down every column of a [nb][ncol] table, in place, by the
+// whole block: the columns' rows are split into P = blockDim / ncol parts; each
+// thread sums its part (independent loads), the parts of a column are scanned
+// in shared memory, and each thread rewrites its rows with the running prefix.
+// totals[c] receives the column sum.  part_sums holds blockDim ints.
+__device__ void columns_scan(int32_t* __restrict__ tab, int nb, int ncol, int* part_sums,
+                             int* totals) {
+    const int P = blockDim.x / ncol;  // ncol <= blockDim
+    const int c = threadIdx.x % ncol, part = threadIdx.x / ncol;
+    const int L = (nb + P - 1) / P;
+    const int b0 = part * L, b1 = min(nb, b0 + L);
+    int sum = 0;
+    if (part < P)
+        for (int b = b0; b < b1; ++b) sum += tab[(size_t)b * ncol + c];
+    if (part < P) part_sums[part * ncol + c] = sum;
+    __syncthreads();
+    if (threadIdx.x < ncol) {
+        int run = 0;
+        for (int q = 0; q < P; ++q) {
+            const int v = part_sums[q * ncol + threadIdx.x];
+            part_sums[q * ncol + threadIdx.x] = run;
+            run += v;
+        }
+        totals[threadIdx.x] = run;
     }
-    for (; b < nb; ++b) {
-        const int c0 = tab[(size_t)b * ncol + c];
-        tab[(size_t)b * ncol + c] = run;
-        run += c0;
+    __syncthreads();
+    if (part < P) {
+        int run = part_sums[part * ncol + c];
+        for (int b = b0; b < b1; ++b) {
+            const int v = tab[(size_t)b * ncol + c];
+            tab[(size_t)b * ncol + c] = run;
+            run += v;
+        }
     }
-    return run;
+    __syncthreads();
 }
 
 __global__ void __launch_bounds__(1024) layout_scan_kernel(
@@ -180,9 +193,12 @@ __global__ void __launch_bounds__(1024) layout_scan_kernel(
     int32_t* __restrict__ slot_start, moe_layout L) {
     __shared__ int warp_sums[32];
     __shared__ int total;
+    __shared__ int part_sums[1024];
+    __shared__ int col_totals[1024];
     const int p = threadIdx.x;  // blockDim.x == 1024 >= E >= W
 
-    const int cnt = p < E ? column_scan(blk_counts, nb, E, p) : 0;
+    columns_scan(blk_counts, nb, E, part_sums, col_totals);
+    const int cnt = p < E ? col_totals[p] : 0;
     const int start = block_exclusive_scan(cnt, warp_sums, &total);
     const int R = total;
     __syncthreads();
@@ -201,7 +217,8 @@ __global__ void __launch_bounds__(1024) layout_scan_kernel(
         L.rank_offsets[W] = R;
     }
     if (!dedup) return;
-    const int rcnt = p < W ? column_scan(blk_rcounts, nb, W, p) : 0;
+    columns_scan(blk_rcounts, nb, W, part_sums, col_totals);
+    const int rcnt = p < W ? col_totals[p] : 0;
     const int rstart = block_exclusive_scan(rcnt, warp_sums, &total);
     const int Rd = total;
     if (p < W) {
