@@ -22,6 +22,12 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kBatch = 8;  // source rows loaded together
+// Dedup combine: one 16-byte chunk per lane and step, up to eight source rows
+// loaded together, at 60 registers (32 warps per SM).  Wider chunks need a
+// second set of fp32 partials and halve the warps per SM; at four chunks the
+// kernel ran 1.85x slower on the k = 6 correlated shape.
+constexpr int kDedupU = 1;
+constexpr int kDedupB = 8;
 
 __device__ __forceinline__ int clamp_row(int r, int bound) {
     return (unsigned)r < (unsigned)bound ? r : 0;
@@ -242,75 +248,79 @@ __global__ void __launch_bounds__(kThreads, U == 4 ? 2 : 3) owner_sum_kernel(
 // partials are summed in fp32 in that order, then the shared row and the
 // residual are added.  Bit-identical to the two-kernel form, without writing
 // the partials out and reading them back.
-template <int U>
+//
+// The token's k source rows are put in that (d, j) order once; the row loop
+// then loads B of them at a time whatever the groups, and a partial is
+// rounded and added where its group ends, so the loads of several dedup rows
+// are in flight together.
+template <int U, int B>
 __global__ void __launch_bounds__(kThreads, U == 1 ? 4 : (U == 2 ? 2 : 1)) dedup_combine_kernel(
     const uint4* __restrict__ y, const float* __restrict__ topk_w,
     const int32_t* __restrict__ pair_row, const int32_t* __restrict__ pair_dedup_row, int N,
     int C, int k, int R, int Rd_bound, const uint4* shared, const uint4* residual, uint4* out) {
-    constexpr int kRows = kBatch / U;  // source rows kept in registers per step
     const int lane = threadIdx.x & 31;
     const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
     if (t >= N) return;
-    const int my_row = lane < k ? clamp_row(pair_row[(size_t)t * k + lane], R) : 0;
-    const float my_w = lane < k ? topk_w[(size_t)t * k + lane] : 0.f;
-    const int my_d = lane < k ? clamp_row(pair_dedup_row[(size_t)t * k + lane], Rd_bound) : -1;
-    // group of lane j = number of distinct dedup rows below my_d
-    bool first = lane < k;
+    const bool live = lane < k;
+    const int my_row = live ? clamp_row(pair_row[(size_t)t * k + lane], R) : 0;
+    const float my_w = live ? topk_w[(size_t)t * k + lane] : 0.f;
+    const int my_d = live ? clamp_row(pair_dedup_row[(size_t)t * k + lane], Rd_bound) : -1;
+    // position of lane j in the (d, j) order: rows of smaller d, then the
+    // lanes below j with the same d
+    int pos = 0;
     for (int jj = 0; jj < k; ++jj) {
         const int o = __shfl_sync(0xffffffffu, my_d, jj);
-        if (jj < lane && o == my_d) first = false;
+        if (o < my_d || (o == my_d && jj < lane)) ++pos;
     }
-    const uint32_t firsts = __ballot_sync(0xffffffffu, first);
-    int group = 0;
+    // lane p takes the row, weight and dedup row at position p
+    int src = 0;
     for (int jj = 0; jj < k; ++jj) {
-        const int o = __shfl_sync(0xffffffffu, my_d, jj);
-        if (((firsts >> jj) & 1u) && o < my_d) ++group;
+        const int q = __shfl_sync(0xffffffffu, pos, jj);
+        if (q == lane) src = jj;
     }
-    const int ngroups = __popc(firsts);
+    const int s_row = __shfl_sync(0xffffffffu, my_row, src);
+    const float s_w = __shfl_sync(0xffffffffu, my_w, src);
+    const int s_d = __shfl_sync(0xffffffffu, my_d, src);
+    const int next_d = __shfl_down_sync(0xffffffffu, s_d, 1);
+    // bit p: position p is the last row of its dedup row
+    const uint32_t ends = __ballot_sync(0xffffffffu, live && (lane == k - 1 || next_d != s_d));
     for (int c0 = 0; c0 < C; c0 += 32 * U) {
-        float acc[U][8];
+        float acc[U][8], part[U][8];
         zero(acc);
-        if (k <= kRows) {
-            // every source row of this step loaded together, then summed group by group
-            uint4 v[kRows][U];
+        zero(part);
+        for (int p0 = 0; p0 < k; p0 += B) {
+            uint4 v[B][U];
 #pragma unroll
-            for (int b = 0; b < kRows; ++b) {
-                if (b < k) {
-                    const int r = __shfl_sync(0xffffffffu, my_row, b);
-                    const uint4* src = y + (size_t)r * C;
+            for (int b = 0; b < B; ++b) {
+                if (p0 + b < k) {
+                    const int r = __shfl_sync(0xffffffffu, s_row, p0 + b);
+                    const uint4* row = y + (size_t)r * C;
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
                         const int c = c0 + u * 32 + lane;
-                        if (c < C) v[b][u] = src[c];
+                        if (c < C) v[b][u] = row[c];
                     }
                 }
             }
-            for (int g = 0; g < ngroups; ++g) {
-                const uint32_t members = __ballot_sync(0xffffffffu, lane < k && group == g);
-                float part[U][8];
-                zero(part);
 #pragma unroll
-                for (int b = 0; b < kRows; ++b) {
-                    const float w = __shfl_sync(0xffffffffu, my_w, b);
-                    if ((members >> b) & 1u) {
+            for (int b = 0; b < B; ++b) {
+                const int p = p0 + b;
+                if (p < k) {
+                    const float w = __shfl_sync(0xffffffffu, s_w, p);
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int c = c0 + u * 32 + lane;
+                        if (c < C) acc_bf16x8(part[u], v[b][u], w);
+                    }
+                    if ((ends >> p) & 1u) {
 #pragma unroll
                         for (int u = 0; u < U; ++u) {
-                            const int c = c0 + u * 32 + lane;
-                            if (c < C) acc_bf16x8(part[u], v[b][u], w);
+                            add_bf16x8(acc[u], pack_bf16x8(part[u]));
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) part[u][i] = 0.f;
                         }
                     }
                 }
-#pragma unroll
-                for (int u = 0; u < U; ++u) add_bf16x8(acc[u], pack_bf16x8(part[u]));
-            }
-        } else {
-            for (int g = 0; g < ngroups; ++g) {
-                const uint32_t members = __ballot_sync(0xffffffffu, lane < k && group == g);
-                float part[U][8];
-                zero(part);
-                gather_weighted<U>(part, y, C, c0, members, my_row, my_w);
-#pragma unroll
-                for (int u = 0; u < U; ++u) add_bf16x8(acc[u], pack_bf16x8(part[u]));
             }
         }
         finish<U>(acc, shared, residual, out, (size_t)t * C, C, c0);
@@ -374,15 +384,8 @@ cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& 
     if (!partial) {
         // one pass, partials in registers (bit-identical to the two kernels below)
         uint4* o = reinterpret_cast<uint4*>(out);
-        if (U == 4)
-            dedup_combine_kernel<4><<<warps_grid(s.N), kThreads, 0, st>>>(
-                yy, w, L.pair_row, L.pair_dedup_row, s.N, C, s.k, R, Rd_max, sh, res, o);
-        else if (U == 2)
-            dedup_combine_kernel<2><<<warps_grid(s.N), kThreads, 0, st>>>(
-                yy, w, L.pair_row, L.pair_dedup_row, s.N, C, s.k, R, Rd_max, sh, res, o);
-        else
-            dedup_combine_kernel<1><<<warps_grid(s.N), kThreads, 0, st>>>(
-                yy, w, L.pair_row, L.pair_dedup_row, s.N, C, s.k, R, Rd_max, sh, res, o);
+        dedup_combine_kernel<kDedupU, kDedupB><<<warps_grid(s.N), kThreads, 0, st>>>(
+            yy, w, L.pair_row, L.pair_dedup_row, s.N, C, s.k, R, Rd_max, sh, res, o);
         return cudaGetLastError();
     }
     uint4* pp = reinterpret_cast<uint4*>(partial);
