@@ -13,4 +13,9 @@ SMALL = {
     "rank_per_expert": synth.Workload("rank_per_expert", 100, 128, 8, 3, 128, 8),
     "e256": synth.Workload("e256", 200, 128, 256, 8, 128, 8),
     "deep_k": synth.Workload("deep_k", 96, 1024, 4, 2, 320, 2),
+    # many experts per token: the combine loads a token's rows eight at a
+    # time, so these put dedup rows across that boundary (12 over 6 ranks,
+    # and the largest k the calls accept, 32 over 16 ranks)
+    "k12": synth.Workload("k12", 70, 264, 24, 12, 128, 6),
+    "k32": synth.Workload("k32", 40, 136, 64, 32, 128, 16),
 }

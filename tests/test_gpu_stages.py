@@ -158,7 +158,7 @@ LONG_ROWS = {
 @pytest.mark.parametrize("dedup", [False, True])
 @pytest.mark.parametrize("residual", [True, False])
 @pytest.mark.parametrize("name", ["tiny", "ragged", "wide", "k_eq_e", "one_rank", "e256",
-                                  "long_k5", "long_k2"])
+                                  "long_k5", "long_k2", "k12", "k32"])
 def test_combine_matches_oracle(name, dedup, residual):
     wl = {**SMALL, **LONG_ROWS}[name]
     L = synth.make_logits(wl)
@@ -207,19 +207,25 @@ def test_combine_in_place_on_residual():
 
 @pytest.mark.parametrize("residual", [True, False])
 @pytest.mark.parametrize("name", ["tiny", "ragged", "wide", "k_eq_e", "one_rank", "e256", "odd_h",
-                                  "deep_k", "long_k5", "long_k2"])
+                                  "deep_k", "long_k5", "long_k2", "k12", "k32", "k12_placed",
+                                  "k32_placed"])
 def test_dedup_combine_one_pass_equals_two_level(name, residual):
     """The one-pass dedup combine (partial = NULL: partials in registers) gives
-    the two-level form's output bit for bit, and both match the oracle."""
-    wl = {**SMALL, **LONG_ROWS}[name]
+    the two-level form's output bit for bit, and both match the oracle.  The
+    "_placed" cases put the experts on ranks by a seeded permutation, so the
+    ranks of a token's experts interleave in its j order."""
+    placed = name.endswith("_placed")
+    wl = {**SMALL, **LONG_ROWS}[name.removesuffix("_placed")]
     ids, w64 = oracle.route(synth.make_logits(wl), wl.k)
     shape = shape_of(wl, True)
-    ref = oracle.dispatch_layout(ids, np.arange(wl.E), wl.E, wl.W)
+    placement = synth.permutation(0, 53, wl.E).astype(np.int32) if placed else np.arange(wl.E)
+    ref = oracle.dispatch_layout(ids, placement, wl.E, wl.W)
     y = synth.normal_bf16(0, 63, (shape.R, wl.H))
     res = synth.make_residual(wl) if residual else None
     lay = moe.Layout(shape)
     ws = moe.workspace(shape)
-    moe.moe_dispatch_layout(dev_i32(ids), None, shape, lay, ws)
+    moe.moe_dispatch_layout(dev_i32(ids), dev_i32(placement.astype(np.int32)) if placed else None,
+                            shape, lay, ws)
     w32 = torch.from_numpy(w64.astype(np.float32)).cuda()
     partial = torch.empty(shape.R_d_max, wl.H, dtype=torch.bfloat16, device="cuda")
     out2 = torch.empty(wl.N, wl.H, dtype=torch.bfloat16, device="cuda")
