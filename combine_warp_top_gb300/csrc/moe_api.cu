@@ -77,6 +77,15 @@ GemmGroup dense_group(const moe_shape& s, void* ws) {
 
 inline cudaStream_t as_stream(void* p) { return reinterpret_cast<cudaStream_t>(p); }
 
+// The kernels move bf16 rows (and the fp32 accumulator) in 16-byte vectors,
+// by TMA, cp.async or plain vector loads: a base address that is not 16-byte
+// aligned is refused here instead of faulting on the device.  NULL passes
+// (whether NULL is allowed is checked separately).
+template <typename... T>
+inline bool aligned16(const T*... p) {
+    return ((((uintptr_t)p & 15u) == 0) && ...);
+}
+
 #define MOE_TRY(expr)                     \
     do {                                  \
         const moe_status _st = (expr);    \
@@ -139,6 +148,7 @@ moe_status moe_dispatch(const uint16_t* x, const moe_layout* layout, const moe_s
     MOE_TRY(check_layout(layout, shape));
     if (shape->N == 0) return MOE_OK;
     if (!x || !xd) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x, xd)) return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_dispatch(x, *layout, *shape, xd, as_stream(stream)));
 }
 
@@ -149,6 +159,7 @@ moe_status moe_expand(const uint16_t* xd, const moe_layout* layout, const moe_sh
     if (!shape->dedup) return MOE_ERR_INVALID_ARG;
     if (shape->N == 0) return MOE_OK;
     if (!xd || !xe) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(xd, xe)) return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_expand(xd, *layout, *shape, xe, as_stream(stream)));
 }
 
@@ -160,6 +171,7 @@ moe_status moe_ffn_gate_up(const uint16_t* rows, const moe_layout* layout, const
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (shape->N == 0) return MOE_OK;
     if (!rows || !w_gate || !w_up || !h) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(rows, w_gate, w_up, h)) return MOE_ERR_INVALID_ARG;
     const GemmGroup g = routed_group(*layout, *shape, ws);
     if (use_pair(g.R, g.E))
         return launch_gate_up_pair(rows, g, shape->H, shape->I, w_gate, w_up, h, as_stream(stream));
@@ -175,6 +187,7 @@ moe_status moe_ffn_gate_up_gather(const uint16_t* src, const int32_t* row_index,
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (shape->N == 0) return MOE_OK;
     if (!src || !row_index || !w_gate || !w_up || !h) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(src, w_gate, w_up, h)) return MOE_ERR_INVALID_ARG;
     if (src_rows <= 0 || src_rows >= ((int64_t)1 << 31)) return MOE_ERR_INVALID_ARG;
     return launch_gate_up(src, routed_group(*layout, *shape, ws), shape->H, shape->I, w_gate, w_up,
                           h, as_stream(stream), row_index, src_rows);
@@ -188,6 +201,7 @@ moe_status moe_ffn_down(const uint16_t* h, const moe_layout* layout, const moe_s
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (shape->N == 0) return MOE_OK;
     if (!h || !w_down || !y) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(h, w_down, y)) return MOE_ERR_INVALID_ARG;
     const GemmGroup g = routed_group(*layout, *shape, ws);
     if (use_pair(g.R, g.E))
         return launch_down_pair(h, g, shape->H, shape->I, w_down, y, as_stream(stream));
@@ -203,6 +217,7 @@ moe_status moe_ffn_down_combine(const uint16_t* h, const float* topk_w, const mo
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (shape->N == 0) return MOE_OK;
     if (!h || !topk_w || !w_down || !acc || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(h, w_down, residual, acc, out)) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = as_stream(stream);
     if (cudaMemsetAsync(acc, 0, (size_t)shape->N * shape->H * sizeof(float), st) != cudaSuccess)
         return MOE_ERR_CUDA;
@@ -221,6 +236,7 @@ moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const mo
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (shape->N == 0) return MOE_OK;
     if (!xd || !w_gate || !w_up || !w_down || !h || !y) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(xd, w_gate, w_up, w_down, h, y)) return MOE_ERR_INVALID_ARG;
     (void)xe;
     if (shape->dedup) {
         // the expansion to expert-major order is done by the GEMM's gather
@@ -241,6 +257,7 @@ moe_status moe_combine(const uint16_t* y, const float* topk_w, const moe_layout*
     MOE_TRY(check_layout(layout, shape));
     if (shape->N == 0) return MOE_OK;
     if (!y || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y, partial, residual, out)) return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_combine(y, topk_w, *layout, *shape, partial, nullptr, residual, out,
                                       as_stream(stream)));
 }
@@ -255,6 +272,7 @@ moe_status moe_shared_expert_ffn(const uint16_t* x, const moe_shape* shape, int3
     if (I_shared % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (shape->N == 0) return MOE_OK;
     if (!x || !w_gate_s || !w_up_s || !w_down_s || !h_s || !y_s) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x, w_gate_s, w_up_s, w_down_s, h_s, y_s)) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = as_stream(stream);
     const GemmGroup g = dense_group(*shape, ws);
     MOE_TRY(cuda_status(launch_dense_group(shape->N, const_cast<int32_t*>(g.counts),
@@ -274,6 +292,7 @@ moe_status moe_combine_shared(const uint16_t* y, const float* topk_w, const moe_
     MOE_TRY(check_layout(layout, shape));
     if (shape->N == 0) return MOE_OK;
     if (!y || !topk_w || !out || !y_shared) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y, partial, y_shared, residual, out)) return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_combine(y, topk_w, *layout, *shape, partial, y_shared, residual, out,
                                       as_stream(stream)));
 }
@@ -291,6 +310,8 @@ moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32
     if (shape->N == 0) return MOE_OK;
     if (!logits || !x || !w_gate || !w_up || !w_down || !topk_ids || !topk_w || !xd || !h ||
         !y || !out)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x, w_gate, w_up, w_down, residual, xd, xe, h, y, partial, out))
         return MOE_ERR_INVALID_ARG;
     MOE_TRY(moe_route(logits, shape, topk_ids, topk_w, stream));
     MOE_TRY(moe_dispatch_layout(topk_ids, placement, shape, layout, ws, ws_bytes, stream));

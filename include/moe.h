@@ -14,7 +14,9 @@
  *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
  *    allocates and frees nothing and keeps no global state besides cached
  *    device attributes.  bf16 tensors are passed as uint16_t (bit patterns).
- *    Every tensor is dense, row-major, and 16-byte aligned.
+ *    Every tensor is dense, row-major, and 16-byte aligned; a bf16 tensor (or
+ *    the fp32 accumulator of moe_ffn_down_combine) whose base is not 16-byte
+ *    aligned is refused with MOE_ERR_INVALID_ARG.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
  *    asynchronous on it, except moe_get_error.
  *  - Argument checks run on the host before any launch and return

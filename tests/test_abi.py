@@ -56,6 +56,28 @@ def test_host_side_checks_without_gpu(lib):
     assert lib.moe_status_str(5) == b"device-side wait timed out"
 
 
+def test_misaligned_rows_are_refused_without_gpu(lib):
+    """A bf16 base address off the 16-byte grid (a view that starts one element
+    into a tensor, say) is refused on the host, before any launch: the kernels
+    move rows in 16-byte vectors."""
+    shape = moe.Shape(64, 64, 8, 2, 2, 64)
+    c = ctypes.byref(shape.c())
+    fake = ctypes.c_void_p(0x10000)   # never dereferenced on the host
+    odd = ctypes.c_void_p(0x10002)    # bf16 element 1 of a tensor at 0x10000
+    lay = moe.MoeLayout(*([0x20000] * len(moe.LAYOUT_FIELDS)))
+    L = ctypes.byref(lay)
+    ws_bytes = ctypes.c_size_t(moe.moe_workspace_bytes(shape))
+    assert lib.moe_dispatch(odd, L, c, fake, None) == 1
+    assert lib.moe_dispatch(fake, L, c, odd, None) == 1
+    assert lib.moe_combine(odd, fake, L, c, None, None, fake, None) == 1
+    assert lib.moe_combine(fake, fake, L, c, None, odd, fake, None) == 1
+    assert lib.moe_combine(fake, fake, L, c, None, None, odd, None) == 1
+    assert lib.moe_ffn_gate_up(fake, L, c, fake, odd, fake, fake, ws_bytes, None) == 1
+    assert lib.moe_ffn_down(odd, L, c, fake, fake, fake, ws_bytes, None) == 1
+    assert lib.moe_ffn_gate_up_gather(odd, fake, ctypes.c_int64(64), L, c, fake, fake, fake,
+                                      fake, ws_bytes, None) == 1
+
+
 def test_workspace_grows_with_tokens(lib):
     small = moe.moe_workspace_bytes(moe.Shape(256, 64, 8, 2, 2, 64))
     large = moe.moe_workspace_bytes(moe.Shape(256 * 64, 64, 8, 2, 2, 64))

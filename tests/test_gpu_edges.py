@@ -70,3 +70,33 @@ def test_layer_edge_shapes_on_cta_pairs(wl, dedup, monkeypatch):
     so most pairs find the tile queue exhausted at once; tiles of one row."""
     monkeypatch.setenv("MOE_GEMM_PAIR", "1")
     run_layer(wl, dedup)
+
+
+def test_misaligned_view_is_refused_and_the_context_survives():
+    """A contiguous bf16 view that starts one element into its buffer is off the
+    16-byte grid the kernels' vector loads need: the call is refused on the host
+    with an invalid-argument status, nothing is launched, and the same call on
+    an aligned copy then matches the oracle."""
+    wl = synth.Workload("align", 64, 128, 8, 2, 64, 2)
+    ids, w64 = oracle.route(synth.make_logits(wl), wl.k)
+    shape = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I)
+    lay = moe.Layout(shape)
+    ws = moe.workspace(shape)
+    moe.moe_dispatch_layout(dev_i32(ids), None, shape, lay, ws)
+    ref = oracle.dispatch_layout(ids, np.arange(wl.E), wl.E, wl.W)
+    y = synth.normal_bf16(0, 65, (shape.R, wl.H))
+    res = synth.make_residual(wl)
+    w32 = torch.from_numpy(w64.astype(np.float32)).cuda()
+    buf = torch.empty(shape.R * wl.H + 8, dtype=torch.bfloat16, device="cuda")
+    y_odd = buf[1:1 + shape.R * wl.H].view(shape.R, wl.H)
+    y_odd.copy_(dev_bf16(y))
+    out = torch.empty(wl.N, wl.H, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe.MoeError) as info:
+        moe.moe_combine(y_odd, w32, lay, shape, None, dev_bf16(res), out)
+    assert info.value.status == 1  # MOE_ERR_INVALID_ARG
+    assert moe.moe_get_error(ws) == 0
+    moe.moe_combine(y_odd.clone(), w32, lay, shape, None, dev_bf16(res), out)
+    torch.cuda.synchronize()
+    want = oracle.combine(oracle.widen_bf16(y), w64.astype(np.float32).astype(np.float64),
+                          ref["pair_row"], res)
+    assert_close(host_f64(out), want, "combine after a refused call")
