@@ -131,9 +131,11 @@ def test_bad_placement_is_reported_by_the_device():
     assert moe.moe_get_error(ws) == 0
 
 
-def test_host_pipeline_matches_device_forward():
+@pytest.mark.parametrize("graphs", [True, False])
+def test_host_pipeline_matches_device_forward(graphs):
     """The overlapped host-buffer path returns, batch by batch, exactly what the
-    device-resident call returns."""
+    device-resident call returns, whether it replays a captured graph per
+    buffer set or calls the layer directly."""
     wl = SMALL["wide"]
     layer, _ = build_layer(wl, False)
     batches, want = [], []
@@ -144,7 +146,8 @@ def test_host_pipeline_matches_device_forward():
         out = torch.empty(wl.N, wl.H, dtype=torch.bfloat16).pin_memory()
         batches.append((L, x, r, out))
         want.append(layer.forward(L.cuda(), x.cuda(), r.cuda()).cpu().clone())
-    pipe = moe.HostPipeline(layer)
+    pipe = moe.HostPipeline(layer, graphs=graphs)
+    assert (pipe.graphs is not None) == graphs
     pipe.run(batches)
     torch.cuda.synchronize()
     for (_, _, _, out), w in zip(batches, want):
