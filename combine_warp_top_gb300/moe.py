@@ -110,6 +110,49 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _sized(t, count, esize, what):
+    """Pointer of t after checking that it holds at least `count` elements of
+    `esize` bytes: what the C call reads or writes for its shape.  The C ABI
+    sees only pointers, so a smaller tensor would send the kernels out of
+    bounds.  None passes (the C call decides whether NULL is allowed)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what}: expected a torch tensor")
+    if t.element_size() != esize:
+        raise ValueError(f"{what}: expected {esize}-byte elements, got {t.dtype}")
+    if t.numel() < count:
+        raise ValueError(f"{what}: {t.numel()} elements, the shape needs {count}")
+    return _ptr(t)
+
+
+def _bf16(t, count, what):
+    return _sized(t, count, 2, what)
+
+
+def _i32(t, count, what):
+    return _sized(t, count, 4, what)
+
+
+def _f32(t, count, what):
+    return _sized(t, count, 4, what)
+
+
+def _ws(ws):
+    """(pointer, size in bytes) of a workspace tensor of any dtype."""
+    return _ptr(ws), ws.numel() * ws.element_size()
+
+
+def _lay(layout, shape):
+    """The C struct of a layout built for this shape's E, k and W, for at least
+    its N tokens, with the dedup arrays if the shape deduplicates."""
+    ls = layout.shape
+    if (ls.E, ls.k, ls.W) != (shape.E, shape.k, shape.W) or ls.N < shape.N or \
+            (shape.dedup and not ls.dedup):
+        raise ValueError("the layout was built for another shape")
+    return ctypes.byref(layout.c)
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -144,6 +187,7 @@ class Layout:
     """Device arrays of one dispatch layout (see moe_layout in include/moe.h)."""
 
     def __init__(self, shape: Shape, device="cuda"):
+        self.shape = shape
         N, E, k, W = shape.N, shape.E, shape.k, shape.W
         i32 = dict(dtype=torch.int32, device=device)
         sizes = dict(expert_counts=E, expert_offsets=E + 1, rank_offsets=W + 1,
@@ -171,72 +215,109 @@ def workspace(shape: Shape, device="cuda") -> torch.Tensor:
 
 
 # ---- the C entry points ----------------------------------------------------------------
+# Each wrapper checks its tensors' element sizes and lengths against the shape
+# (the C side cannot), then passes plain pointers.
+
+def _rows_d(shape: Shape) -> int:
+    return shape.R_d_max if shape.dedup else shape.R
+
 
 def moe_route(logits, shape: Shape, topk_ids, topk_w, stream=None):
-    _check(load().moe_route(_ptr(logits), ctypes.byref(shape.c()), _ptr(topk_ids), _ptr(topk_w),
+    s = shape
+    _check(load().moe_route(_f32(logits, s.N * s.E, "logits"), ctypes.byref(s.c()),
+                            _i32(topk_ids, s.R, "topk_ids"), _f32(topk_w, s.R, "topk_w"),
                             _stream(stream)), "moe_route")
 
 
 def moe_route_full_softmax(logits, shape: Shape, topk_ids, topk_w, stream=None):
-    _check(load().moe_route_full_softmax(_ptr(logits), ctypes.byref(shape.c()), _ptr(topk_ids),
-                                         _ptr(topk_w), _stream(stream)), "moe_route_full_softmax")
+    s = shape
+    _check(load().moe_route_full_softmax(_f32(logits, s.N * s.E, "logits"), ctypes.byref(s.c()),
+                                         _i32(topk_ids, s.R, "topk_ids"),
+                                         _f32(topk_w, s.R, "topk_w"), _stream(stream)),
+           "moe_route_full_softmax")
 
 
 def moe_route_sigmoid_bias(logits, bias, shape: Shape, topk_ids, topk_w, stream=None):
-    _check(load().moe_route_sigmoid_bias(_ptr(logits), _ptr(bias), ctypes.byref(shape.c()),
-                                         _ptr(topk_ids), _ptr(topk_w), _stream(stream)),
+    s = shape
+    _check(load().moe_route_sigmoid_bias(_f32(logits, s.N * s.E, "logits"),
+                                         _f32(bias, s.E, "bias"), ctypes.byref(s.c()),
+                                         _i32(topk_ids, s.R, "topk_ids"),
+                                         _f32(topk_w, s.R, "topk_w"), _stream(stream)),
            "moe_route_sigmoid_bias")
 
 
 def moe_dispatch_layout(topk_ids, placement, shape: Shape, layout: Layout, ws, stream=None):
-    _check(load().moe_dispatch_layout(_ptr(topk_ids), _ptr(placement), ctypes.byref(shape.c()),
-                                      ctypes.byref(layout.c), _ptr(ws), ws.numel(),
-                                      _stream(stream)), "moe_dispatch_layout")
+    s = shape
+    _check(load().moe_dispatch_layout(_i32(topk_ids, s.R, "topk_ids"),
+                                      _i32(placement, s.E, "placement"), ctypes.byref(s.c()),
+                                      _lay(layout, s), *_ws(ws), _stream(stream)),
+           "moe_dispatch_layout")
 
 
 def moe_dispatch_layout_noalloc(topk_ids, placement, shape: Shape, layout: Layout, stream=None):
-    _check(load().moe_dispatch_layout_noalloc(_ptr(topk_ids), _ptr(placement),
-                                              ctypes.byref(shape.c()), ctypes.byref(layout.c),
+    s = shape
+    _check(load().moe_dispatch_layout_noalloc(_i32(topk_ids, s.R, "topk_ids"),
+                                              _i32(placement, s.E, "placement"),
+                                              ctypes.byref(s.c()), _lay(layout, s),
                                               _stream(stream)), "moe_dispatch_layout_noalloc")
 
 
 def moe_dispatch(x, layout: Layout, shape: Shape, xd, stream=None):
-    _check(load().moe_dispatch(_ptr(x), ctypes.byref(layout.c), ctypes.byref(shape.c()), _ptr(xd),
-                               _stream(stream)), "moe_dispatch")
+    s = shape
+    _check(load().moe_dispatch(_bf16(x, s.N * s.H, "x"), _lay(layout, s), ctypes.byref(s.c()),
+                               _bf16(xd, _rows_d(s) * s.H, "xd"), _stream(stream)),
+           "moe_dispatch")
 
 
 def moe_expert_ffn(xd, layout: Layout, shape: Shape, w_gate, w_up, w_down, xe, h, y, ws,
                    stream=None):
-    _check(load().moe_expert_ffn(_ptr(xd), ctypes.byref(layout.c), ctypes.byref(shape.c()),
-                                 _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(xe), _ptr(h), _ptr(y),
-                                 _ptr(ws), ws.numel(), _stream(stream)), "moe_expert_ffn")
+    s = shape
+    _check(load().moe_expert_ffn(_bf16(xd, _rows_d(s) * s.H, "xd"), _lay(layout, s),
+                                 ctypes.byref(s.c()), _bf16(w_gate, s.E * s.I * s.H, "w_gate"),
+                                 _bf16(w_up, s.E * s.I * s.H, "w_up"),
+                                 _bf16(w_down, s.E * s.H * s.I, "w_down"), _ptr(xe),
+                                 _bf16(h, s.R * s.I, "h"), _bf16(y, s.R * s.H, "y"), *_ws(ws),
+                                 _stream(stream)), "moe_expert_ffn")
 
 
 def moe_expand(xd, layout: Layout, shape: Shape, xe, stream=None):
-    _check(load().moe_expand(_ptr(xd), ctypes.byref(layout.c), ctypes.byref(shape.c()), _ptr(xe),
-                             _stream(stream)), "moe_expand")
+    s = shape
+    _check(load().moe_expand(_bf16(xd, s.R_d_max * s.H, "xd"), _lay(layout, s),
+                             ctypes.byref(s.c()), _bf16(xe, s.R * s.H, "xe"), _stream(stream)),
+           "moe_expand")
 
 
 def moe_ffn_gate_up(rows, layout: Layout, shape: Shape, w_gate, w_up, h, ws, stream=None):
-    _check(load().moe_ffn_gate_up(_ptr(rows), ctypes.byref(layout.c), ctypes.byref(shape.c()),
-                                  _ptr(w_gate), _ptr(w_up), _ptr(h), _ptr(ws), ws.numel(),
-                                  _stream(stream)), "moe_ffn_gate_up")
+    s = shape
+    _check(load().moe_ffn_gate_up(_bf16(rows, s.R * s.H, "rows"), _lay(layout, s),
+                                  ctypes.byref(s.c()), _bf16(w_gate, s.E * s.I * s.H, "w_gate"),
+                                  _bf16(w_up, s.E * s.I * s.H, "w_up"), _bf16(h, s.R * s.I, "h"),
+                                  *_ws(ws), _stream(stream)), "moe_ffn_gate_up")
 
 
 def moe_ffn_gate_up_gather(src, row_index, layout: Layout, shape: Shape, w_gate, w_up, h, ws,
                            stream=None):
-    _check(load().moe_ffn_gate_up_gather(_ptr(src), _ptr(row_index), src.shape[0],
-                                         ctypes.byref(layout.c), ctypes.byref(shape.c()),
-                                         _ptr(w_gate), _ptr(w_up), _ptr(h), _ptr(ws), ws.numel(),
-                                         _stream(stream)), "moe_ffn_gate_up_gather")
+    """src: the [src_rows, H] rows that row_index points into."""
+    s = shape
+    src_rows = src.numel() // s.H
+    _check(load().moe_ffn_gate_up_gather(_bf16(src, src_rows * s.H, "src"),
+                                         _i32(row_index, s.R, "row_index"), src_rows,
+                                         _lay(layout, s), ctypes.byref(s.c()),
+                                         _bf16(w_gate, s.E * s.I * s.H, "w_gate"),
+                                         _bf16(w_up, s.E * s.I * s.H, "w_up"),
+                                         _bf16(h, s.R * s.I, "h"), *_ws(ws), _stream(stream)),
+           "moe_ffn_gate_up_gather")
 
 
 def moe_ffn_down_combine(h, topk_w, layout: Layout, shape: Shape, w_down, residual, acc, out,
                          ws, stream=None):
-    _check(load().moe_ffn_down_combine(_ptr(h), _ptr(topk_w), ctypes.byref(layout.c),
-                                       ctypes.byref(shape.c()), _ptr(w_down), _ptr(residual),
-                                       _ptr(acc), _ptr(out), _ptr(ws), ws.numel(),
-                                       _stream(stream)), "moe_ffn_down_combine")
+    s = shape
+    _check(load().moe_ffn_down_combine(_bf16(h, s.R * s.I, "h"), _f32(topk_w, s.R, "topk_w"),
+                                       _lay(layout, s), ctypes.byref(s.c()),
+                                       _bf16(w_down, s.E * s.H * s.I, "w_down"),
+                                       _bf16(residual, s.N * s.H, "residual"),
+                                       _f32(acc, s.N * s.H, "acc"), _bf16(out, s.N * s.H, "out"),
+                                       *_ws(ws), _stream(stream)), "moe_ffn_down_combine")
 
 
 def moe_layer_skips_dispatch(shape: Shape) -> bool:
@@ -246,45 +327,67 @@ def moe_layer_skips_dispatch(shape: Shape) -> bool:
 
 
 def moe_ffn_down(h, layout: Layout, shape: Shape, w_down, y, ws, stream=None):
-    _check(load().moe_ffn_down(_ptr(h), ctypes.byref(layout.c), ctypes.byref(shape.c()),
-                               _ptr(w_down), _ptr(y), _ptr(ws), ws.numel(), _stream(stream)),
+    s = shape
+    _check(load().moe_ffn_down(_bf16(h, s.R * s.I, "h"), _lay(layout, s), ctypes.byref(s.c()),
+                               _bf16(w_down, s.E * s.H * s.I, "w_down"),
+                               _bf16(y, s.R * s.H, "y"), *_ws(ws), _stream(stream)),
            "moe_ffn_down")
 
 
 def moe_combine(y, topk_w, layout: Layout, shape: Shape, partial, residual, out, stream=None):
-    _check(load().moe_combine(_ptr(y), _ptr(topk_w), ctypes.byref(layout.c),
-                              ctypes.byref(shape.c()), _ptr(partial), _ptr(residual), _ptr(out),
-                              _stream(stream)), "moe_combine")
+    s = shape
+    _check(load().moe_combine(_bf16(y, s.R * s.H, "y"), _f32(topk_w, s.R, "topk_w"),
+                              _lay(layout, s), ctypes.byref(s.c()),
+                              _bf16(partial, s.R_d_max * s.H, "partial"),
+                              _bf16(residual, s.N * s.H, "residual"),
+                              _bf16(out, s.N * s.H, "out"), _stream(stream)), "moe_combine")
 
 
 def moe_layer_forward(logits, x, placement, w_gate, w_up, w_down, residual, shape: Shape,
                       topk_ids, topk_w, layout: Layout, xd, xe, h, y, partial, out, ws,
                       stream=None):
+    s = shape
+    # xd is not written when the dispatch is fused into the gate/up GEMM
+    xd_rows = 0 if moe_layer_skips_dispatch(s) else _rows_d(s)
     _check(load().moe_layer_forward(
-        _ptr(logits), _ptr(x), _ptr(placement), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
-        _ptr(residual), ctypes.byref(shape.c()), _ptr(topk_ids), _ptr(topk_w),
-        ctypes.byref(layout.c), _ptr(xd), _ptr(xe), _ptr(h), _ptr(y), _ptr(partial), _ptr(out),
-        _ptr(ws), ws.numel(), _stream(stream)), "moe_layer_forward")
+        _f32(logits, s.N * s.E, "logits"), _bf16(x, s.N * s.H, "x"),
+        _i32(placement, s.E, "placement"), _bf16(w_gate, s.E * s.I * s.H, "w_gate"),
+        _bf16(w_up, s.E * s.I * s.H, "w_up"), _bf16(w_down, s.E * s.H * s.I, "w_down"),
+        _bf16(residual, s.N * s.H, "residual"), ctypes.byref(s.c()),
+        _i32(topk_ids, s.R, "topk_ids"), _f32(topk_w, s.R, "topk_w"), _lay(layout, s),
+        _bf16(xd, xd_rows * s.H, "xd"), _ptr(xe), _bf16(h, s.R * s.I, "h"),
+        _bf16(y, s.R * s.H, "y"), _bf16(partial, s.R_d_max * s.H, "partial"),
+        _bf16(out, s.N * s.H, "out"), *_ws(ws), _stream(stream)), "moe_layer_forward")
 
 
 def moe_shared_expert_ffn(x, shape: Shape, I_shared: int, w_gate_s, w_up_s, w_down_s, h_s, y_s, ws,
                           stream=None):
-    _check(load().moe_shared_expert_ffn(_ptr(x), ctypes.byref(shape.c()), I_shared, _ptr(w_gate_s),
-                                        _ptr(w_up_s), _ptr(w_down_s), _ptr(h_s), _ptr(y_s), _ptr(ws),
-                                        ws.numel(), _stream(stream)), "moe_shared_expert_ffn")
+    s, Is = shape, I_shared
+    _check(load().moe_shared_expert_ffn(_bf16(x, s.N * s.H, "x"), ctypes.byref(s.c()), Is,
+                                        _bf16(w_gate_s, Is * s.H, "w_gate_s"),
+                                        _bf16(w_up_s, Is * s.H, "w_up_s"),
+                                        _bf16(w_down_s, s.H * Is, "w_down_s"),
+                                        _bf16(h_s, s.N * Is, "h_s"), _bf16(y_s, s.N * s.H, "y_s"),
+                                        *_ws(ws), _stream(stream)), "moe_shared_expert_ffn")
 
 
 def moe_combine_shared(y, topk_w, layout: Layout, shape: Shape, partial, y_shared, residual, out,
                        stream=None):
-    _check(load().moe_combine_shared(_ptr(y), _ptr(topk_w), ctypes.byref(layout.c),
-                                     ctypes.byref(shape.c()), _ptr(partial), _ptr(y_shared),
-                                     _ptr(residual), _ptr(out), _stream(stream)),
+    s = shape
+    _check(load().moe_combine_shared(_bf16(y, s.R * s.H, "y"), _f32(topk_w, s.R, "topk_w"),
+                                     _lay(layout, s), ctypes.byref(s.c()),
+                                     _bf16(partial, s.R_d_max * s.H, "partial"),
+                                     _bf16(y_shared, s.N * s.H, "y_shared"),
+                                     _bf16(residual, s.N * s.H, "residual"),
+                                     _bf16(out, s.N * s.H, "out"), _stream(stream)),
            "moe_combine_shared")
 
 
 def moe_coselection(topk_ids, shape: Shape, coselect, ws, stream=None):
-    _check(load().moe_coselection(_ptr(topk_ids), ctypes.byref(shape.c()), _ptr(coselect),
-                                  _ptr(ws), ws.numel(), _stream(stream)), "moe_coselection")
+    s = shape
+    _check(load().moe_coselection(_i32(topk_ids, s.R, "topk_ids"), ctypes.byref(s.c()),
+                                  _i32(coselect, s.E * s.E, "coselect"), *_ws(ws),
+                                  _stream(stream)), "moe_coselection")
 
 
 def moe_placement_search(coselect_host, ranks: int, nodes: int = 1, max_swaps: int = 1 << 20):

@@ -78,6 +78,49 @@ def test_misaligned_rows_are_refused_without_gpu(lib):
                                       fake, ws_bytes, None) == 1
 
 
+def test_binding_checks_sizes_against_the_shape(lib):
+    """The C calls see only pointers, so the Python binding checks each tensor's
+    element size and length against the shape before calling: an undersized
+    or wrongly typed tensor, or a layout built for another shape, raises
+    instead of sending a kernel out of bounds.  Each tensor is checked before
+    its device check, so host tensors show it here for the first argument."""
+    import torch
+    shape = moe.Shape(64, 128, 8, 2, 2, 64)
+    R, N, H, I, E = shape.R, shape.N, shape.H, shape.I, shape.E
+    lay = moe.Layout.__new__(moe.Layout)  # host-side stand-in: no device arrays
+    lay.shape = shape
+    lay.c = moe.MoeLayout()
+    bf = torch.bfloat16
+    out = torch.empty(N * H, dtype=bf)
+    with pytest.raises(ValueError, match="y: .* elements, the shape needs"):
+        moe.moe_combine(torch.empty(R * H - 1, dtype=bf), torch.empty(R), lay, shape, None, None,
+                        out)
+    with pytest.raises(ValueError, match="y: expected 2-byte elements"):
+        moe.moe_combine(torch.empty(R * H), torch.empty(R), lay, shape, None, None, out)
+    with pytest.raises(ValueError, match="h: .* elements"):
+        moe.moe_ffn_down(torch.empty(R * I - 8, dtype=bf), lay, shape,
+                         torch.empty(E * H * I, dtype=bf), torch.empty(R * H, dtype=bf),
+                         torch.empty(16, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="logits"):
+        moe.moe_route(torch.empty(N * E - 1), shape, torch.empty(R, dtype=torch.int32),
+                      torch.empty(R))
+    # a layout must come from a shape with the same E, k, W and at least N tokens
+    other = moe.Layout.__new__(moe.Layout)
+    other.shape = moe.Shape(32, 128, 8, 2, 2, 64)
+    with pytest.raises(ValueError, match="another shape"):
+        moe._lay(other, shape)
+    other.shape = moe.Shape(64, 128, 8, 2, 4, 64)
+    with pytest.raises(ValueError, match="another shape"):
+        moe._lay(other, shape)
+    with pytest.raises(ValueError, match="another shape"):
+        moe._lay(lay, moe.Shape(64, 128, 8, 2, 2, 64, dedup=True))
+    moe._lay(lay, moe.Shape(16, 128, 8, 2, 2, 64))  # fewer tokens fit
+    # correctly sized host tensors get as far as the device check
+    with pytest.raises(ValueError, match="device tensors"):
+        moe.moe_combine(torch.empty(R * H, dtype=bf), torch.empty(R), lay, shape, None, None,
+                        out)
+
+
 def test_workspace_grows_with_tokens(lib):
     small = moe.moe_workspace_bytes(moe.Shape(256, 64, 8, 2, 2, 64))
     large = moe.moe_workspace_bytes(moe.Shape(256 * 64, 64, 8, 2, 2, 64))

@@ -109,9 +109,15 @@ def test_invalid_arguments_are_rejected():
     with pytest.raises(moe.MoeError) as e:
         moe.moe_dispatch_layout(ids, None, good, lay, small_ws)
     assert e.value.status == 3
-    with pytest.raises(moe.MoeError):
-        moe.moe_dispatch_layout(ids, None, moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, True),
-                                lay, moe.workspace(good))  # dedup arrays missing
+    dshape = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, True)
+    ws = moe.workspace(dshape)
+    # a plain layout has no dedup arrays: the binding refuses it for a dedup
+    # shape, and so does the C call it would make
+    with pytest.raises(ValueError, match="another shape"):
+        moe.moe_dispatch_layout(ids, None, dshape, lay, ws)
+    st = lib.moe_dispatch_layout(ids.data_ptr(), None, ctypes.byref(dshape.c()),
+                                 ctypes.byref(lay.c), ws.data_ptr(), ws.numel(), None)
+    assert st == 1
 
 
 def test_bad_placement_is_reported_by_the_device():
