@@ -97,7 +97,8 @@ def check_invariants(layout_fn, ids, placement, E, W):
 
 
 @pytest.mark.parametrize("N,E,k,W", [(50, 8, 2, 2), (40, 16, 4, 4), (30, 6, 6, 3), (33, 8, 3, 8),
-                                     (25, 8, 8, 1), (64, 12, 1, 4)])
+                                     (25, 8, 8, 1), (64, 12, 1, 4), (40, 24, 12, 6),
+                                     (20, 64, 32, 16)])
 def test_layout_invariants(N, E, k, W):
     ids = random_ids(N, E, k, seed=N + E)
     check_invariants(oracle.dispatch_layout, ids, np.arange(E), E, W)
