@@ -37,6 +37,13 @@ def check_route_brute_force(route_fn):
         L = rng.integers(-3, 4, size=(1, E)).astype(np.float32) * np.float32(0.5)
         ids, w = route_fn(L, k)
         assert ids[0].tolist() == selected_by_definition(L[0].tolist(), k), (L, k, ids)
+    # many experts and up to the largest k the library accepts
+    for trial in range(40):
+        E = int(rng.integers(24, 65))
+        k = int(rng.integers(8, min(E, 32) + 1))
+        L = rng.integers(-4, 5, size=(1, E)).astype(np.float32) * np.float32(0.25)
+        ids, w = route_fn(L, k)
+        assert ids[0].tolist() == selected_by_definition(L[0].tolist(), k), (L, k, ids)
 
 
 def check_subset_sum_is_max(route_fn):
