@@ -193,3 +193,75 @@ def test_sigmoid_router_mutant_with_biased_weights_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "route_sigmoid_bias", mutant)
     with pytest.raises(AssertionError):
         route_pins.test_sigmoid_bias_router_pins()
+
+
+# ---- bf16 widening and the Table I counters ------------------------------------------
+
+import test_oracle_helpers as helper_pins  # noqa: E402
+
+
+def widen_shift_15(a):
+    """Slip: shift by 15 instead of 16."""
+    a = np.asarray(a, dtype=np.uint16)
+    return (a.astype(np.uint32) << 15).view(np.float32).astype(np.float64)
+
+
+def widen_drops_sign(a):
+    """Slip: the sign bit masked off."""
+    a = np.asarray(a, dtype=np.uint16) & np.uint16(0x7FFF)
+    return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def widen_nan_to_zero(a):
+    """Slip: non-finite patterns flushed to zero."""
+    v = oracle.widen_bf16(a)
+    return np.where(np.isfinite(v), v, 0.0)
+
+
+def widen_as_fp16(a):
+    """Slip: the bits read as IEEE half precision instead of bfloat16."""
+    return np.asarray(a, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def widen_low_half(a):
+    """Slip: the pattern put in the low half of the binary32 word."""
+    return np.asarray(a, dtype=np.uint16).astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("mutant", [widen_shift_15, widen_drops_sign, widen_nan_to_zero,
+                                    widen_as_fp16, widen_low_half])
+def test_widen_mutants_are_caught(mutant):
+    assert fails(helper_pins.WIDEN_PINS, mutant)
+
+
+def stats_share_counts_two_ranks(layout, N, k, W):
+    s = oracle.layout_stats(layout, N, k, W)
+    distinct = layout["rank_member"].sum(axis=1)
+    s["same_rank_share"] = float(np.mean(distinct <= 2))
+    return s
+
+
+def stats_ranks_over_rows(layout, N, k, W):
+    """Slip: distinct ranks divided by rows instead of tokens."""
+    s = oracle.layout_stats(layout, N, k, W)
+    s["ranks_per_token"] = layout["n_dedup_rows"] / (N * k)
+    return s
+
+
+def stats_reduction_inverted(layout, N, k, W):
+    s = oracle.layout_stats(layout, N, k, W)
+    s["dedup_reduction"] = layout["n_dedup_rows"] / (N * k)
+    return s
+
+
+def stats_load_over_max(layout, N, k, W):
+    """Slip: the mean load taken over the ranks instead of the experts."""
+    s = oracle.layout_stats(layout, N, k, W)
+    s["max_over_mean_load"] = float(layout["expert_counts"].max() / (N * k / W))
+    return s
+
+
+@pytest.mark.parametrize("mutant", [stats_share_counts_two_ranks, stats_ranks_over_rows,
+                                    stats_reduction_inverted, stats_load_over_max])
+def test_layout_stats_mutants_are_caught(mutant):
+    assert fails(helper_pins.STATS_PINS, mutant)
