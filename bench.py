@@ -44,6 +44,8 @@ def parse_args(argv=None):
     p.add_argument("--tokens", type=int, default=None, help="override N (profiling cases)")
     p.add_argument("--experts", type=int, default=None, help="override E (profiling cases)")
     p.add_argument("--dedup", choices=["auto", "on", "off"], default="auto")
+    p.add_argument("--gemm", choices=["auto", "single", "pair"], default="auto",
+                   help="grouped-GEMM kernel (the shape's gemm field)")
     p.add_argument("--placement-search", action="store_true",
                    help="place experts by the co-selection search before timing the layer")
     p.add_argument("--shared-expert", type=int, default=0, metavar="I_S",
@@ -385,7 +387,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     wl = workload(args)
     seed = rank  # every rank has its own tokens; weights are the same layer
-    shape = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=wl.dedup)
+    shape = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=wl.dedup, gemm=args.gemm)
 
     w_gate = synth.make_weight_device(wl, "gate")
     w_up = synth.make_weight_device(wl, "up")

@@ -1,9 +1,6 @@
 // C ABI entry points of libmoe: argument checks, workspace sizing, and the
 // chaining of the kernels of the other files on the caller's stream.
 // Declarations and the contract of every call are in include/moe.h.
-#include <stdio.h>
-#include <stdlib.h>
-
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -30,6 +27,9 @@ moe_status check_shape(const moe_shape* s) {
     if (s->E > kMaxE || s->k > kMaxK) return MOE_ERR_UNSUPPORTED;
     if (s->H % 8 != 0 || s->I % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if ((long long)s->N * s->k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    if (s->gemm != MOE_GEMM_AUTO && s->gemm != MOE_GEMM_SINGLE_CTA &&
+        s->gemm != MOE_GEMM_CTA_PAIR)
+        return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 
@@ -52,12 +52,11 @@ moe_status check_ws(const moe_shape* s, void* ws, size_t ws_bytes) {
 inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // CTA-pair (256-row) GEMM tiles pay off when experts have many rows; with few
-// rows per expert the single-CTA 128-row tiles waste less.  MOE_GEMM_PAIR=0/1
-// forces one or the other (tests run both kernels on small shapes).
-bool use_pair(long long R, int E) {
-    const char* v = getenv("MOE_GEMM_PAIR");
-    if (v && v[0] == '0') return false;
-    if (v && v[0] == '1') return true;
+// rows per expert the single-CTA 128-row tiles waste less.  The shape's gemm
+// field can name either kernel instead of the automatic choice.
+bool use_pair(long long R, int E, int32_t gemm) {
+    if (gemm == MOE_GEMM_SINGLE_CTA) return false;
+    if (gemm == MOE_GEMM_CTA_PAIR) return true;
     return R >= 512LL * E;
 }
 
@@ -173,7 +172,7 @@ moe_status moe_ffn_gate_up(const uint16_t* rows, const moe_layout* layout, const
     if (!rows || !w_gate || !w_up || !h) return MOE_ERR_INVALID_ARG;
     if (!aligned16(rows, w_gate, w_up, h)) return MOE_ERR_INVALID_ARG;
     const GemmGroup g = routed_group(*layout, *shape, ws);
-    if (use_pair(g.R, g.E))
+    if (use_pair(g.R, g.E, shape->gemm))
         return launch_gate_up_pair(rows, g, shape->H, shape->I, w_gate, w_up, h, as_stream(stream));
     return launch_gate_up(rows, g, shape->H, shape->I, w_gate, w_up, h, as_stream(stream));
 }
@@ -203,7 +202,7 @@ moe_status moe_ffn_down(const uint16_t* h, const moe_layout* layout, const moe_s
     if (!h || !w_down || !y) return MOE_ERR_INVALID_ARG;
     if (!aligned16(h, w_down, y)) return MOE_ERR_INVALID_ARG;
     const GemmGroup g = routed_group(*layout, *shape, ws);
-    if (use_pair(g.R, g.E))
+    if (use_pair(g.R, g.E, shape->gemm))
         return launch_down_pair(h, g, shape->H, shape->I, w_down, y, as_stream(stream));
     return launch_down(h, g, shape->H, shape->I, w_down, y, as_stream(stream));
 }
@@ -277,7 +276,7 @@ moe_status moe_shared_expert_ffn(const uint16_t* x, const moe_shape* shape, int3
     const GemmGroup g = dense_group(*shape, ws);
     MOE_TRY(cuda_status(launch_dense_group(shape->N, const_cast<int32_t*>(g.counts),
                                            const_cast<int32_t*>(g.offsets), st)));
-    if (use_pair(g.R, g.E)) {
+    if (use_pair(g.R, g.E, shape->gemm)) {
         MOE_TRY(launch_gate_up_pair(x, g, shape->H, I_shared, w_gate_s, w_up_s, h_s, st));
         return launch_down_pair(h_s, g, shape->H, I_shared, w_down_s, y_s, st);
     }
@@ -333,7 +332,7 @@ int32_t moe_layer_skips_dispatch(const moe_shape* shape) {
     // plain rows are gathered when the single-CTA GEMM runs (the weight-streaming
     // regime, where fusing the copy saves its HBM traffic); the CTA-pair kernel
     // has no gather mode
-    return use_pair((long long)shape->N * shape->k, shape->E) ? 0 : 1;
+    return use_pair((long long)shape->N * shape->k, shape->E, shape->gemm) ? 0 : 1;
 }
 
 moe_status moe_coselection(const int32_t* topk_ids, const moe_shape* shape, int32_t* coselect,

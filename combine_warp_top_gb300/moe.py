@@ -8,6 +8,7 @@ is no fallback of any kind.
 from __future__ import annotations
 
 import ctypes
+import dataclasses
 import os
 from dataclasses import dataclass
 
@@ -16,7 +17,9 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
-SHAPE_FIELDS = ("N", "H", "E", "k", "W", "I", "dedup")
+SHAPE_FIELDS = ("N", "H", "E", "k", "W", "I", "dedup", "gemm")
+# moe_gemm_kernel values of include/moe.h
+GEMM_KERNELS = {"auto": 0, "single": 1, "pair": 2}
 LAYOUT_FIELDS = ("expert_counts", "expert_offsets", "rank_offsets", "row_token", "pair_row",
                  "dedup_counts", "dedup_offsets", "dedup_row_token", "pair_dedup_row",
                  "expand_src", "n_dedup_rows")
@@ -170,9 +173,15 @@ class Shape:
     W: int
     I: int
     dedup: bool = False
+    # which grouped-GEMM kernel runs: "auto", "single" (128-row tiles, one CTA)
+    # or "pair" (256-row tiles on a 2-CTA cluster); see moe_gemm_kernel
+    gemm: str = "auto"
 
     def c(self) -> MoeShape:
-        return MoeShape(self.N, self.H, self.E, self.k, self.W, self.I, int(bool(self.dedup)))
+        if self.gemm not in GEMM_KERNELS:
+            raise ValueError(f"gemm must be one of {sorted(GEMM_KERNELS)}")
+        return MoeShape(self.N, self.H, self.E, self.k, self.W, self.I, int(bool(self.dedup)),
+                        GEMM_KERNELS[self.gemm])
 
     @property
     def R(self) -> int:
@@ -451,8 +460,7 @@ class MoELayer:
         rows_d = shape.R_d_max if shape.dedup else shape.R
         # plain rows gathered inside the gate/up GEMM need no dispatch buffer
         self.fused_dispatch = moe_layer_skips_dispatch(shape)
-        self._xd_rows = max(rows_d, 1)
-        self.xd = torch.empty(1 if self.fused_dispatch else self._xd_rows, H, **bf)
+        self.xd = torch.empty(1 if self.fused_dispatch else max(rows_d, 1), H, **bf)
         self.xe = None  # the dedup expansion happens inside the gate/up GEMM
         self.h = torch.empty(max(shape.R, 1), I, **bf)
         self.y = torch.empty(max(shape.R, 1), H, **bf)
@@ -464,18 +472,8 @@ class MoELayer:
                     if fuse_combine else None)
         self.ws = workspace(shape, device)
 
-    def refresh_form(self):
-        """Re-read which form the library runs for this shape (the GEMM
-        choice can be forced through MOE_GEMM_PAIR at any time) and give the
-        dispatch buffer its full size when the dispatch is no longer fused."""
-        self.fused_dispatch = moe_layer_skips_dispatch(self.shape)
-        if not self.fused_dispatch and self.xd.shape[0] < self._xd_rows:
-            self.xd = torch.empty(self._xd_rows, self.shape.H, dtype=torch.bfloat16,
-                                  device=self.xd.device)
-
     def forward(self, logits, x, residual=None, out=None, stream=None):
         out = self.out if out is None else out
-        self.refresh_form()
         if self.shared is not None or self.fuse_combine:
             return self.forward_stages(logits, x, residual, out, stream)
         moe_layer_forward(logits, x, self.placement, self.w_gate, self.w_up, self.w_down,
@@ -517,7 +515,6 @@ class MoELayer:
         out = self.out if out is None else out
         st = torch.cuda.current_stream() if stream is None else stream
         s = self.shape
-        self.refresh_form()
 
         def rec(name, i):
             if events is not None and name in events:
@@ -709,7 +706,7 @@ class MicrobatchPipeline:
         self.placement = placement
         self.w = (w_gate, w_up, w_down)
         self.shared = shared
-        sub = Shape(self.mb, shape.H, shape.E, shape.k, shape.W, shape.I, shape.dedup)
+        sub = dataclasses.replace(shape, N=self.mb)
         self.sets = [MoELayer(sub, w_gate, w_up, w_down, placement, device, shared)
                      for _ in range(depth)]
         self.vec = torch.cuda.Stream(device=device)
@@ -733,7 +730,7 @@ class MicrobatchPipeline:
         b_done = [torch.cuda.Event() for _ in chunks]
 
         def sub_shape(t0, t1):
-            return Shape(t1 - t0, s.H, s.E, s.k, s.W, s.I, s.dedup)
+            return dataclasses.replace(s, N=t1 - t0)
 
         def combine(m):
             t0, t1 = chunks[m]
@@ -753,7 +750,8 @@ class MicrobatchPipeline:
             # vector-unit stages of microbatch m
             moe_route(logits[t0:t1], sm, L.topk_ids, L.topk_w, vec)
             moe_dispatch_layout(L.topk_ids, self.placement, sm, L.layout, L.ws, vec)
-            L.refresh_form()
+            # a chunk never has more rows than its buffer set's shape, so a set
+            # sized for the unfused form also fits a fused chunk
             fused = moe_layer_skips_dispatch(sm)
             if not fused:
                 moe_dispatch(x[t0:t1], L.layout, sm, L.xd, vec)
@@ -793,7 +791,7 @@ class MicrobatchPipeline:
         total = 0
         for t0, t1 in self.chunks():
             s = self.shape
-            sub = Shape(t1 - t0, s.H, s.E, s.k, s.W, s.I, s.dedup)
+            sub = dataclasses.replace(s, N=t1 - t0)
             dispatch = 0 if moe_layer_skips_dispatch(sub) else 1
             total += 1 + 3 + dispatch + 2 + 2 + 1 + (
                 5 if self.shared is not None else 0)

@@ -49,12 +49,34 @@ typedef enum {
     MOE_ERR_DEVICE_ASSERT = 6  /* a device-side consistency check failed */
 } moe_status;
 
+/* Which tensor-core kernel runs the grouped GEMMs (moe_shape.gemm).  Both give
+ * the same results to fp32 accumulation order; they differ in speed only.
+ *  MOE_GEMM_AUTO        the CTA-pair kernel when the problem has at least 512
+ *                       rows per expert on average (N*k >= 512*E), else the
+ *                       single-CTA kernel
+ *  MOE_GEMM_SINGLE_CTA  128-row tiles, one CTA each (cta_group::1); the only
+ *                       kernel with a gather mode
+ *  MOE_GEMM_CTA_PAIR    256-row tiles shared by a 2-CTA cluster (cta_group::2)
+ * Calls that gather rows inside the GEMM (moe_ffn_gate_up_gather, the dedup
+ * form of moe_expert_ffn) and moe_ffn_down_combine always run the single-CTA
+ * kernel for their gathered / fused launch. */
+typedef enum {
+    MOE_GEMM_AUTO = 0,
+    MOE_GEMM_SINGLE_CTA = 1,
+    MOE_GEMM_CTA_PAIR = 2
+} moe_gemm_kernel;
+
 /* N tokens of width H; E experts, top-k; W ranks; SwiGLU intermediate width I;
  * dedup != 0 selects the deduplicating dispatcher ("Expert Coupling" Sec. V-A):
- * one row per distinct (token, rank) instead of one per (token, expert). */
+ * one row per distinct (token, rank) instead of one per (token, expert).
+ * gemm: a moe_gemm_kernel value (0 = automatic choice); any other value is
+ * refused with MOE_ERR_INVALID_ARG.  Every behaviour of the library is set by
+ * these fields and the call's arguments: nothing is read from the
+ * environment. */
 typedef struct {
     int32_t N, H, E, k, W, I;
     int32_t dedup;
+    int32_t gemm;
 } moe_shape;
 
 /* Dispatch layout: caller-owned device arrays of int32, written by
@@ -273,7 +295,8 @@ moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32
 /* 1 when moe_layer_forward, for this shape, gathers the plain rows inside the
  * gate/up GEMM instead of running moe_dispatch first; 0 otherwise (dedup
  * form, or a shape whose GEMMs run on the CTA-pair kernel, which has no
- * gather mode).  Lets a caller that runs the stages itself do the same. */
+ * gather mode).  A function of the shape alone (its gemm field included).
+ * Lets a caller that runs the stages itself do the same. */
 int32_t moe_layer_skips_dispatch(const moe_shape* shape);
 
 /* Co-selection counts of "Expert Coupling" Sec. V-A / Appendix A-D Algorithm 1:

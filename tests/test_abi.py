@@ -125,3 +125,34 @@ def test_workspace_grows_with_tokens(lib):
     small = moe.moe_workspace_bytes(moe.Shape(256, 64, 8, 2, 2, 64))
     large = moe.moe_workspace_bytes(moe.Shape(256 * 64, 64, 8, 2, 2, 64))
     assert large > small
+
+
+def test_gemm_kernel_choice_is_an_argument(lib):
+    """Which GEMM kernel runs is set by the shape's gemm field alone: values
+    outside moe_gemm_kernel are refused, and whether the layer fuses its plain
+    dispatch into the gate/up GEMM follows from the field (no environment or
+    other global state is consulted)."""
+    bad = moe.MoeShape(4096, 7168, 8, 2, 8, 2048, 0, 3)
+    assert lib.moe_workspace_bytes(ctypes.byref(bad)) == 0
+    assert lib.moe_route(None, ctypes.byref(bad), None, None, None) == 1
+    # 8192 rows over 8 experts: the automatic choice is the CTA-pair kernel,
+    # which has no gather mode, so the dispatch is not fused
+    auto = moe.Shape(4096, 7168, 8, 2, 8, 2048)
+    assert not moe.moe_layer_skips_dispatch(auto)
+    assert moe.moe_layer_skips_dispatch(moe.Shape(4096, 7168, 8, 2, 8, 2048, gemm="single"))
+    assert not moe.moe_layer_skips_dispatch(moe.Shape(4096, 7168, 8, 2, 8, 2048, gemm="pair"))
+    # few rows per expert: the single-CTA kernel, dispatch fused, unless the pair is named
+    few = moe.Shape(4096, 7168, 256, 8, 8, 2048)
+    assert moe.moe_layer_skips_dispatch(few)
+    assert not moe.moe_layer_skips_dispatch(moe.Shape(4096, 7168, 256, 8, 8, 2048, gemm="pair"))
+    # the dedup form never skips the dispatch (its rows are the dedup rows)
+    assert not moe.moe_layer_skips_dispatch(moe.Shape(4096, 7168, 256, 8, 8, 2048, dedup=True))
+    with pytest.raises(ValueError):
+        moe.Shape(64, 128, 8, 2, 2, 64, gemm="fast").c()
+
+
+def test_library_sources_read_no_environment():
+    csrc = os.path.join(ROOT, "combine_warp_top_gb300", "csrc")
+    for fn in os.listdir(csrc):
+        text = open(os.path.join(csrc, fn)).read()
+        assert "getenv" not in text, fn

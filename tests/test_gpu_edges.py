@@ -33,9 +33,9 @@ def test_layout_largest_expert_counts(N, E, k, W):
     assert int(got["n_dedup_rows"][0]) == ref["n_dedup_rows"]
 
 
-def run_layer(wl, dedup=False):
+def run_layer(wl, dedup=False, gemm="auto"):
     w = [synth.make_weight(wl, m) for m in ("gate", "up", "down")]
-    shape = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=dedup)
+    shape = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=dedup, gemm=gemm)
     layer = moe.MoELayer(shape, *[dev_bf16(a) for a in w])
     L, x, res = synth.make_logits(wl), synth.make_x(wl), synth.make_residual(wl)
     out = layer.forward(torch.from_numpy(L).cuda(), dev_bf16(x), dev_bf16(res))
@@ -65,11 +65,11 @@ def test_layer_edge_shapes(wl, dedup):
 
 @pytest.mark.parametrize("dedup", [False, True])
 @pytest.mark.parametrize("wl", EDGE, ids=lambda w: w.name)
-def test_layer_edge_shapes_on_cta_pairs(wl, dedup, monkeypatch):
-    """The same shapes on the CTA-pair GEMMs (forced): fewer tiles than pairs,
-    so most pairs find the tile queue exhausted at once; tiles of one row."""
-    monkeypatch.setenv("MOE_GEMM_PAIR", "1")
-    run_layer(wl, dedup)
+def test_layer_edge_shapes_on_cta_pairs(wl, dedup):
+    """The same shapes on the CTA-pair GEMMs (named in the shape): fewer tiles
+    than pairs, so most pairs find the tile queue exhausted at once; tiles of
+    one row."""
+    run_layer(wl, dedup, gemm="pair")
 
 
 def test_misaligned_view_is_refused_and_the_context_survives():

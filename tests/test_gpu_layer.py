@@ -14,10 +14,10 @@ from gpu_util import assert_close, dev_bf16, dev_i32, host_f64, host_u16
 pytestmark = pytest.mark.gpu
 
 
-def build_layer(wl, dedup, placement=None, N=None):
+def build_layer(wl, dedup, placement=None, N=None, gemm="auto"):
     N = wl.N if N is None else N
     wg, wu, wd = (synth.make_weight(wl, w) for w in ("gate", "up", "down"))
-    shape = moe.Shape(N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=dedup)
+    shape = moe.Shape(N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=dedup, gemm=gemm)
     layer = moe.MoELayer(shape, dev_bf16(wg), dev_bf16(wu), dev_bf16(wd),
                          None if placement is None else dev_i32(placement))
     return layer, (wg, wu, wd)
@@ -201,25 +201,25 @@ def test_cuda_graph_replay_matches_eager(dedup):
     layer.check_device_errors()
 
 
-def test_fused_dispatch_and_staged_forms_agree(monkeypatch):
-    """On a shape whose plain dispatch is fused into the gate/up GEMM, the
-    layer gives bit for bit the output of the staged form (dispatch copy, then
-    the CTA-pair GEMMs forced), and switching form after the layer was built
-    gives the dispatch buffer its full size."""
+def test_fused_dispatch_and_staged_forms_agree():
+    """On a shape whose plain dispatch is fused into the gate/up GEMM (the
+    single-CTA kernel, named in the shape), the layer gives bit for bit the
+    output of the staged form (dispatch copy, then the CTA-pair GEMMs, named
+    in the shape); which form runs follows from the shape alone."""
     wl = SMALL["wide"]
-    monkeypatch.setenv("MOE_GEMM_PAIR", "0")
-    layer, (wg, wu, wd) = build_layer(wl, False)
-    assert layer.fused_dispatch and moe.moe_layer_skips_dispatch(layer.shape)
-    assert layer.xd.shape[0] == 1
+    fused_layer, _ = build_layer(wl, False, gemm="single")
+    assert fused_layer.fused_dispatch and moe.moe_layer_skips_dispatch(fused_layer.shape)
+    assert fused_layer.xd.shape[0] == 1
+    layer, _ = build_layer(wl, False, gemm="pair")
+    assert not layer.fused_dispatch and not moe.moe_layer_skips_dispatch(layer.shape)
+    assert layer.xd.shape[0] == layer.shape.R
     L = torch.from_numpy(synth.make_logits(wl)).cuda()
     x, res = dev_bf16(synth.make_x(wl)), dev_bf16(synth.make_residual(wl))
-    fused = layer.forward(L, x, res).clone()
-    monkeypatch.setenv("MOE_GEMM_PAIR", "1")
-    assert not moe.moe_layer_skips_dispatch(layer.shape)
+    fused = fused_layer.forward(L, x, res).clone()
     staged = layer.forward(L, x, res).clone()
     torch.cuda.synchronize()
+    fused_layer.check_device_errors()
     layer.check_device_errors()
-    assert layer.xd.shape[0] == layer.shape.R
     # same K order in both GEMM kernels and the same combine: identical bits
     assert torch.equal(fused.view(torch.int16), staged.view(torch.int16))
     # and the dispatched rows the staged form wrote are the oracle's
