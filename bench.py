@@ -18,6 +18,7 @@ time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import datetime as dt
 import json
 import os
@@ -57,8 +58,11 @@ def parse_args(argv=None):
     p.add_argument("--eager", action="store_true",
                    help="launch every step from Python instead of replaying a captured CUDA graph")
     p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--others", default="auto",
+                   help="workloads measured after the headline one: a comma list, 'none', or "
+                        "'auto' (the five other benchmark workloads when the default "
+                        "DeepSeek-V3 layer runs on one GPU without options)")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
     return p.parse_args(argv)
 
@@ -218,63 +222,132 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------- oracle timing
 
-def oracle_worker(spec):
-    """Times the CPU oracle (route + the layer output straight from the MoE
-    definition) on routed (token, expert) pairs of the workload.  Runs in its
-    own single-threaded process.  spec: argv of the workload, number of steps,
-    seconds of oracle time per step (at least one pair per step).
+COMBINE_SAMPLE_TOKENS = 1024
 
-    Sample: the routed pairs, in token order, whose expert is one of the first
-    four experts met in the routing; their weights are generated once before
-    any timing (every pair costs the oracle the same, whichever the expert)."""
+
+def oracle_worker(spec):
+    """Times the CPU oracle's steps of one layer step of the workload, in its
+    own process (the BLAS thread count is set by the caller's environment).
+
+    Sample, per step:
+      * route, dispatch layout and dispatch (dedup: the dedup rows and their
+        expansion) over all N tokens;
+      * the expert FFN: oracle.swiglu_mlp, the oracle's per-expert step, on the
+        rows this routing gives each of ``experts_per_step`` seeded experts
+        (their weights generated and widened before the timer starts), scaled
+        to all R = N*k rows by the share of rows the sampled experts hold;
+      * the combine (plain: oracle.combine; dedup: oracle.combine_dedup) over
+        the first min(N, 1024) tokens, scaled to N.
+    Successive steps take successive experts of one seeded permutation."""
     import numpy as np
 
     import oracle
     from combine_warp_top_gb300 import synth
     args = parse_args(spec["argv"])
     wl = workload(args)
-    n_tok = min(wl.N, 4096)
-    L = synth.make_logits(wl, N=n_tok)
-    x = synth.make_x(wl, N=n_tok)
-    res = synth.make_residual(wl, N=n_tok)
-    ids_all, _ = oracle.route(L, wl.k)
-    chosen = []
-    for e in ids_all.reshape(-1):
-        if int(e) not in chosen:
-            chosen.append(int(e))
-        if len(chosen) == 4:
-            break
-    weights = {e: tuple(synth.make_weight(wl, m, experts=[e])[0] for m in ("gate", "up", "down"))
-               for e in chosen}
-    pairs_list = [(t, j) for t in range(n_tok) for j in range(wl.k)
-                  if int(ids_all[t, j]) in weights]
-    steps = []
-    p = 0
+    rng = np.random.default_rng(spec.get("seed", 0))
+    L = synth.make_logits(wl)
+    x = synth.make_x(wl)
+    res = synth.make_residual(wl)
+    placement = synth.make_placement(wl)
+    N, k, H = wl.N, wl.k, wl.H
+    R = N * k
+    # untimed: which experts hold rows under this routing (the sample's pool)
+    ids0, _ = oracle.route(L, k)
+    counts0 = np.bincount(ids0.reshape(-1), minlength=wl.E)
+    pool = rng.permutation(np.nonzero(counts0)[0])
+    n_sub = min(N, COMBINE_SAMPLE_TOKENS)
+    y_rows = rng.standard_normal((R, H)) if n_sub == N else None
+    steps, nxt = [], 0
     for _ in range(spec["steps"]):
-        t_oracle, pairs = 0.0, 0
-        while pairs == 0 or t_oracle < spec["seconds"]:
-            t, j = pairs_list[p % len(pairs_list)]
-            p += 1
-            c0 = time.perf_counter()
-            ids, w = oracle.route(L[t:t + 1], wl.k)
-            e = int(ids[0, j])
-            wg, wu, wd = weights[e]
-            oracle.token_outputs(x[t:t + 1], ids[:, j:j + 1], w[:, j:j + 1],
-                                 lambda _e: (wg, wu, wd), res[t:t + 1] if j == 0 else None)
-            t_oracle += time.perf_counter() - c0
-            pairs += 1
-        steps.append({"pairs": pairs, "tokens": pairs / wl.k, "seconds": t_oracle})
-    return {"steps": steps, "k": wl.k, "experts_sampled": chosen}
+        experts = [int(pool[(nxt + i) % len(pool)]) for i in range(spec["experts_per_step"])]
+        experts = sorted(set(experts))
+        nxt += spec["experts_per_step"]
+        weights = {e: tuple(oracle.widen_bf16(synth.make_weight(wl, m, experts=[e])[0])
+                            for m in ("gate", "up", "down")) for e in experts}
+        t = {}
+        c = time.perf_counter()
+        ids, w = oracle.route(L, k)
+        t["route"] = time.perf_counter() - c
+        c = time.perf_counter()
+        lay = oracle.dispatch_layout(ids, placement, wl.E, wl.W)
+        t["layout"] = time.perf_counter() - c
+        c = time.perf_counter()
+        if wl.dedup:
+            xd = oracle.expand(oracle.dispatch_dedup(x, lay["dedup_row_token"]), lay["expand_src"])
+        else:
+            xd = oracle.dispatch(x, lay["row_token"])
+        t["dispatch"] = time.perf_counter() - c
+        rows, ffn = 0, 0.0
+        for e in experts:
+            a, n = int(lay["expert_offsets"][e]), int(lay["expert_counts"][e])
+            c = time.perf_counter()
+            oracle.swiglu_mlp(oracle.widen_bf16(xd[a:a + n]), *weights[e])
+            ffn += time.perf_counter() - c
+            rows += n
+        t["ffn"] = ffn * R / max(rows, 1)
+        # combine over the first n_sub tokens: their k rows, compacted
+        pr = lay["pair_row"][:n_sub]
+        y_sub = y_rows[pr.reshape(-1)] if y_rows is not None else \
+            rng.standard_normal((n_sub * k, H))
+        pr_sub = np.arange(n_sub * k).reshape(n_sub, k)
+        c = time.perf_counter()
+        if wl.dedup:
+            d = lay["pair_dedup_row"][:n_sub]
+            uniq, dd = np.unique(d, return_inverse=True)
+            oracle.combine_dedup(y_sub, w[:n_sub], pr_sub, dd.reshape(n_sub, k), len(uniq),
+                                 res[:n_sub])
+        else:
+            oracle.combine(y_sub, w[:n_sub], pr_sub, res[:n_sub])
+        t["combine"] = (time.perf_counter() - c) * N / n_sub
+        total = sum(t.values())
+        steps.append({"seconds": total, "tokens": N, "stage_s": t, "experts": experts,
+                      "rows_sampled": rows})
+    return {"steps": steps, "threads": spec["threads"], "n_sub": n_sub}
 
 
-def run_oracle(argv, seconds, steps=1):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    spec = json.dumps({"argv": argv, "seconds": seconds, "steps": steps})
+def run_oracle(argv, threads, steps=1, experts_per_step=4, seed=0):
+    """The oracle worker in a subprocess whose BLAS and OpenMP pools have
+    `threads` threads."""
+    n = str(threads)
+    env = dict(os.environ, OMP_NUM_THREADS=n, OPENBLAS_NUM_THREADS=n, MKL_NUM_THREADS=n)
+    spec = json.dumps({"argv": argv, "steps": steps, "experts_per_step": experts_per_step,
+                       "seed": seed, "threads": threads})
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-worker", spec],
                        capture_output=True, text=True, env=env, cwd=ROOT)
     if r.returncode != 0:
         raise RuntimeError("oracle worker failed:\n" + r.stderr[-2000:])
     return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def oracle_sample_text(wl, experts_per_step, steps, n_sub):
+    return (f"each step: route, dispatch layout and dispatch of all {wl.N} tokens of the "
+            f"{wl.name} workload; the expert FFN (oracle.swiglu_mlp, weights widened before "
+            f"timing) on the rows of {experts_per_step} seeded experts, scaled to all "
+            f"{wl.N * wl.k} rows by the rows they hold; the combine over {n_sub} tokens, scaled "
+            f"to {wl.N}; float64 numpy; {steps} step(s)")
+
+
+def cpu_baseline(argv, wl):
+    """The oracle timed with every host core and with one (bounded samples)."""
+    ncpu = os.cpu_count() or 1
+    runs = {}
+    for threads, experts in ((ncpu, 8), (1, 2)):
+        r = run_oracle(argv, threads, steps=1, experts_per_step=experts)
+        st = r["steps"][0]
+        runs[threads] = (st, r["n_sub"], experts)
+    st, n_sub, experts = runs[ncpu]
+    st1, n_sub1, experts1 = runs[1]
+    return {
+        "value": round(st["tokens"] / st["seconds"], 3), "unit": "tokens/s", "cores": ncpu,
+        "kind": "oracle",
+        "sample": oracle_sample_text(wl, experts, 1, n_sub) +
+                  f"; {ncpu} threads in the BLAS calls (the other steps are single-threaded numpy)",
+        "stage_s": {k: round(v, 4) for k, v in st["stage_s"].items()},
+        "one_core": {"value": round(st1["tokens"] / st1["seconds"], 3), "unit": "tokens/s",
+                     "cores": 1, "sample": oracle_sample_text(wl, experts1, 1, n_sub1),
+                     "stage_s": {k: round(v, 4) for k, v in st1["stage_s"].items()}},
+    }
 
 
 def strip_args(argv):
@@ -283,7 +356,7 @@ def strip_args(argv):
         if skip:
             skip = False
             continue
-        if a in ("--impl", "--gpus", "--steps", "--warmup", "--e2e-steps", "--cpu-seconds"):
+        if a in ("--impl", "--gpus", "--steps", "--warmup", "--e2e-steps", "--others"):
             skip = True
             continue
         if a.startswith("--impl=") or a == "--no-cpu-baseline":
@@ -376,16 +449,19 @@ def placement_search(wl, shape, logits_d, repeats=20):
 
 # ---------------------------------------------------------------------------- our arm
 
-def run_ours(args):
+OTHER_WORKLOADS = ("tiny", "mixtral", "correlated_contiguous", "correlated_placed", "skewed")
+
+
+def measure(args, wl, world, rank, headline=True):
+    """Builds the layer of workload `wl`, times K steps (after W warm-up
+    steps) and returns its figures.  headline=False skips the end-to-end run,
+    the placement search and the microbatch / fused-combine / shared-expert
+    options (the other benchmark workloads are measured as plain layers)."""
     import numpy as np
     import torch
 
     from combine_warp_top_gb300 import moe, synth
 
-    world, rank, local = dist_info()
-    dist_init(world, local)
-    torch.cuda.set_device(local)
-    wl = workload(args)
     seed = rank  # every rank has its own tokens; weights are the same layer
     shape = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=wl.dedup, gemm=args.gemm)
 
@@ -396,19 +472,21 @@ def run_ours(args):
     placement_d = None if wl.placement == "contiguous" else torch.from_numpy(placement).cuda()
     L_h = torch.from_numpy(synth.make_logits(wl, seed)).pin_memory()
     search = None
-    if args.placement_search:
+    if headline and args.placement_search:
         search = placement_search(wl, shape, L_h.cuda())
         placement_d = search.pop("placement").cuda()
     shared = None
-    if args.shared_expert:
+    if headline and args.shared_expert:
         I_s = args.shared_expert
         shared = tuple(synth.normal_bf16_device(
             torch.empty(*shp, dtype=torch.bfloat16, device="cuda"), 0, stream_id, std=0.02)
             for stream_id, shp in ((103, (I_s, wl.H)), (104, (I_s, wl.H)), (105, (wl.H, I_s))))
-    if args.fuse_combine and (args.microbatch or args.shared_expert):
+    fuse_combine = headline and args.fuse_combine
+    microbatch = args.microbatch if headline else 0
+    if fuse_combine and (microbatch or shared is not None):
         raise SystemExit("--fuse-combine runs the plain layer: no --microbatch, no --shared-expert")
     layer = moe.MoELayer(shape, w_gate, w_up, w_down, placement_d, shared=shared,
-                         fuse_combine=args.fuse_combine)
+                         fuse_combine=fuse_combine)
 
     x_h = torch.from_numpy(synth.make_x(wl, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
     r_h = torch.from_numpy(synth.make_residual(wl, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -416,21 +494,13 @@ def run_ours(args):
     L_d, x_d, r_d = L_h.cuda(), x_h.cuda(), r_h.cuda()
     torch.cuda.synchronize()
 
-    # rows a dedup dispatcher would send for this routing (reported, not timed)
-    dshape = moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=True)
-    dlay, dws = moe.Layout(dshape), moe.workspace(dshape)
-    moe.moe_route(L_d, shape, layer.topk_ids, layer.topk_w)
-    moe.moe_dispatch_layout(layer.topk_ids, placement_d, dshape, dlay, dws)
-    torch.cuda.synchronize()
-    R_d = int(dlay["n_dedup_rows"].item())
-    counts = dlay["expert_counts"].cpu().numpy()
-    del dlay, dws
+    rows = dispatch_rows(wl, shape, L_d, placement_d)
 
     stream = torch.cuda.current_stream()
     pipe = None
-    if args.microbatch:
+    if microbatch:
         pipe = moe.MicrobatchPipeline(shape, w_gate, w_up, w_down, placement_d,
-                                      microbatch=args.microbatch, shared=shared)
+                                      microbatch=microbatch, shared=shared)
     runner = pipe if pipe is not None else layer
     n_mb = len(pipe.chunks()) if pipe is not None else 0
 
@@ -504,28 +574,30 @@ def run_ours(args):
         stage_ms = {"gate_up": statistics.mean(sum(a.elapsed_time(b) for a, b in g) for g in gev)}
         stages = ["gate_up"]
 
-    # end to end through the public host-buffer API: every step copies its
-    # inputs from pinned host memory and its output back, overlapped with the
-    # neighbouring steps' compute (moe.HostPipeline)
-    e2e_steps = args.e2e_steps or max(3, min(args.steps, 50))
-    host = moe.HostPipeline(runner, with_residual=True)
-    batches = [(L_h, x_h, r_h, out_h)] * e2e_steps
-    host.run(batches[:2])
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    host.run(batches)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    runner.check_device_errors()
-
-    if rank != 0:
-        return None
+    e2e = None
+    if headline:
+        # end to end through the public host-buffer API: every step copies its
+        # inputs from pinned host memory and its output back, overlapped with
+        # the neighbouring steps' compute (moe.HostPipeline)
+        e2e_steps = args.e2e_steps or max(3, min(args.steps, 50))
+        host = moe.HostPipeline(runner, with_residual=True)
+        batches = [(L_h, x_h, r_h, out_h)] * e2e_steps
+        host.run(batches[:2])
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        host.run(batches)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+        runner.check_device_errors()
+        e2e = {"value": round(wl.N * e2e_steps * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": wl.N * wl.E * 4 + 2 * wl.N * wl.H * 2,
+               "d2h_bytes_per_step": wl.N * wl.H * 2, "steps": e2e_steps}
 
     pk, pk_src = peaks()
-    alg = algorithmic(wl, R_d, layer.fused_dispatch)
+    alg = algorithmic(wl, rows["dedup"], layer.fused_dispatch)
     if shared is not None:
         I_s = args.shared_expert
         alg["shared"] = dict(bytes=3 * I_s * wl.H * 2 + 2 * wl.N * wl.H * 2 + 2 * wl.N * I_s * 2,
@@ -541,20 +613,67 @@ def run_ours(args):
             d["TFLOP/s"] = round(alg[s]["flops"] / ms / 1e9, 1)
             d["tensor_frac"] = round(d["TFLOP/s"] / pk["bf16_tflops_sustained"], 3)
             d["bound"] = "tensor" if alg[s]["flops"] / alg[s]["bytes"] > ridge else "hbm"
+        else:
+            d["bound"] = "hbm"
         stage_report[s] = d
 
+    roof = roofline(wl, alg, stage_ms, pk, pk_src, ridge, layer, pipe, n_mb)
+    res = {
+        "value": round(wl.N * args.steps * world / (elapsed_ms / 1e3), 1),
+        "ms_per_step": round(elapsed_ms / args.steps, 4),
+        "roofline": roof, "stages": stage_report, "clocks": clocks, "dispatch_rows": rows,
+        "gpu_launches": runner.kernel_launches_per_step() * args.steps,
+        "graph": graph is not None, "e2e": e2e, "search": search,
+    }
+    del graph, layer, pipe, runner, w_gate, w_up, w_down
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def dispatch_rows(wl, shape, L_d, placement_d):
+    """Rows the plain and the deduplicating dispatcher send for this routing,
+    with the per-layer counters of "Expert Coupling" Table I, from the
+    library's own routing and layout tables (not timed)."""
+    import numpy as np
+    import torch
+
+    from combine_warp_top_gb300 import moe
+    dshape = dataclasses.replace(shape, dedup=True)
+    ids = torch.empty(wl.N * wl.k, dtype=torch.int32, device="cuda")
+    w = torch.empty(wl.N * wl.k, dtype=torch.float32, device="cuda")
+    dlay, dws = moe.Layout(dshape), moe.workspace(dshape)
+    moe.moe_route(L_d, shape, ids, w)
+    moe.moe_dispatch_layout(ids, placement_d, dshape, dlay, dws)
+    torch.cuda.synchronize()
+    R, R_d = wl.N * wl.k, int(dlay["n_dedup_rows"].item())
+    counts = dlay["expert_counts"].cpu().numpy()
+    # distinct ranks of each token = its dedup rows
+    per_token = np.bincount(dlay["dedup_row_token"][:R_d].cpu().numpy(), minlength=wl.N)
+    return {"plain": R, "dedup": R_d, "dedup_reduction": round(1 - R_d / R, 4),
+            "ranks_per_token": round(R_d / wl.N, 4),
+            "same_rank_share": round(float(np.mean(per_token == 1)), 4),
+            "max_over_mean_expert_load": round(float(counts.max() / counts.mean()), 3)}
+
+
+def roofline(wl, alg, stage_ms, pk, pk_src, ridge, layer, pipe, n_mb):
+    """The roofline object of the dominant kernel, the gate/up GEMM."""
     dom = "gate_up"
     a = alg[dom]
-    intensity = a["flops"] / a["bytes"]
-    if intensity > ridge:
+    if a["flops"] / a["bytes"] > ridge:
         achieved = a["flops"] / stage_ms[dom] / 1e9
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops_sustained"],
-                "unit": "TFLOP/s"}
+        roof = {"bound": "tensor", "achieved": round(achieved, 1),
+                "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s"}
     else:
         achieved = a["bytes"] / stage_ms[dom] / 1e6
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s"}
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 3)
     roof["traffic"] = recorded_traffic(wl)
+    if roof["frac"] > 1.0:
+        roof["note"] = ("above 1: the peak is a copy probe (half its bytes writes); this kernel "
+                        "mostly reads, and its DRAM traffic is at least its algorithmic bytes, "
+                        "so no L2 hit inflates the figure")
     if wl.dedup:
         roof["kernel"] = ("grouped_gemm_kernel<SwiGLU, gathered rows> (moe_ffn_gate_up_gather: "
                           "the dedup expansion done by the GEMM's gather warps)")
@@ -565,60 +684,90 @@ def run_ours(args):
         roof["kernel"] = "grouped_gemm_kernel<SwiGLU> or its CTA-pair form (moe_ffn_gate_up)"
     if pipe is not None:
         roof["kernel"] += f", summed over the {n_mb} microbatches of a step"
-    roof["peak_source"] = f"{pk_src} ({'bf16_tflops_sustained' if roof['unit'] == 'TFLOP/s' else 'hbm_gbs'})"
+    peak_key = "bf16_tflops_sustained" if roof["unit"] == "TFLOP/s" else "hbm_gbs"
+    roof["peak_source"] = f"{pk_src} ({peak_key})"
     roof["algorithmic_per_launch"] = {"bytes": a["bytes"], "flops": a["flops"]}
+    return roof
 
-    tokens = wl.N * args.steps * world
-    value = tokens / (elapsed_ms / 1e3)
-    e2e_value = wl.N * e2e_steps * world / (e2e_ms / 1e3)
+
+def workload_config(wl):
+    return {"workload": wl.name, "N": wl.N, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
+            "W": wl.W, "dedup": wl.dedup, "placement": wl.placement}
+
+
+def l2_note(wl):
+    wbytes = 3 * wl.E * wl.H * wl.I * 2
+    if wbytes > 129e6:
+        return f"no flush: {wbytes / 1e9:.2f} GB of expert weights read per step, larger than the 129 MB L2"
+    return (f"no flush: the {wbytes / 1e6:.1f} MB of weights fit in L2 and stay there from step to "
+            f"step (a latency-bound case)")
+
+
+def run_ours(args):
+    world, rank, local = dist_info()
+    dist_init(world, local)
+    import torch
+    torch.cuda.set_device(local)
+    wl = workload(args)
+    r = measure(args, wl, world, rank, headline=True)
+    others = []
+    if args.others == "auto":
+        default = (args.workload == "deepseek_v3" and args.tokens is None and args.experts is None
+                   and args.dedup == "auto" and not (args.microbatch or args.fuse_combine or
+                                                     args.shared_expert or args.placement_search))
+        others = list(OTHER_WORKLOADS) if default and world == 1 else []
+    elif args.others != "none":
+        others = [w for w in args.others.split(",") if w]
+    extra = {}
+    for name in others:
+        from combine_warp_top_gb300 import synth
+        o = measure(args, synth.WORKLOADS[name], world, rank, headline=False)
+        extra[name] = {"value": o["value"], "unit": "tokens/s", "ms_per_step": o["ms_per_step"],
+                       "config": workload_config(synth.WORKLOADS[name]),
+                       "roofline": {k: o["roofline"][k] for k in ("bound", "achieved", "peak",
+                                                                   "unit", "frac", "traffic")},
+                       "stages": o["stages"], "dispatch_rows": o["dispatch_rows"],
+                       "gpu_launches": o["gpu_launches"], "clocks": o["clocks"]}
+    if rank != 0:
+        return None
+    cfg = workload_config(wl)
+    cfg.update({
+        "shared_expert_I": args.shared_expert or None,
+        "fused_combine": bool(args.fuse_combine),
+        "microbatch": args.microbatch or None,
+        "gemm": args.gemm,
+        "launch": ("one CUDA graph of the K timed steps, timing nodes around gate/up only; "
+                   "the other stages' times from a second, instrumented replay of the K steps")
+                  if r["graph"] else "eager, one C call per stage",
+        "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU",
+        "l2": l2_note(wl)})
     line = {
         "metric": METRIC,
-        "value": round(value, 1),
+        "value": r["value"],
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(elapsed_ms / args.steps, 4),
+        "ms_per_step": r["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded SplitMix64/Box-Muller; random-init expert weights)",
-        "config": {"workload": wl.name, "N": wl.N, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
-                   "W": wl.W, "dedup": wl.dedup, "placement": wl.placement,
-                   "shared_expert_I": args.shared_expert or None,
-                   "fused_combine": bool(args.fuse_combine),
-                   "microbatch": args.microbatch or None,
-                   "launch": ("one CUDA graph of the K timed steps, timing nodes around "
-                              "gate/up only; the other stages' times from a second, "
-                              "instrumented replay of the K steps") if graph is not None
-                             else "eager, one C call per stage",
-                   "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU",
-                   "l2": f"no flush: {3 * wl.E * wl.H * wl.I * 2 / 1e9:.2f} GB of expert weights "
-                         "read per step, larger than the 129 MB L2"},
-        "roofline": roof,
-        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": wl.N * wl.E * 4 + 2 * wl.N * wl.H * 2,
-                "d2h_bytes_per_step": wl.N * wl.H * 2},
-        "gpu_launches": runner.kernel_launches_per_step() * args.steps,
-        "clocks": clocks,
-        "stages": stage_report,
-        "dispatch_rows": {"plain": wl.N * wl.k, "dedup": R_d,
-                          "dedup_reduction": round(1 - R_d / (wl.N * wl.k), 4),
-                          "max_over_mean_expert_load": round(float(counts.max() / counts.mean()), 3)},
+        "config": cfg,
+        "roofline": r["roofline"],
+        "e2e": r["e2e"],
+        "gpu_launches": r["gpu_launches"],
+        "clocks": r["clocks"],
+        "stages": r["stages"],
+        "dispatch_rows": r["dispatch_rows"],
     }
-    if search is not None:
-        line["placement_search"] = search
+    if r["search"] is not None:
+        line["placement_search"] = r["search"]
+    if extra:
+        line["workloads"] = extra
     if not args.no_cpu_baseline and world == 1:
-        cb = run_oracle(strip_args(sys.argv[1:]), args.cpu_seconds)["steps"][0]
-        line["cpu_baseline"] = {
-            "value": round(cb["tokens"] / cb["seconds"], 4), "unit": "tokens/s", "cores": 1,
-            "kind": "oracle",
-            "sample": f"{cb['pairs']} routed (token, expert) pairs = {cb['tokens']:.3g} tokens of "
-                      f"the {wl.name} workload, pairs in token order whose expert is one of the "
-                      f"first four experts routed to (route + one SwiGLU expert + weighted sum "
-                      f"+ residual, float64 numpy, one thread), {cb['seconds']:.1f} s of oracle "
-                      f"time"}
+        line["cpu_baseline"] = cpu_baseline(strip_args(sys.argv[1:]), wl)
     return line
 
 
@@ -643,30 +792,30 @@ def instrumented_stage_ms(layer, L_d, x_d, r_d, stages, steps):
 
 
 def run_reference(args):
+    """The oracle as it stands, timed on every host core: K steps after W
+    warm-up steps, each a bounded sample of the workload (oracle_worker)."""
     world, rank, _ = dist_info()
     if rank != 0:
         return None
     wl = workload(args)
     argv = strip_args(sys.argv[1:])
-    steps_total = args.steps + args.warmup
-    # each step gets an equal share of about two minutes of oracle time
-    per_step = 120.0 / steps_total
-    r = run_oracle(argv, per_step, steps=steps_total)["steps"][args.warmup:]
-    tokens = sum(s["tokens"] for s in r)
-    secs = sum(s["seconds"] for s in r)
+    ncpu = os.cpu_count() or 1
+    experts = 2
+    r = run_oracle(argv, ncpu, steps=args.steps + args.warmup, experts_per_step=experts)
+    timed = r["steps"][args.warmup:]
+    tokens = sum(s["tokens"] for s in timed)
+    secs = sum(s["seconds"] for s in timed)
     value = tokens / secs if secs > 0 else 0.0
+    sample = (oracle_sample_text(wl, experts, len(timed), r["n_sub"]) +
+              f"; {ncpu} threads in the BLAS calls")
     return {
         "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / len(r) * 1e3, 3),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / len(timed) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": wl.name, "N": wl.N, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
-                   "W": wl.W, "dedup": wl.dedup, "placement": wl.placement},
-        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"each step: routed (token, expert) pairs of the {wl.name} "
-                                   f"workload whose expert is one of the first four routed to, "
-                                   f"for ~{per_step:.2f} s of oracle time, at least one pair "
-                                   f"({tokens:.3g} tokens over {len(r)} timed steps)"},
+        "config": workload_config(wl),
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": ncpu,
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

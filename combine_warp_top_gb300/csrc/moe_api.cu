@@ -1,6 +1,8 @@
 // C ABI entry points of libmoe: argument checks, workspace sizing, and the
 // chaining of the kernels of the other files on the caller's stream.
 // Declarations and the contract of every call are in include/moe.h.
+#include <nvtx3/nvToolsExt.h>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -85,6 +87,18 @@ inline bool aligned16(const T*... p) {
     return ((((uintptr_t)p & 15u) == 0) && ...);
 }
 
+// An NVTX range named after the entry point around every call that enqueues
+// work: profilers (Nsight Systems, ncu's NVTX filters) show the C ABI calls on
+// the timeline.  With no tool attached a push/pop is a check of one function
+// pointer.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define MOE_RANGE() const NvtxRange _moe_nvtx_range(__func__)
+
 #define MOE_TRY(expr)                     \
     do {                                  \
         const moe_status _st = (expr);    \
@@ -105,6 +119,7 @@ size_t moe_workspace_bytes(const moe_shape* shape) {
 
 moe_status moe_route(const float* logits, const moe_shape* shape, int32_t* topk_ids,
                      float* topk_w, void* stream) {
+    MOE_RANGE();
     MOE_TRY(check_shape(shape));
     if (shape->N == 0) return MOE_OK;
     if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
@@ -114,6 +129,7 @@ moe_status moe_route(const float* logits, const moe_shape* shape, int32_t* topk_
 
 moe_status moe_route_full_softmax(const float* logits, const moe_shape* shape, int32_t* topk_ids,
                                   float* topk_w, void* stream) {
+    MOE_RANGE();
     MOE_TRY(check_shape(shape));
     if (shape->N == 0) return MOE_OK;
     if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
@@ -123,6 +139,7 @@ moe_status moe_route_full_softmax(const float* logits, const moe_shape* shape, i
 
 moe_status moe_route_sigmoid_bias(const float* logits, const float* bias, const moe_shape* shape,
                                   int32_t* topk_ids, float* topk_w, void* stream) {
+    MOE_RANGE();
     MOE_TRY(check_shape(shape));
     if (shape->N == 0) return MOE_OK;
     if (!logits || !bias || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
@@ -133,6 +150,7 @@ moe_status moe_route_sigmoid_bias(const float* logits, const float* bias, const 
 moe_status moe_dispatch_layout(const int32_t* topk_ids, const int32_t* placement,
                                const moe_shape* shape, const moe_layout* layout, void* ws,
                                size_t ws_bytes, void* stream) {
+    MOE_RANGE();
     MOE_TRY(check_shape(shape));
     MOE_TRY(check_layout(layout, shape));
     MOE_TRY(check_ws(shape, ws, ws_bytes));
@@ -143,6 +161,7 @@ moe_status moe_dispatch_layout(const int32_t* topk_ids, const int32_t* placement
 
 moe_status moe_dispatch(const uint16_t* x, const moe_layout* layout, const moe_shape* shape,
                         uint16_t* xd, void* stream) {
+    MOE_RANGE();
     MOE_TRY(check_shape(shape));
     MOE_TRY(check_layout(layout, shape));
     if (shape->N == 0) return MOE_OK;
@@ -153,6 +172,7 @@ moe_status moe_dispatch(const uint16_t* x, const moe_layout* layout, const moe_s
 
 moe_status moe_expand(const uint16_t* xd, const moe_layout* layout, const moe_shape* shape,
                       uint16_t* xe, void* stream) {
+    MOE_RANGE();
     MOE_TRY(check_shape(shape));
     MOE_TRY(check_layout(layout, shape));
     if (!shape->dedup) return MOE_ERR_INVALID_ARG;
@@ -165,6 +185,7 @@ moe_status moe_expand(const uint16_t* xd, const moe_layout* layout, const moe_sh
 moe_status moe_ffn_gate_up(const uint16_t* rows, const moe_layout* layout, const moe_shape* shape,
                            const uint16_t* w_gate, const uint16_t* w_up, uint16_t* h, void* ws,
                            size_t ws_bytes, void* stream) {
+    MOE_RANGE();
     MOE_TRY(check_shape(shape));
     MOE_TRY(check_layout(layout, shape));
     MOE_TRY(check_ws(shape, ws, ws_bytes));
@@ -181,6 +202,7 @@ moe_status moe_ffn_gate_up_gather(const uint16_t* src, const int32_t* row_index,
                                   const moe_layout* layout, const moe_shape* shape,
                                   const uint16_t* w_gate, const uint16_t* w_up, uint16_t* h,
                                   void* ws, size_t ws_bytes, void* stream) {
+    MOE_RANGE();
     MOE_TRY(check_shape(shape));
     MOE_TRY(check_layout(layout, shape));
     MOE_TRY(check_ws(shape, ws, ws_bytes));
@@ -195,6 +217,7 @@ moe_status moe_ffn_gate_up_gather(const uint16_t* src, const int32_t* row_index,
 moe_status moe_ffn_down(const uint16_t* h, const moe_layout* layout, const moe_shape* shape,
                         const uint16_t* w_down, uint16_t* y, void* ws, size_t ws_bytes,
                         void* stream) {
+    MOE_RANGE();
     MOE_TRY(check_shape(shape));
     MOE_TRY(check_layout(layout, shape));
     MOE_TRY(check_ws(shape, ws, ws_bytes));
@@ -211,6 +234,7 @@ moe_status moe_ffn_down_combine(const uint16_t* h, const float* topk_w, const mo
                                 const moe_shape* shape, const uint16_t* w_down,
                                 const uint16_t* residual, float* acc, uint16_t* out, void* ws,
                                 size_t ws_bytes, void* stream) {
+    MOE_RANGE();
     MOE_TRY(check_shape(shape));
     MOE_TRY(check_layout(layout, shape));
     MOE_TRY(check_ws(shape, ws, ws_bytes));
@@ -230,6 +254,7 @@ moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const mo
                           const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
                           uint16_t* xe, uint16_t* h, uint16_t* y, void* ws, size_t ws_bytes,
                           void* stream) {
+    MOE_RANGE();
     MOE_TRY(check_shape(shape));
     MOE_TRY(check_layout(layout, shape));
     MOE_TRY(check_ws(shape, ws, ws_bytes));
@@ -252,6 +277,7 @@ moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const mo
 moe_status moe_combine(const uint16_t* y, const float* topk_w, const moe_layout* layout,
                        const moe_shape* shape, uint16_t* partial, const uint16_t* residual,
                        uint16_t* out, void* stream) {
+    MOE_RANGE();
     MOE_TRY(check_shape(shape));
     MOE_TRY(check_layout(layout, shape));
     if (shape->N == 0) return MOE_OK;
@@ -265,6 +291,7 @@ moe_status moe_shared_expert_ffn(const uint16_t* x, const moe_shape* shape, int3
                                  const uint16_t* w_gate_s, const uint16_t* w_up_s,
                                  const uint16_t* w_down_s, uint16_t* h_s, uint16_t* y_s, void* ws,
                                  size_t ws_bytes, void* stream) {
+    MOE_RANGE();
     MOE_TRY(check_shape(shape));
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (I_shared <= 0) return MOE_ERR_INVALID_ARG;
@@ -287,6 +314,7 @@ moe_status moe_shared_expert_ffn(const uint16_t* x, const moe_shape* shape, int3
 moe_status moe_combine_shared(const uint16_t* y, const float* topk_w, const moe_layout* layout,
                               const moe_shape* shape, uint16_t* partial, const uint16_t* y_shared,
                               const uint16_t* residual, uint16_t* out, void* stream) {
+    MOE_RANGE();
     MOE_TRY(check_shape(shape));
     MOE_TRY(check_layout(layout, shape));
     if (shape->N == 0) return MOE_OK;
@@ -303,6 +331,7 @@ moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32
                              const moe_layout* layout, uint16_t* xd, uint16_t* xe, uint16_t* h,
                              uint16_t* y, uint16_t* partial, uint16_t* out, void* ws,
                              size_t ws_bytes, void* stream) {
+    MOE_RANGE();
     MOE_TRY(check_shape(shape));
     MOE_TRY(check_layout(layout, shape));
     MOE_TRY(check_ws(shape, ws, ws_bytes));
@@ -337,6 +366,7 @@ int32_t moe_layer_skips_dispatch(const moe_shape* shape) {
 
 moe_status moe_coselection(const int32_t* topk_ids, const moe_shape* shape, int32_t* coselect,
                            void* ws, size_t ws_bytes, void* stream) {
+    MOE_RANGE();
     MOE_TRY(check_shape(shape));
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (!coselect || (shape->N > 0 && !topk_ids)) return MOE_ERR_INVALID_ARG;
@@ -347,6 +377,7 @@ moe_status moe_coselection(const int32_t* topk_ids, const moe_shape* shape, int3
 
 moe_status moe_placement_search(const int32_t* coselect, int32_t E, int32_t ranks, int32_t nodes,
                                 int64_t max_swaps, int32_t* placement, int64_t* swaps_made) {
+    MOE_RANGE();
     if (!coselect || !placement || E <= 0 || ranks <= 0 || nodes <= 0 || max_swaps < 0)
         return MOE_ERR_INVALID_ARG;
     if (ranks % nodes != 0 || E % ranks != 0) return MOE_ERR_INVALID_ARG;
@@ -357,12 +388,14 @@ moe_status moe_placement_search(const int32_t* coselect, int32_t E, int32_t rank
 }
 
 moe_status moe_selftest_wait_timeout(void* ws, int64_t limit_cycles, void* stream) {
+    MOE_RANGE();
     if (!ws) return MOE_ERR_WORKSPACE;
     if (limit_cycles <= 0 || limit_cycles > (int64_t)1 << 32) return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_wait_selftest(limit_cycles, ws_ptr<int>(ws, 0), as_stream(stream)));
 }
 
 moe_status moe_get_error(void* ws, void* stream) {
+    MOE_RANGE();
     if (!ws) return MOE_ERR_WORKSPACE;
     cudaStream_t st = as_stream(stream);
     int code = 0;

@@ -88,3 +88,22 @@ def test_recorded_traffic_follows_the_gemm_sources(tmp_path, monkeypatch):
     with open(tmp_path / bench.TRAFFIC_SOURCES[2], "a") as f:
         f.write("static int changed_code;\n")
     assert bench.recorded_traffic(bench.workload(args)) is None
+
+
+def test_oracle_worker_times_every_stage_of_a_step():
+    """The CPU baseline's worker times route, layout, dispatch, the sampled
+    expert FFN (scaled to all rows) and the combine, in a one-thread process."""
+    r = bench.run_oracle(["--workload", "tiny"], threads=1, steps=2, experts_per_step=2)
+    assert r["threads"] == 1 and len(r["steps"]) == 2
+    for st in r["steps"]:
+        assert set(st["stage_s"]) == {"route", "layout", "dispatch", "ffn", "combine"}
+        assert st["tokens"] == 64 and st["seconds"] > 0
+        assert st["rows_sampled"] > 0 and len(st["experts"]) == 2
+    # successive steps sample different experts of one permutation
+    assert r["steps"][0]["experts"] != r["steps"][1]["experts"]
+
+
+def test_oracle_worker_dedup_combine_sample():
+    r = bench.run_oracle(["--workload", "correlated_placed", "--tokens", "300"], threads=1,
+                         steps=1, experts_per_step=1)
+    assert r["steps"][0]["tokens"] == 300 and r["n_sub"] == 300

@@ -24,7 +24,8 @@ def bench_line(*args):
 
 
 @pytest.mark.parametrize("extra", [[], ["--eager"], ["--workload", "correlated_placed",
-                                                      "--tokens", "2048"]])
+                                                      "--tokens", "2048"],
+                                   ["--others", "tiny"]])
 def test_bench_json_contract(extra):
     args = ["--workload", "tiny", "--steps", "3", "--warmup", "3", "--no-cpu-baseline",
             "--e2e-steps", "3"]
@@ -46,3 +47,15 @@ def test_bench_json_contract(extra):
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] > 0
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    if "--others" in extra:
+        # one compact entry per extra workload, measured like the headline
+        o = d["workloads"]["tiny"]
+        for key in ("value", "unit", "ms_per_step", "config", "roofline", "stages",
+                    "dispatch_rows", "gpu_launches", "clocks"):
+            assert key in o, key
+        assert o["value"] > 0 and o["roofline"]["frac"] > 0
+    rows = d["dispatch_rows"]
+    for key in ("plain", "dedup", "dedup_reduction", "ranks_per_token", "same_rank_share",
+                "max_over_mean_expert_load"):
+        assert key in rows, key
+    assert abs(rows["ranks_per_token"] - rows["dedup"] / d["config"]["N"]) < 1e-3

@@ -6,7 +6,16 @@ Integer results are checked in full against the oracle: routing ids, every
 layout table, the dedup row count.  Copies are checked bit for bit on sampled
 rows.  Float outputs are checked on sampled tokens, each recomputed by the
 oracle straight from the MoE definition with host-generated weights of the
-experts those tokens use."""
+experts those tokens use (each expert's weights generated and widened once).
+
+Tile-coverage rule of the float check: the sampled tokens are chosen so that
+every (expert, 128-row block) tile of the plain expert-major rows holds at
+least one checked row, and the last row of every expert's segment (its ragged
+tail) is checked.  A 128-row block is the single-CTA kernel's tile and half of
+the CTA-pair kernel's 256-row tile (both start at the segment's first row), so
+every tile of either GEMM kernel, in every n-block (a checked row is checked
+in all its columns), reaches the check, and so does every token block of the
+combine through the checked tokens' rows."""
 import numpy as np
 import pytest
 import torch
@@ -17,9 +26,69 @@ from gpu_util import assert_close, dev_i32, host_f64, host_u16
 
 pytestmark = pytest.mark.gpu
 
-# workload -> number of sampled tokens for the float check
-SAMPLES = {"deepseek_v3": 8, "mixtral": 16, "correlated_contiguous": 24, "correlated_placed": 24,
-           "skewed": 12}
+WORKLOADS = ["deepseek_v3", "mixtral", "correlated_contiguous", "correlated_placed", "skewed"]
+# tokens sampled for the option checks that are not the benchmarked path
+SAMPLES = {"deepseek_v3": 8, "correlated_placed": 24}
+BLOCK = 128
+
+
+def tile_covering_tokens(ref, N, k, rng, block=BLOCK):
+    """Tokens whose rows reach every (expert, block-row) tile of the plain
+    expert-major rows and every expert's last row: first the token of each
+    non-empty expert's last row, then, visiting the tiles in a seeded random
+    order, the token of a random row of each tile not yet reached (a token
+    reaches the tiles of all k of its rows).  Returns (tokens, tile count)."""
+    off, cnt = ref["expert_offsets"], ref["expert_counts"]
+    row_token, pair_row = ref["row_token"], ref["pair_row"]
+    tile_of_row = np.empty(N * k, np.int64)
+    tiles = []  # (first row, last row) of every tile
+    for e in range(len(cnt)):
+        a, n = int(off[e]), int(cnt[e])
+        for b0 in range(0, n, block):
+            tile_of_row[a + b0:a + min(n, b0 + block)] = len(tiles)
+            tiles.append((a + b0, a + min(n, b0 + block) - 1))
+    covered = np.zeros(len(tiles), bool)
+    chosen = [0, N - 1] + [int(row_token[int(off[e]) + int(cnt[e]) - 1])
+                           for e in range(len(cnt)) if cnt[e] > 0]
+    for t in chosen:
+        covered[tile_of_row[pair_row[t]]] = True
+    for i in rng.permutation(len(tiles)):
+        if not covered[i]:
+            first, last = tiles[i]
+            t = int(row_token[int(rng.integers(first, last + 1))])
+            chosen.append(t)
+            covered[tile_of_row[pair_row[t]]] = True
+    assert covered.all()
+    return np.unique(np.array(chosen, np.int64)), len(tiles)
+
+
+def prefetched_weights(wl, experts, asked, ahead=2):
+    """weights_of(e) for oracle.token_outputs, which asks for the experts in
+    ascending order: host-generated bf16 weights of expert e, the next experts'
+    generated on a worker thread while the oracle works on this one."""
+    from concurrent.futures import ThreadPoolExecutor
+    order = [int(e) for e in sorted(experts)]
+    pool = ThreadPoolExecutor(1)
+    futures = {}
+
+    def gen(e):
+        return tuple(synth.make_weight(wl, m, experts=[e])[0] for m in ("gate", "up", "down"))
+
+    def submit(i):
+        if i < len(order) and order[i] not in futures:
+            futures[order[i]] = pool.submit(gen, order[i])
+
+    for i in range(ahead):
+        submit(i)
+
+    def weights_of(e):
+        asked.append(e)
+        i = order.index(e)
+        for j in range(i, i + ahead + 1):
+            submit(j)
+        return futures.pop(e).result()
+
+    return weights_of
 
 
 def bf16_host(a):
@@ -48,7 +117,7 @@ def run_full(name, fuse_combine=False):
     return wl, layer, L, x, res, placement, out
 
 
-@pytest.mark.parametrize("name", list(SAMPLES))
+@pytest.mark.parametrize("name", WORKLOADS)
 def test_full_size_workload(name):
     wl, layer, L, x, res, placement, out = run_full(name)
     N, k = wl.N, wl.k
@@ -86,18 +155,17 @@ def test_full_size_workload(name):
         rows = rng.choice(N * k, size=512, replace=False)
         xd = xd_buf[torch.from_numpy(rows).cuda()]
         assert np.array_equal(host_u16(xd), x[ref["row_token"][rows]])
-    # float outputs on sampled tokens (the first, the last and random ones)
-    n = SAMPLES[wl.name]
-    toks = np.unique(np.concatenate([[0, N - 1], rng.choice(N, size=n - 2, replace=False)]))
-    cache = {}
-
-    def weights_of(e):
-        if e not in cache:
-            cache.clear()
-            cache[e] = tuple(synth.make_weight(wl, m, experts=[e])[0] for m in ("gate", "up", "down"))
-        return cache[e]
-
+    # every output finite (a property at any size)
+    assert bool(torch.isfinite(out.float()).all())
+    # float outputs on the tokens that reach every GEMM tile (module docstring)
+    toks, n_tiles = tile_covering_tokens(ref, N, k, rng)
+    # each expert's weights are generated and widened once: token_outputs asks
+    # for every expert once, in ascending order
+    asked = []
+    weights_of = prefetched_weights(wl, np.unique(ref_ids[toks]), asked)
     want, y_want = oracle.token_outputs(x[toks], ref_ids[toks], ref_w[toks], weights_of, res[toks])
+    assert len(asked) == len(set(asked))
+    print(f"{name}: {len(toks)} tokens checked, {n_tiles} tiles, {len(asked)} experts")
     got_out = host_f64(out[torch.from_numpy(toks).cuda()])
     assert_close(got_out, want, f"{name} out")
     # the MoE delta alone: rerun without the residual (subtracting it from the
