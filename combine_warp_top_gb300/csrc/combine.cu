@@ -10,11 +10,13 @@
 // owner); FarSkip-Collective Sec. 3 (the layer output is added into the
 // residual stream).
 //
-// One warp per output row.  Each lane owns U 16-byte chunks (8 bf16 each) per
-// step along the row; the source rows of a chunk are loaded together, then
-// accumulated in fp32 in j order.  These are latency-bound chains of loads,
-// so the dedup kernels are compiled with register caps that keep 24-32 warps
-// per SM in flight where that costs no spills.
+// The plain combine runs on persistent warps that each walk units of (token,
+// 2 x 512-byte column stripes), with the next unit's row indices loaded while
+// the current unit's rows are in flight.  The dedup kernels take one warp per
+// output row; each lane owns U 16-byte chunks (8 bf16 each) per step along the
+// row, the source rows of a chunk are loaded together, then accumulated in
+// fp32 in j order.  These are latency-bound chains of loads, so the kernels
+// are compiled with register caps that keep 24-32 warps per SM in flight.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -155,23 +157,92 @@ __device__ __forceinline__ void finish(float (&acc)[U][8], const uint4* shared,
     }
 }
 
-// Plain combine: out[t] = bf16(residual[t] + sum_j w[t,j] * y[pair_row[t,j]]).
-template <int U>
-__global__ void __launch_bounds__(kThreads) combine_kernel(
+// Plain combine, persistent: warps walk units (token t, group of kU stripes of
+// 32 lanes x 16 bytes); lane l covers chunks s*32*kU + q*32 + l (q < kU) of the
+// token's k source rows, the shared row and the residual.  All loads of a unit
+// are issued before any is used (source rows kKB at a time), and the pair_row
+// and topk_w entries of the warp's NEXT unit are loaded while this unit's rows
+// are in flight, so no unit waits on its own index load.  Sums in j order in
+// fp32, then + shared, then + residual:
+// out[t] = bf16(residual[t] + shared[t] + sum_j w[t,j] * y[pair_row[t,j]]).
+template <int kU, int kKB, bool kShared>
+__global__ void __launch_bounds__(kThreads, kShared ? 3 : 4) combine_rows_kernel(
     const uint4* __restrict__ y, const float* __restrict__ topk_w,
-    const int32_t* __restrict__ pair_row, int N, int C, int k, int R, const uint4* shared,
-    const uint4* residual, uint4* out) {
+    const int32_t* __restrict__ pair_row, int N, int C, int k, int R, int groups,
+    const uint4* __restrict__ shared, const uint4* __restrict__ residual,
+    uint4* __restrict__ out) {
     const int lane = threadIdx.x & 31;
-    const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
-    if (t >= N) return;
-    const int my_row = lane < k ? clamp_row(pair_row[(size_t)t * k + lane], R) : 0;
-    const float my_w = lane < k ? topk_w[(size_t)t * k + lane] : 0.f;
-    const uint32_t all = k >= 32 ? 0xffffffffu : ((1u << k) - 1u);
-    for (int c0 = 0; c0 < C; c0 += 32 * U) {
-        float acc[U][8];
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const long long units = (long long)N * groups;
+    long long u = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    int next_row = 0;
+    float next_w = 0.f;
+    if (u < units && lane < k) {
+        const size_t i = (size_t)(u / groups) * k + lane;
+        next_row = clamp_row(pair_row[i], R);
+        next_w = topk_w[i];
+    }
+    for (; u < units; u += nwarps) {
+        const int t = (int)(u / groups);
+        const int c0 = (int)(u % groups) * 32 * kU + lane;
+        const int my_row = next_row;
+        const float my_w = next_w;
+        const size_t base = (size_t)t * C;
+        uint4 r[kU], sh[kU];
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+            const int c = c0 + q * 32;
+            if (c < C) {
+                if (kShared) sh[q] = shared[base + c];
+                if (residual) r[q] = residual[base + c];
+            }
+        }
+        float acc[kU][8];
         zero(acc);
-        gather_weighted<U>(acc, y, C, c0, all, my_row, my_w);
-        finish<U>(acc, shared, residual, out, (size_t)t * C, C, c0);
+        for (int j0 = 0; j0 < k; j0 += kKB) {
+            uint4 v[kKB][kU];
+#pragma unroll
+            for (int b = 0; b < kKB; ++b) {
+                if (j0 + b < k) {
+                    const int row = __shfl_sync(0xffffffffu, my_row, j0 + b);
+                    const uint4* src = y + (size_t)row * C;
+#pragma unroll
+                    for (int q = 0; q < kU; ++q) {
+                        const int c = c0 + q * 32;
+                        if (c < C) v[b][q] = src[c];
+                    }
+                }
+            }
+            if (j0 == 0) {
+                // the next unit's indices, while this unit's rows are in flight
+                const long long un = u + nwarps;
+                if (un < units && lane < k) {
+                    const size_t i = (size_t)(un / groups) * k + lane;
+                    next_row = clamp_row(pair_row[i], R);
+                    next_w = topk_w[i];
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kKB; ++b) {
+                if (j0 + b < k) {
+                    const float w = __shfl_sync(0xffffffffu, my_w, j0 + b);
+#pragma unroll
+                    for (int q = 0; q < kU; ++q) {
+                        const int c = c0 + q * 32;
+                        if (c < C) acc_bf16x8(acc[q], v[b][q], w);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+            const int c = c0 + q * 32;
+            if (c < C) {
+                if (kShared) add_bf16x8(acc[q], sh[q]);
+                if (residual) add_bf16x8(acc[q], r[q]);
+                out[base + c] = pack_bf16x8(acc[q]);
+            }
+        }
     }
 }
 
@@ -252,7 +323,9 @@ __global__ void __launch_bounds__(kThreads, U == 4 ? 2 : 3) owner_sum_kernel(
 // The token's k source rows are put in that (d, j) order once; the row loop
 // then loads B of them at a time whatever the groups, and a partial is
 // rounded and added where its group ends, so the loads of several dedup rows
-// are in flight together.
+// are in flight together.  The residual chunk of the next step along the row
+// is loaded together with this step's first source rows, so a step waits on
+// one round of loads instead of two.
 template <int U, int B>
 __global__ void __launch_bounds__(kThreads, U == 1 ? 4 : (U == 2 ? 2 : 1)) dedup_combine_kernel(
     const uint4* __restrict__ y, const float* __restrict__ topk_w,
@@ -284,10 +357,20 @@ __global__ void __launch_bounds__(kThreads, U == 1 ? 4 : (U == 2 ? 2 : 1)) dedup
     const int next_d = __shfl_down_sync(0xffffffffu, s_d, 1);
     // bit p: position p is the last row of its dedup row
     const uint32_t ends = __ballot_sync(0xffffffffu, live && (lane == k - 1 || next_d != s_d));
+    const size_t base = (size_t)t * C;
+    uint4 res_next[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int c = u * 32 + lane;
+        if (residual && c < C) res_next[u] = residual[base + c];
+    }
     for (int c0 = 0; c0 < C; c0 += 32 * U) {
         float acc[U][8], part[U][8];
         zero(acc);
         zero(part);
+        uint4 res_here[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) res_here[u] = res_next[u];
         for (int p0 = 0; p0 < k; p0 += B) {
             uint4 v[B][U];
 #pragma unroll
@@ -300,6 +383,13 @@ __global__ void __launch_bounds__(kThreads, U == 1 ? 4 : (U == 2 ? 2 : 1)) dedup
                         const int c = c0 + u * 32 + lane;
                         if (c < C) v[b][u] = row[c];
                     }
+                }
+            }
+            if (p0 == 0) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = c0 + 32 * U + u * 32 + lane;
+                    if (residual && c < C) res_next[u] = residual[base + c];
                 }
             }
 #pragma unroll
@@ -323,7 +413,15 @@ __global__ void __launch_bounds__(kThreads, U == 1 ? 4 : (U == 2 ? 2 : 1)) dedup
                 }
             }
         }
-        finish<U>(acc, shared, residual, out, (size_t)t * C, C, c0);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = c0 + u * 32 + lane;
+            if (c < C) {
+                if (shared) add_bf16x8(acc[u], shared[base + c]);
+                if (residual) add_bf16x8(acc[u], res_here[u]);
+                out[base + c] = pack_bf16x8(acc[u]);
+            }
+        }
     }
 }
 
@@ -371,12 +469,23 @@ cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& 
     if (!s.dedup) {
         const uint4* yy = reinterpret_cast<const uint4*>(y);
         uint4* o = reinterpret_cast<uint4*>(out);
-        // four chunks per lane whatever k: each source row is read 2 KB at a
-        // time (rows in batches of two), which measured faster from HBM than
-        // more rows of 512 B at once (k = 8: 0.117 -> 0.107 ms on the
-        // DeepSeek-V3 shape)
-        combine_kernel<4><<<warps_grid(s.N), kThreads, 0, st>>>(yy, w, L.pair_row, s.N, C, s.k,
-                                                                 R, sh, res, o);
+        // persistent warps, two 16-byte chunks per lane, source rows two at a
+        // time, the next unit's indices prefetched (measured against
+        // combine_kernel<4>: 0.86 -> 0.935 of HBM on the DeepSeek-V3 shape,
+        // 0.76 -> 0.84 on Mixtral's k = 2, 0.97 -> 1.0 on the skewed shape)
+        constexpr int kU = 2, kKB = 2;
+        const int groups = (C + 32 * kU - 1) / (32 * kU);
+        const long long units = (long long)s.N * groups;
+        const int per_sm = sh ? 3 : 4;
+        long long blocks = (units + kThreads / 32 - 1) / (kThreads / 32);
+        const long long cap = (long long)sm_count() * per_sm;
+        if (blocks > cap) blocks = cap;
+        if (sh)
+            combine_rows_kernel<kU, kKB, true><<<(int)blocks, kThreads, 0, st>>>(
+                yy, w, L.pair_row, s.N, C, s.k, R, groups, sh, res, o);
+        else
+            combine_rows_kernel<kU, kKB, false><<<(int)blocks, kThreads, 0, st>>>(
+                yy, w, L.pair_row, s.N, C, s.k, R, groups, nullptr, res, o);
         return cudaGetLastError();
     }
     const int Rd_max = s.N * (s.k < s.W ? s.k : s.W);

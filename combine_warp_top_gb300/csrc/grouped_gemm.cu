@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1)
                         const __grid_constant__ CUtensorMap tmOut,
                         const int32_t* __restrict__ expert_offsets,
                         const int32_t* __restrict__ expert_counts,
-                        const int32_t* __restrict__ mblk_prefix, int E, int K, int n_out,
+                        int E, int K, int n_out,
                         __nv_bfloat16* __restrict__ out, int* err,
                         const int32_t* __restrict__ a_rows, int a_total, int a_src_rows,
                         const uint16_t* __restrict__ a_src, int a_keep, const CombineArgs cmb) {
@@ -116,11 +116,14 @@ __global__ void __launch_bounds__(threads_for(kGather), 1)
     const int NB = (n_out + BNo - 1) / BNo;
     const int KB = (K + BK - 1) / BK;
 
-    for (int i = threadIdx.x; i <= E; i += blockDim.x) ctl->prefix[i] = mblk_prefix[i];
     for (int i = threadIdx.x; i < E; i += blockDim.x) {
         ctl->offs[i] = expert_offsets[i];
         ctl->cnts[i] = expert_counts[i];
     }
+    __syncthreads();
+    // the tile schedule: m-blocks before each expert, from the counts (an
+    // epilogue warp, idle until the first accumulator is ready)
+    if (warp == 2) warp_mblk_prefix(ctl->cnts, E, BM, ctl->prefix);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             // kGather: the producer's arrive plus one cp.async arrival per gather thread
@@ -456,40 +459,6 @@ __global__ void __launch_bounds__(threads_for(kGather), 1)
     }
 }
 
-// m-blocks per expert, exclusive prefix over expert ids: mblk_prefix[E+1];
-// one more entry, mblk_prefix[E+1], is reset to 0 for the tile counter.
-__global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* __restrict__ counts, int E,
-                                                        int bm, int32_t* __restrict__ mblk_prefix) {
-    __shared__ int warp_sums[32];
-    const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
-    const int v = e < E ? (counts[e] + bm - 1) / bm : 0;
-    int incl = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-    }
-    if (lane == 31) warp_sums[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const int ws = warp_sums[lane];
-        int wi = ws;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, wi, off);
-            if (lane >= off) wi += o;
-        }
-        warp_sums[lane] = wi - ws;
-    }
-    __syncthreads();
-    const int excl = warp_sums[warp] + incl - v;
-    if (e < E) mblk_prefix[e] = excl;
-    if (e == E - 1) {
-        mblk_prefix[E] = excl + v;
-        mblk_prefix[E + 1] = 0;  // tile counter of a dynamically scheduled GEMM
-    }
-}
-
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -534,12 +503,6 @@ bool map_3d(CUtensorMap* m, const void* ptr, uint64_t E, uint64_t rows, uint64_t
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_schedule(const int32_t* counts, int E, int bm, int32_t* prefix,
-                            cudaStream_t st) {
-    schedule_kernel<<<1, 1024, 0, st>>>(counts, E, bm, prefix);
-    return cudaGetLastError();
-}
-
 namespace {
 
 bool set_smem_attr() {
@@ -557,12 +520,11 @@ bool set_smem_attr() {
                                 (int)kSmemBytes) == cudaSuccess;
 }
 
-// Writes the m-block prefix of the tile schedule and returns the persistent
-// grid size for a GEMM with `n_blocks` n-blocks: never more CTAs than tiles,
-// never more than one per SM.
+// The persistent grid size for a GEMM with `n_blocks` n-blocks: never more
+// CTAs than tiles, never more than one per SM.  (The kernel derives the tile
+// schedule itself from the expert counts.)
 moe_status schedule(const GemmGroup& g, long long n_blocks, cudaStream_t st, int* grid) {
-    schedule_kernel<<<1, 1024, 0, st>>>(g.counts, g.E, BM, g.prefix);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    (void)st;
     // tiles <= n_blocks * (ceil(R / BM) + E): each expert adds at most one ragged m-block
     const long long tiles = n_blocks * ((g.R + BM - 1) / BM + g.E);
     const int sms = sm_count();
@@ -596,11 +558,11 @@ moe_status launch_gate_up(const uint16_t* rows, const GemmGroup& g, int H, int I
     __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(h);
     if (gather)
         grouped_gemm_kernel<true, true, false><<<grid, threads_for(true), kSmemBytes, st>>>(
-            a, bg, bu, o, g.offsets, g.counts, g.prefix, g.E, H, I, hb, g.err, gather, (int)g.R,
+            a, bg, bu, o, g.offsets, g.counts, g.E, H, I, hb, g.err, gather, (int)g.R,
             (int)src_rows, rows, keep_src ? 1 : 0, CombineArgs{});
     else
         grouped_gemm_kernel<true, false, false><<<grid, kThreads, kSmemBytes, st>>>(
-            a, bg, bu, o, g.offsets, g.counts, g.prefix, g.E, H, I, hb, g.err, nullptr, 0, 0,
+            a, bg, bu, o, g.offsets, g.counts, g.E, H, I, hb, g.err, nullptr, 0, 0,
             nullptr, 0, CombineArgs{});
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -617,7 +579,7 @@ moe_status launch_down(const uint16_t* h, const GemmGroup& g, int H, int I, cons
     const moe_status ss = schedule(g, (H + kMmaN - 1) / kMmaN, st, &grid);
     if (ss != MOE_OK) return ss;
     grouped_gemm_kernel<false, false, false><<<grid, kThreads, kSmemBytes, st>>>(
-        a, bd, bd, o, g.offsets, g.counts, g.prefix, g.E, I, H,
+        a, bd, bd, o, g.offsets, g.counts, g.E, I, H,
         reinterpret_cast<__nv_bfloat16*>(y), g.err, nullptr, 0, 0, nullptr, 0, CombineArgs{});
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -634,7 +596,7 @@ moe_status launch_down_combine(const uint16_t* h, const GemmGroup& g, int H, int
     const moe_status ss = schedule(g, (H + kMmaN - 1) / kMmaN, st, &grid);
     if (ss != MOE_OK) return ss;
     grouped_gemm_kernel<false, false, true><<<grid, kThreads, kSmemBytes, st>>>(
-        a, bd, bd, o, g.offsets, g.counts, g.prefix, g.E, I, H, nullptr, g.err, nullptr, 0, 0,
+        a, bd, bd, o, g.offsets, g.counts, g.E, I, H, nullptr, g.err, nullptr, 0, 0,
         nullptr, 0, cmb);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -159,8 +159,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                              const __grid_constant__ CUtensorMap tmOut,
                              const int32_t* __restrict__ expert_offsets,
                              const int32_t* __restrict__ expert_counts,
-                             const int32_t* __restrict__ mblk_prefix, int E, int K, int n_out,
-                             __nv_bfloat16* __restrict__ out, int* err, int* tile_counter) {
+                             int E, int K, int n_out, __nv_bfloat16* __restrict__ out,
+                             int* err, int* tile_counter) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* tiles = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -176,11 +176,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int NB = (n_out + BNo - 1) / BNo;
     const int KB = (K + BK - 1) / BK;
 
-    for (int i = threadIdx.x; i <= E; i += blockDim.x) ctl->prefix[i] = mblk_prefix[i];
     for (int i = threadIdx.x; i < E; i += blockDim.x) {
         ctl->offs[i] = expert_offsets[i];
         ctl->cnts[i] = expert_counts[i];
     }
+    __syncthreads();
+    // the tile schedule: m-blocks of 256 rows before each expert, from the
+    // counts (an epilogue warp, idle until the first accumulator is ready)
+    if (warp == 2) warp_mblk_prefix(ctl->cnts, E, BMP, ctl->prefix);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), 1);
@@ -435,6 +438,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc_pair(tmem, kTmemCols);
     }
+    // The tile counter returns to zero for the next launch: every pair counts
+    // itself out once its scheduler is past its last fetch (the barriers
+    // above), and the last pair out resets both counters.  Nothing waits here.
+    if (leader && threadIdx.x == 0) {
+        __threadfence();
+        const int before = atomicAdd(tile_counter + 1, 1);
+        if (before == (int)(gridDim.x / 2) - 1) {
+            atomicExch(tile_counter, 0);
+            atomicExch(tile_counter + 1, 0);
+        }
+    }
 }
 
 bool set_pair_smem_attr() {
@@ -446,9 +460,10 @@ bool set_pair_smem_attr() {
                                 (int)kSmemBytes) == cudaSuccess;
 }
 
-// 256-row schedule; grid = 2 CTAs per pair, at most one CTA per SM.
+// Grid of the 256-row tiles: 2 CTAs per pair, at most one CTA per SM.  (The
+// kernel derives the tile schedule itself from the expert counts.)
 moe_status pair_schedule(const GemmGroup& g, long long n_blocks, cudaStream_t st, int* grid) {
-    if (launch_schedule(g.counts, g.E, BMP, g.prefix, st) != cudaSuccess) return MOE_ERR_CUDA;
+    (void)st;
     const long long tiles = n_blocks * ((g.R + BMP - 1) / BMP + g.E);
     const long long pairs_max = sm_count() / 2;
     const long long pairs = tiles < pairs_max ? tiles : pairs_max;
@@ -471,7 +486,7 @@ moe_status launch_gate_up_pair(const uint16_t* rows, const GemmGroup& g, int H, 
     const moe_status ss = pair_schedule(g, (I + kMmaN / 2 - 1) / (kMmaN / 2), st, &grid);
     if (ss != MOE_OK) return ss;
     grouped_gemm_pair_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(
-        a, bg, bu, o, g.offsets, g.counts, g.prefix, g.E, H, I,
+        a, bg, bu, o, g.offsets, g.counts, g.E, H, I,
         reinterpret_cast<__nv_bfloat16*>(h), g.err, g.prefix + g.E + 1);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -488,7 +503,7 @@ moe_status launch_down_pair(const uint16_t* h, const GemmGroup& g, int H, int I,
     const moe_status ss = pair_schedule(g, (H + kMmaN - 1) / kMmaN, st, &grid);
     if (ss != MOE_OK) return ss;
     grouped_gemm_pair_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(
-        a, bd, bd, o, g.offsets, g.counts, g.prefix, g.E, I, H,
+        a, bd, bd, o, g.offsets, g.counts, g.E, I, H,
         reinterpret_cast<__nv_bfloat16*>(y), g.err, g.prefix + g.E + 1);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

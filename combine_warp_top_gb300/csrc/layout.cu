@@ -8,15 +8,22 @@
 // expert IDs) and Appendix A-A2 (the receiver expands rows to expert-major
 // order).
 //
-// Three launches, all deterministic:
+// Two launches for small N, three otherwise, all deterministic:
 //  1. count:   per block of 256 tokens, one 32-bit mask per (warp, slot) and
 //              per (warp, rank) records which lanes (tokens) hit it; the block
 //              count of a key is the sum of the popcounts.  OR-ing the rank
 //              bits merges a token's experts on one rank for free, which is the
 //              deduplication.
-//  2. scan:    one block turns the per-block counts into exclusive bases
-//              (blocks in token order) and the totals into slot/rank offsets.
-//  3. scatter: each block rebuilds its masks; a pair's row is its warp's base
+//     scan:    the per-block counts become exclusive bases (blocks in token
+//              order) and the totals become slot/rank offsets.  With at most
+//              kFuseScanBlocks count blocks the last count block to finish
+//              does this (a completion counter in the workspace tells it that
+//              it is last; nothing waits), on a copy of the table in its shared
+//              memory; otherwise a separate one-block launch of 1024 threads
+//              does it (measured faster from 16 count blocks on: the one block
+//              of the fused form walks the table in a longer dependent chain
+//              than the launch it saves).
+//  2. scatter: each block rebuilds its masks; a pair's row is its warp's base
 //              plus the popcount of the lower lanes' bits, so tokens ascend
 //              inside every segment exactly as in a stable sort.
 #include "moe_internal.cuh"
@@ -25,6 +32,9 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 32 * kLayoutWarps;
+// Count blocks up to which the last count block runs the scan itself (their
+// tables always fit in the count kernel's shared memory).
+constexpr int kFuseScanBlocks = 2;
 
 // slot_of[e] = the placement slot holding expert e.  Invalid placements are
 // reported and resolved deterministically (lowest slot wins, unplaced experts
@@ -97,29 +107,6 @@ __device__ void build_masks(const Smem& s, const int32_t* __restrict__ ids, int 
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads) layout_count_kernel(
-    const int32_t* __restrict__ ids, const int32_t* __restrict__ placement, int N, int E, int k,
-    int W, int dedup, int32_t* __restrict__ blk_counts, int32_t* __restrict__ blk_rcounts,
-    int* err) {
-    extern __shared__ uint32_t sm[];
-    const Smem s = carve(sm, E, W);
-    build_slot_of(s.slot_of, placement, E, err);
-    build_masks(s, ids, N, E, k, W, dedup, err);
-    for (int p = threadIdx.x; p < E; p += blockDim.x) {
-        int c = 0;
-#pragma unroll
-        for (int w = 0; w < kLayoutWarps; ++w) c += __popc(s.mask[w * E + p]);
-        blk_counts[(size_t)blockIdx.x * E + p] = c;
-    }
-    if (dedup) {
-        for (int r = threadIdx.x; r < W; r += blockDim.x) {
-            int c = 0;
-#pragma unroll
-            for (int w = 0; w < kLayoutWarps; ++w) c += __popc(s.rmask[w * W + r]);
-            blk_rcounts[(size_t)blockIdx.x * W + r] = c;
-        }
-    }
-}
 
 // Exclusive scan of one value per thread over a block of up to 1024 threads.
 __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
@@ -150,14 +137,45 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
     return r;
 }
 
+// Exclusive scan of n values (n up to 4 * blockDim): each thread takes a run
+// of consecutive values.  out[i] = sum of in[0..i); *total = the sum.
+__device__ void block_scan_values(const int* in, int n, int* out, int* warp_sums, int* total) {
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int i0 = threadIdx.x * per, i1 = min(n, i0 + per);
+    int sum = 0;
+    for (int i = i0; i < i1; ++i) sum += in[i];
+    int run = block_exclusive_scan(sum, warp_sums, total);
+    for (int i = i0; i < i1; ++i) {
+        const int v = in[i];
+        out[i] = run;
+        run += v;
+    }
+    __syncthreads();
+}
+
 // Exclusive scan down every column of a [nb][ncol] table, in place, by the
-// whole block: the columns' rows are split into P = blockDim / ncol parts; each
-// thread sums its part (independent loads), the parts of a column are scanned
-// in shared memory, and each thread rewrites its rows with the running prefix.
-// totals[c] receives the column sum.  part_sums holds blockDim ints.
+// whole block (global or shared memory).  With ncol <= blockDim the rows of a
+// column are split into P = blockDim / ncol parts: each thread sums its part
+// (independent loads), the parts of a column are scanned through part_sums,
+// and each thread rewrites its rows with the running prefix; with more
+// columns than threads each thread walks whole columns.  totals[c] receives
+// the column sum.  part_sums holds blockDim ints.
 __device__ void columns_scan(int32_t* __restrict__ tab, int nb, int ncol, int* part_sums,
                              int* totals) {
-    const int P = blockDim.x / ncol;  // ncol <= blockDim
+    if (ncol > (int)blockDim.x) {
+        for (int c = threadIdx.x; c < ncol; c += blockDim.x) {
+            int run = 0;
+            for (int b = 0; b < nb; ++b) {
+                const int v = tab[(size_t)b * ncol + c];
+                tab[(size_t)b * ncol + c] = run;
+                run += v;
+            }
+            totals[c] = run;
+        }
+        __syncthreads();
+        return;
+    }
+    const int P = blockDim.x / ncol;
     const int c = threadIdx.x % ncol, part = threadIdx.x / ncol;
     const int L = (nb + P - 1) / P;
     const int b0 = part * L, b1 = min(nb, b0 + L);
@@ -187,48 +205,113 @@ __device__ void columns_scan(int32_t* __restrict__ tab, int nb, int ncol, int* p
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(1024) layout_scan_kernel(
-    const int32_t* __restrict__ placement, int nb, int E, int W, int dedup,
-    int32_t* __restrict__ blk_counts, int32_t* __restrict__ blk_rcounts,
-    int32_t* __restrict__ slot_start, moe_layout L) {
-    __shared__ int warp_sums[32];
-    __shared__ int total;
-    __shared__ int part_sums[1024];
-    __shared__ int col_totals[1024];
-    const int p = threadIdx.x;  // blockDim.x == 1024 >= E >= W
+// Scratch of the scan, in the block's shared memory.
+struct ScanSmem {
+    int part_sums[1024];
+    int totals[kMaxE];
+    int starts[kMaxE];
+    int warp_sums[32];
+    int total;
+};
 
-    columns_scan(blk_counts, nb, E, part_sums, col_totals);
-    const int cnt = p < E ? col_totals[p] : 0;
-    const int start = block_exclusive_scan(cnt, warp_sums, &total);
-    const int R = total;
-    __syncthreads();
-    if (p < E) {
+// The scan proper: per-block counts -> exclusive bases in place; column totals
+// -> slot and rank offsets, the layout's counts and offsets, and (dedup) the
+// dedup row counts and offsets.  tab / rtab: [nb][E] / [nb][W] tables in
+// global or shared memory.  Any block size; every thread of the block calls it.
+__device__ void scan_counts(const int32_t* __restrict__ placement, int nb, int E, int W,
+                            int dedup, int32_t* tab, int32_t* rtab,
+                            int32_t* __restrict__ slot_start, const moe_layout& L, ScanSmem& ss) {
+    columns_scan(tab, nb, E, ss.part_sums, ss.totals);
+    block_scan_values(ss.totals, E, ss.starts, ss.warp_sums, &ss.total);
+    const int R = ss.total;
+    const int per_rank = E / W;
+    for (int p = threadIdx.x; p < E; p += blockDim.x) {
+        const int start = ss.starts[p];
         slot_start[p] = start;
         int e = placement ? placement[p] : p;
         if (e < 0 || e >= E) e = 0;  // reported by the count kernel
-        L.expert_counts[e] = cnt;
+        L.expert_counts[e] = ss.totals[p];
         L.expert_offsets[e] = start;
-        const int per_rank = E / W;
         if (p % per_rank == 0) L.rank_offsets[p / per_rank] = start;
     }
-    if (p == 0) {
+    if (threadIdx.x == 0) {
         slot_start[E] = R;
         L.expert_offsets[E] = R;
         L.rank_offsets[W] = R;
     }
+    __syncthreads();
     if (!dedup) return;
-    columns_scan(blk_rcounts, nb, W, part_sums, col_totals);
-    const int rcnt = p < W ? col_totals[p] : 0;
-    const int rstart = block_exclusive_scan(rcnt, warp_sums, &total);
-    const int Rd = total;
-    if (p < W) {
-        L.dedup_counts[p] = rcnt;
-        L.dedup_offsets[p] = rstart;
+    columns_scan(rtab, nb, W, ss.part_sums, ss.totals);
+    block_scan_values(ss.totals, W, ss.starts, ss.warp_sums, &ss.total);
+    for (int r = threadIdx.x; r < W; r += blockDim.x) {
+        L.dedup_counts[r] = ss.totals[r];
+        L.dedup_offsets[r] = ss.starts[r];
     }
-    if (p == 0) {
-        L.dedup_offsets[W] = Rd;
-        *L.n_dedup_rows = Rd;
+    if (threadIdx.x == 0) {
+        L.dedup_offsets[W] = ss.total;
+        *L.n_dedup_rows = ss.total;
     }
+}
+
+// The scan as its own one-block launch, on the tables in global memory (for
+// tables larger than kScanSmemBytes).
+__global__ void __launch_bounds__(1024) layout_scan_kernel(
+    const int32_t* __restrict__ placement, int nb, int E, int W, int dedup,
+    int32_t* __restrict__ blk_counts, int32_t* __restrict__ blk_rcounts,
+    int32_t* __restrict__ slot_start, moe_layout L) {
+    __shared__ ScanSmem ss;
+    scan_counts(placement, nb, E, W, dedup, blk_counts, blk_rcounts, slot_start, L, ss);
+}
+
+// Count pass; with fuse_scan the last block to finish also runs the scan, on
+// a copy of the count tables in its (then free) dynamic shared memory.
+// done: completion counter, zero before the launch and reset to zero by the
+// last block.
+__global__ void __launch_bounds__(kThreads) layout_count_kernel(
+    const int32_t* __restrict__ ids, const int32_t* __restrict__ placement, int N, int E, int k,
+    int W, int dedup, int32_t* __restrict__ blk_counts, int32_t* __restrict__ blk_rcounts,
+    int* err, int fuse_scan, int* done, int32_t* __restrict__ slot_start, moe_layout L) {
+    extern __shared__ uint32_t sm[];
+    __shared__ ScanSmem ss;
+    __shared__ int is_last;
+    const Smem s = carve(sm, E, W);
+    build_slot_of(s.slot_of, placement, E, err);
+    build_masks(s, ids, N, E, k, W, dedup, err);
+    for (int p = threadIdx.x; p < E; p += blockDim.x) {
+        int c = 0;
+#pragma unroll
+        for (int w = 0; w < kLayoutWarps; ++w) c += __popc(s.mask[w * E + p]);
+        blk_counts[(size_t)blockIdx.x * E + p] = c;
+    }
+    if (dedup) {
+        for (int r = threadIdx.x; r < W; r += blockDim.x) {
+            int c = 0;
+#pragma unroll
+            for (int w = 0; w < kLayoutWarps; ++w) c += __popc(s.rmask[w * W + r]);
+            blk_rcounts[(size_t)blockIdx.x * W + r] = c;
+        }
+    }
+    if (!fuse_scan) return;
+    // publish this block's counts, then learn whether it is the last one
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = atomicAdd(done, 1) == (int)gridDim.x - 1;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    const int nb = gridDim.x;
+    int32_t* tab = reinterpret_cast<int32_t*>(sm);  // the masks are no longer needed
+    int32_t* rtab = tab + (size_t)nb * E;
+    for (size_t i = threadIdx.x; i < (size_t)nb * E; i += blockDim.x) tab[i] = blk_counts[i];
+    if (dedup)
+        for (size_t i = threadIdx.x; i < (size_t)nb * W; i += blockDim.x) rtab[i] = blk_rcounts[i];
+    __syncthreads();
+    scan_counts(placement, nb, E, W, dedup, tab, rtab, slot_start, L, ss);
+    __syncthreads();
+    for (size_t i = threadIdx.x; i < (size_t)nb * E; i += blockDim.x) blk_counts[i] = tab[i];
+    if (dedup)
+        for (size_t i = threadIdx.x; i < (size_t)nb * W; i += blockDim.x) blk_rcounts[i] = rtab[i];
+    if (threadIdx.x == 0) atomicExch(done, 0);
 }
 
 __global__ void __launch_bounds__(kThreads) layout_scatter_kernel(
@@ -294,8 +377,12 @@ cudaError_t launch_layout(const int32_t* ids, const int32_t* placement, const mo
     int32_t* blk_counts = ws_ptr<int32_t>(ws, wl.blk_counts);
     int32_t* blk_rcounts = ws_ptr<int32_t>(ws, wl.blk_rcounts);
     int32_t* slot_start = ws_ptr<int32_t>(ws, wl.slot_start);
+    int* done = ws_ptr<int>(ws, wl.err) + 1;  // completion counter of the count pass
     const int nb = layout_blocks(s.N);
     const size_t smem = smem_bytes(s.E, s.W);
+    // few count blocks: the last one scans the count tables in its shared
+    // memory (nb * (E + W) ints, less than the masks' smem_bytes)
+    const bool fuse = nb > 0 && nb <= kFuseScanBlocks;
     cudaError_t e;
     if (smem > 48 * 1024) {
         e = cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -306,13 +393,16 @@ cudaError_t launch_layout(const int32_t* ids, const int32_t* placement, const mo
         if (e != cudaSuccess) return e;
     }
     if (nb > 0) {
-        layout_count_kernel<<<nb, kThreads, smem, st>>>(ids, placement, s.N, s.E, s.k, s.W,
-                                                        s.dedup, blk_counts, blk_rcounts, err);
+        layout_count_kernel<<<nb, kThreads, smem, st>>>(
+            ids, placement, s.N, s.E, s.k, s.W, s.dedup, blk_counts, blk_rcounts, err, fuse ? 1 : 0,
+            done, slot_start, L);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    layout_scan_kernel<<<1, 1024, 0, st>>>(placement, nb, s.E, s.W, s.dedup, blk_counts,
-                                            blk_rcounts, slot_start, L);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (!fuse) {
+        layout_scan_kernel<<<1, 1024, 0, st>>>(placement, nb, s.E, s.W, s.dedup, blk_counts,
+                                                blk_rcounts, slot_start, L);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     if (nb > 0) {
         layout_scatter_kernel<<<nb, kThreads, smem, st>>>(ids, placement, s.N, s.E, s.k, s.W,
                                                           s.dedup, blk_counts, blk_rcounts,

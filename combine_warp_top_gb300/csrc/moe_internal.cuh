@@ -24,7 +24,8 @@ struct Workspace {
     size_t blk_counts;   // int32 [nblk][E]  per-block counts by placement slot
     size_t blk_rcounts;  // int32 [nblk][W]  per-block dedup counts by rank
     size_t slot_start;   // int32 [E+1]      first row of each slot
-    size_t mblk_prefix;  // int32 [E+2]      GEMM m-blocks before expert e; [E+1]: tile counter
+    size_t mblk_prefix;  // int32 [E+3]      [E+1]: tile counter of the CTA-pair GEMM, [E+2]: its
+                         //                  exit counter (both return to 0 after every launch)
     size_t dense;        // int32 [8]        shared expert: count, offsets, schedule
     size_t total;
 };
@@ -41,7 +42,7 @@ inline Workspace workspace_layout(const moe_shape& s) {
     w.blk_counts = o;  o = align256(o + nb * s.E * 4);
     w.blk_rcounts = o; o = align256(o + nb * s.W * 4);
     w.slot_start = o;  o = align256(o + (size_t)(s.E + 1) * 4);
-    w.mblk_prefix = o; o = align256(o + (size_t)(s.E + 2) * 4);
+    w.mblk_prefix = o; o = align256(o + (size_t)(s.E + 3) * 4);
     w.dense = o;       o = align256(o + 8 * 4);
     w.total = o;
     return w;
@@ -49,6 +50,30 @@ inline Workspace workspace_layout(const moe_shape& s) {
 
 template <typename T>
 inline T* ws_ptr(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+// prefix[e] = sum over experts e' < e of ceil(cnts[e'] / bm) (the GEMM m-blocks
+// before expert e), prefix[E] = the total; run by one whole warp over arrays in
+// shared memory (each lane scans a contiguous run of experts, then the 32 run
+// sums are scanned by shuffles).
+__device__ __forceinline__ void warp_mblk_prefix(const int* cnts, int E, int bm, int* prefix) {
+    const int lane = threadIdx.x & 31;
+    const int per = (E + 31) / 32;
+    const int e0 = lane * per, e1 = e0 + per < E ? e0 + per : E;
+    int sum = 0;
+    for (int e = e0; e < e1; ++e) sum += (cnts[e] + bm - 1) / bm;
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    int run = incl - sum;
+    for (int e = e0; e < e1; ++e) {
+        prefix[e] = run;
+        run += (cnts[e] + bm - 1) / bm;
+    }
+    if (lane == 31) prefix[E] = incl;
+}
 
 // Device-side status recording: the first error sticks.
 __device__ __forceinline__ void set_error(int* err, int code) {
@@ -79,9 +104,10 @@ cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& 
                            const uint16_t* residual, uint16_t* out, cudaStream_t st);
 
 // One grouped GEMM problem: R rows in E expert segments (device arrays
-// counts[E], offsets[E] of the segments), plus device scratch for its tile
-// schedule (prefix[0..E], and prefix[E+1] as a tile counter) and the error
-// word.
+// counts[E], offsets[E] of the segments), plus device scratch for the CTA-pair
+// kernel's tile counter (prefix[E+1]) and exit counter (prefix[E+2]), both zero
+// between launches, and the error word.  Each GEMM derives its tile schedule
+// from the counts in its own prologue.
 struct GemmGroup {
     const int32_t* counts;
     const int32_t* offsets;
@@ -132,9 +158,6 @@ moe_status placement_search(const int32_t* W, int E, int ranks, int nodes, long 
 bool map_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
 bool map_3d(CUtensorMap* m, const void* ptr, uint64_t E, uint64_t rows, uint64_t cols,
             uint32_t box_rows);
-// prefix[e] = sum over experts before e of ceil(counts / bm); prefix[E] = total.
-cudaError_t launch_schedule(const int32_t* counts, int E, int bm, int32_t* prefix,
-                            cudaStream_t st);
 
 // CTA-pair GEMMs (grouped_gemm_2sm.cu): 256-row tiles on tcgen05 cta_group::2.
 moe_status launch_gate_up_pair(const uint16_t* rows, const GemmGroup& g, int H, int I,

@@ -427,6 +427,17 @@ def moe_status_str(status: int) -> str:
     return _lib_status_str(status)
 
 
+def layout_launches(shape: Shape) -> int:
+    """Kernels moe_dispatch_layout launches for this shape: count and scatter,
+    plus a separate scan unless there are at most two count blocks of 256
+    tokens, whose last block then runs the scan (csrc/layout.cu,
+    kFuseScanBlocks)."""
+    nb = (shape.N + 255) // 256
+    if nb == 0:
+        return 1
+    return 2 if nb <= 2 else 3
+
+
 # ---- a layer with its buffers ----------------------------------------------------------
 
 class MoELayer:
@@ -570,17 +581,17 @@ class MoELayer:
             moe_ffn_gate_up(self.xd, lay, s, self.w_gate, self.w_up, self.h, self.ws, st)
 
     def kernel_launches_per_step(self) -> int:
-        """Kernels of this library launched by one forward (route 1, layout 3,
-        dispatch 1 unless fused into the gate/up GEMM, each GEMM 2 with its
-        schedule, combine 1, shared expert 5)."""
+        """Kernels of this library launched by one forward (route 1, layout 2 or
+        3, dispatch 1 unless fused into the gate/up GEMM, each GEMM 1, combine 1,
+        shared expert 3)."""
         s = self.shape
         if s.N == 0:
             return 0
-        shared = 5 if self.shared is not None else 0  # dense segment + 2 x (schedule + GEMM)
+        shared = 3 if self.shared is not None else 0  # dense segment + 2 GEMMs
         dispatch = 0 if self.fused_dispatch else 1
-        # fused combine: schedule + GEMM + finish (the accumulator memset is a copy-engine op)
-        down_combine = 3 if self.fuse_combine else 2 + 1
-        return 1 + 3 + dispatch + 2 + down_combine + shared
+        # fused combine: GEMM + finish (the accumulator memset is a copy-engine op)
+        down_combine = 2 if self.fuse_combine else 1 + 1
+        return 1 + layout_launches(s) + dispatch + 1 + down_combine + shared
 
     def forward_host(self, logits_h, x_h, residual_h, out_h, dev_inputs=None, stream=None):
         """Whole layer from host buffers: copy the step's inputs host->device,
@@ -793,6 +804,6 @@ class MicrobatchPipeline:
             s = self.shape
             sub = dataclasses.replace(s, N=t1 - t0)
             dispatch = 0 if moe_layer_skips_dispatch(sub) else 1
-            total += 1 + 3 + dispatch + 2 + 2 + 1 + (
-                5 if self.shared is not None else 0)
+            total += 1 + layout_launches(sub) + dispatch + 1 + 1 + 1 + (
+                3 if self.shared is not None else 0)
         return total
