@@ -333,7 +333,10 @@ moe_status moe_placement_search(const int32_t* coselect, int32_t E, int32_t rank
  * (held until the process exits), so shapes with moe_workspace_bytes() > 1 MiB
  * return MOE_ERR_WORKSPACE.  It allocates nothing.  Every call on a GPU shares
  * that array: calls that overlap on the GPU race.  The first call on a device
- * looks up the array's address; make it before any stream capture.
+ * looks up the array's address; make it before any stream capture.  That
+ * address is kept for the life of the process, so after cudaDeviceReset on a
+ * device this entry point must not be called on it again.  Shapes up to
+ * N = 253,440 tokens fit at E = 256, W = 8 (697,856 at E = 64, W = 32).
  * Device-detected input problems are not reported by this variant. */
 moe_status moe_dispatch_layout_noalloc(const int32_t* topk_ids, const int32_t* placement,
                                        const moe_shape* shape, const moe_layout* layout,

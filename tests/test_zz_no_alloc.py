@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from combine_warp_top_gb300 import moe, synth
 
 pytestmark = pytest.mark.gpu
@@ -17,27 +18,44 @@ def _tables(layout):
     return {n: t.cpu().numpy().copy() for n, t in layout.tensors.items()}
 
 
-def test_noalloc_layout_equals_workspace_layout_twice():
+# N = 300: two count blocks, whose last block runs the scan itself; N = 3000:
+# twelve, with the separate scan launch.  Plain and dedup; contiguous
+# placement (NULL) and the correlated workload's permutation.
+@pytest.mark.parametrize("N", [300, 3000])
+@pytest.mark.parametrize("dedup", [False, True])
+@pytest.mark.parametrize("placed", [False, True])
+def test_noalloc_layout_equals_workspace_layout_twice(N, dedup, placed):
     lib = moe.load()
     wl = synth.WORKLOADS["correlated_placed"]
-    N = 3000
-    shape = moe.Shape(N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=True)
+    shape = moe.Shape(N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=dedup)
     L = torch.from_numpy(synth.make_logits(wl, N=N)).cuda()
     ids = torch.empty(N * wl.k, dtype=torch.int32, device="cuda")
     w = torch.empty(N * wl.k, dtype=torch.float32, device="cuda")
     moe.moe_route(L, shape, ids, w)
-    placement = torch.from_numpy(synth.make_placement(wl)).cuda()
+    placement_h = synth.make_placement(wl) if placed else np.arange(wl.E, dtype=np.int32)
+    placement = torch.from_numpy(placement_h).cuda() if placed else None
 
     ref_layout, ws = moe.Layout(shape), moe.workspace(shape)
     moe.moe_dispatch_layout(ids, placement, shape, ref_layout, ws)
     torch.cuda.synchronize()
     assert moe.moe_get_error(ws) == 0
     want = _tables(ref_layout)
+    # the workspace form is itself the oracle's layout
+    ref = oracle.dispatch_layout(ids.view(N, wl.k).cpu().numpy(), placement_h, wl.E, wl.W)
+    for key in ("expert_counts", "expert_offsets", "rank_offsets", "row_token"):
+        assert np.array_equal(want[key][:len(ref[key])], ref[key]), key
+    assert np.array_equal(want["pair_row"].reshape(N, wl.k), ref["pair_row"])
+    if dedup:
+        Rd = ref["n_dedup_rows"]
+        assert int(want["n_dedup_rows"][0]) == Rd
+        assert np.array_equal(want["dedup_row_token"][:Rd], ref["dedup_row_token"])
+        assert np.array_equal(want["pair_dedup_row"].reshape(N, wl.k), ref["pair_dedup_row"])
 
     for _ in range(2):  # the static scratch keeps the previous call's contents
         got_layout = moe.Layout(shape)
         st = lib.moe_dispatch_layout_noalloc(
-            ctypes.c_void_p(ids.data_ptr()), ctypes.c_void_p(placement.data_ptr()),
+            ctypes.c_void_p(ids.data_ptr()),
+            None if placement is None else ctypes.c_void_p(placement.data_ptr()),
             ctypes.byref(shape.c()), ctypes.byref(got_layout.c),
             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
         assert st == 0, moe.moe_status_str(st)
