@@ -505,6 +505,7 @@ def measure(args, wl, world, rank, headline=True):
     n_mb = len(pipe.chunks()) if pipe is not None else 0
 
     use_graph = pipe is None and not args.eager
+    alone_ms = {}
 
     def step(i):
         if pipe is None:
@@ -568,6 +569,7 @@ def measure(args, wl, world, rank, headline=True):
             # nodes around each; gate/up keeps the timed region's figure
             full = instrumented_stage_ms(layer, L_d, x_d, r_d, stages, args.steps)
             stage_ms = {s: stage_ms.get(s, full[s]) for s in stages}
+            alone_ms = stage_alone_ms(layer, L_d, x_d, r_d, stages, args.steps)
             runner.check_device_errors()
     else:
         # gate/up launches of all microbatches of a step, on the GEMM stream
@@ -615,6 +617,13 @@ def measure(args, wl, world, rank, headline=True):
             d["bound"] = "tensor" if alg[s]["flops"] / alg[s]["bytes"] > ridge else "hbm"
         else:
             d["bound"] = "hbm"
+        if s in alone_ms:
+            a_ms = alone_ms[s]
+            d["alone_ms"] = round(a_ms, 4)
+            d["alone_hbm_frac"] = round(alg[s]["bytes"] / a_ms / 1e6 / pk["hbm_gbs"], 3)
+            if "flops" in alg[s]:
+                d["alone_tensor_frac"] = round(alg[s]["flops"] / a_ms / 1e9 /
+                                               pk["bf16_tflops_sustained"], 3)
         stage_report[s] = d
 
     roof = roofline(wl, alg, stage_ms, pk, pk_src, ridge, layer, pipe, n_mb)
@@ -789,6 +798,32 @@ def instrumented_stage_ms(layer, L_d, x_d, r_d, stages, steps):
     graph.replay()
     torch.cuda.synchronize()
     return {s: statistics.mean(e[s][0].elapsed_time(e[s][1]) for e in ev) for s in stages}
+
+
+def stage_alone_ms(layer, L_d, x_d, r_d, stages, reps):
+    """Per-launch device time of every stage run alone: a graph of `reps`
+    back-to-back launches of that stage on the layer's own buffers (no other
+    stage, no timing node between the launches), replayed once to upload it
+    and once under CUDA events.  The in-step figures carry the cost of the
+    timing nodes around each stage; these do not."""
+    import torch
+    st = torch.cuda.current_stream()
+    out = {}
+    for name in stages:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(reps):
+                layer.run_stage(name, L_d, x_d, r_d, layer.out, torch.cuda.current_stream())
+        graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        graph.replay()
+        e1.record(st)
+        torch.cuda.synchronize()
+        out[name] = e0.elapsed_time(e1) / reps
+        del graph
+    return out
 
 
 def run_reference(args):

@@ -525,46 +525,40 @@ class MoELayer:
         they are recorded around each stage on the stream."""
         out = self.out if out is None else out
         st = torch.cuda.current_stream() if stream is None else stream
-        s = self.shape
-
-        def rec(name, i):
+        for name in self.stage_names():
             if events is not None and name in events:
-                events[name][i].record(st)
+                events[name][0].record(st)
+            self.run_stage(name, logits, x, residual, out, st)
+            if events is not None and name in events:
+                events[name][1].record(st)
+        return out
 
-        rec("route", 0)
-        moe_route(logits, s, self.topk_ids, self.topk_w, st)
-        rec("route", 1)
-        rec("layout", 0)
-        moe_dispatch_layout(self.topk_ids, self.placement, s, self.layout, self.ws, st)
-        rec("layout", 1)
-        if not self.fused_dispatch:
-            rec("dispatch", 0)
+    def run_stage(self, name, logits, x, residual, out, st):
+        """One stage of forward_stages() on this layer's buffers (one C call)."""
+        s = self.shape
+        if name == "route":
+            moe_route(logits, s, self.topk_ids, self.topk_w, st)
+        elif name == "layout":
+            moe_dispatch_layout(self.topk_ids, self.placement, s, self.layout, self.ws, st)
+        elif name == "dispatch":
             moe_dispatch(x, self.layout, s, self.xd, st)
-            rec("dispatch", 1)
-        rec("gate_up", 0)
-        self._gate_up(x, st)
-        rec("gate_up", 1)
-        if self.fuse_combine:
-            rec("down_combine", 0)
+        elif name == "gate_up":
+            self._gate_up(x, st)
+        elif name == "down_combine":
             moe_ffn_down_combine(self.h, self.topk_w, self.layout, s, self.w_down, residual,
                                  self.acc, out, self.ws, st)
-            rec("down_combine", 1)
-            return out
-        rec("down", 0)
-        moe_ffn_down(self.h, self.layout, s, self.w_down, self.y, self.ws, st)
-        rec("down", 1)
-        if self.shared is not None:
-            rec("shared", 0)
+        elif name == "down":
+            moe_ffn_down(self.h, self.layout, s, self.w_down, self.y, self.ws, st)
+        elif name == "shared":
             moe_shared_expert_ffn(x, s, self.I_shared, *self.shared, self.h_s, self.y_s, self.ws, st)
-            rec("shared", 1)
-        rec("combine", 0)
-        if self.shared is not None:
-            moe_combine_shared(self.y, self.topk_w, self.layout, s, self.partial, self.y_s,
-                               residual, out, st)
+        elif name == "combine":
+            if self.shared is not None:
+                moe_combine_shared(self.y, self.topk_w, self.layout, s, self.partial, self.y_s,
+                                   residual, out, st)
+            else:
+                moe_combine(self.y, self.topk_w, self.layout, s, self.partial, residual, out, st)
         else:
-            moe_combine(self.y, self.topk_w, self.layout, s, self.partial, residual, out, st)
-        rec("combine", 1)
-        return out
+            raise ValueError(f"unknown stage {name}")
 
     def _gate_up(self, x, st):
         """The gate/up stage as moe_layer_forward runs it: dedup rows expanded
