@@ -107,3 +107,26 @@ def test_oracle_worker_dedup_combine_sample():
     r = bench.run_oracle(["--workload", "correlated_placed", "--tokens", "300"], threads=1,
                          steps=1, experts_per_step=1)
     assert r["steps"][0]["tokens"] == 300 and r["n_sub"] == 300
+
+
+def test_reference_arm_prints_its_contract_line():
+    """bench.py --impl reference: the oracle timed on the host cores, one JSON
+    line with the same metric and workload keys as the repo's arm, marked as
+    the reference, with its cpu_baseline and zero-copy e2e."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--workload", "tiny", "--steps", "2", "--warmup", "1"],
+                         capture_output=True, text=True, cwd=root, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [line for line in out.stdout.splitlines() if line.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
+    assert d["steps"] == 2 and d["warmup"] == 1 and d["value"] > 0
+    assert d["config"]["workload"] == "tiny" and d["higher_is_better"] is True
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0

@@ -54,6 +54,10 @@ def test_bench_json_contract(extra):
                     "dispatch_rows", "gpu_launches", "clocks"):
             assert key in o, key
         assert o["value"] > 0 and o["roofline"]["frac"] > 0
+    # every stage is also timed alone (graph mode only)
+    if "--eager" not in extra:
+        for name, st in d["stages"].items():
+            assert st["alone_ms"] > 0 and st["alone_hbm_frac"] >= 0, name
     rows = d["dispatch_rows"]
     for key in ("plain", "dedup", "dedup_reduction", "ranks_per_token", "same_rank_share",
                 "max_over_mean_expert_load"):
