@@ -26,7 +26,7 @@ struct Workspace {
     size_t slot_start;   // int32 [E+1]      first row of each slot
     size_t mblk_prefix;  // int32 [E+3]      [E+1]: tile counter of the CTA-pair GEMM, [E+2]: its
                          //                  exit counter (both return to 0 after every launch)
-    size_t dense;        // int32 [8]        shared expert: count, offsets, schedule
+    size_t dense;        // int32 [8]        shared expert: count, offsets, tile counters
     size_t total;
 };
 
@@ -153,8 +153,8 @@ cudaError_t launch_coselection(const int32_t* ids, const moe_shape& s, int32_t* 
 moe_status placement_search(const int32_t* W, int E, int ranks, int nodes, long long max_swaps,
                             int32_t* placement, long long* swaps_made);
 
-// Tensor maps (bf16, 128-byte swizzle, zero fill) and the GEMM tile schedule
-// (grouped_gemm.cu), shared by the single-CTA and the CTA-pair GEMMs.
+// Tensor maps (bf16, 128-byte swizzle, zero fill; grouped_gemm.cu), shared by
+// the single-CTA and the CTA-pair GEMMs.
 bool map_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
 bool map_3d(CUtensorMap* m, const void* ptr, uint64_t E, uint64_t rows, uint64_t cols,
             uint32_t box_rows);

@@ -111,7 +111,8 @@ typedef struct {
 } moe_layout;
 
 /* Bytes of device workspace that the calls taking `ws` need for this shape
- * (error word, per-block counts, tile schedule).  0 if the shape is invalid.
+ * (error word, per-block counts, the CTA-pair GEMM's tile counters).  0 if the
+ * shape is invalid.
  * The caller zero-fills the workspace once after allocating it (the first
  * int32 is the error word); the calls keep it valid afterwards.  One workspace
  * must not be shared by calls running concurrently. */
@@ -193,7 +194,8 @@ moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const mo
  * moe_ffn_gate_up: h = bf16(SiLU(rows Wg[e]^T) * (rows Wu[e]^T)) for the
  *                  expert-major rows [N*k, H] (xd when plain, xe when dedup).
  * moe_ffn_down:    y = bf16(h Wd[e]^T).
- * Both GEMM calls take the workspace (they write their tile schedule there). */
+ * Both GEMM calls take the workspace (the CTA-pair kernel keeps its tile
+ * counters there; they return to zero after every launch). */
 moe_status moe_expand(const uint16_t* xd, const moe_layout* layout, const moe_shape* shape,
                       uint16_t* xe, void* stream);
 moe_status moe_ffn_gate_up(const uint16_t* rows, const moe_layout* layout, const moe_shape* shape,
@@ -263,7 +265,7 @@ moe_status moe_combine(const uint16_t* y, const float* topk_w, const moe_layout*
  *   y_s = bf16(h_s Wd_s^T)                    bf16 [N, H]
  * w_gate_s, w_up_s bf16 [I_shared, H]; w_down_s bf16 [H, I_shared];
  * I_shared % 8 == 0.  ws: the layer's workspace (a reserved corner holds this
- * call's schedule). */
+ * call's tile counters). */
 moe_status moe_shared_expert_ffn(const uint16_t* x, const moe_shape* shape, int32_t I_shared,
                                  const uint16_t* w_gate_s, const uint16_t* w_up_s,
                                  const uint16_t* w_down_s, uint16_t* h_s, uint16_t* y_s, void* ws,
