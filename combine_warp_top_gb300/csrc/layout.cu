@@ -8,33 +8,35 @@
 // expert IDs) and Appendix A-A2 (the receiver expands rows to expert-major
 // order).
 //
-// Two launches for small N, three otherwise, all deterministic:
+// Two launches (three when the count tables exceed kScanTableBytes), all
+// deterministic:
 //  1. count:   per block of 256 tokens, one 32-bit mask per (warp, slot) and
 //              per (warp, rank) records which lanes (tokens) hit it; the block
 //              count of a key is the sum of the popcounts.  OR-ing the rank
 //              bits merges a token's experts on one rank for free, which is the
 //              deduplication.
-//     scan:    the per-block counts become exclusive bases (blocks in token
-//              order) and the totals become slot/rank offsets.  With at most
-//              kFuseScanBlocks count blocks the last count block to finish
-//              does this (a completion counter in the workspace tells it that
-//              it is last; nothing waits), on a copy of the table in its shared
-//              memory; otherwise a separate one-block launch of 1024 threads
-//              does it (measured faster from 16 count blocks on: the one block
-//              of the fused form walks the table in a longer dependent chain
-//              than the launch it saves).
-//  2. scatter: each block rebuilds its masks; a pair's row is its warp's base
-//              plus the popcount of the lower lanes' bits, so tokens ascend
-//              inside every segment exactly as in a stable sort.
+//  2. scatter: each block rebuilds its masks and derives its own bases: it
+//              copies the whole per-block count table into shared memory, sums
+//              every column (the slot and rank totals, scanned into the slot
+//              and rank offsets) and the part of it above its own row (the
+//              blocks before it in token order).  Block 0 also writes the
+//              layout's count and offset tables.  A pair's row is its warp's
+//              base plus the popcount of the lower lanes' bits, so tokens
+//              ascend inside every segment exactly as in a stable sort.
+//     With larger tables a one-block scan launch between the two turns the
+//     table into bases once, and the scatter blocks read theirs.
 #include "moe_internal.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kThreads = 32 * kLayoutWarps;
-// Count blocks up to which the last count block runs the scan itself (their
-// tables always fit in the count kernel's shared memory).
-constexpr int kFuseScanBlocks = 2;
+// Largest per-block count table ([nb][E] + [nb][W] int32) that every scatter
+// block scans for itself in its shared memory.  Measured against the separate
+// scan launch: 2 us faster with one count block (N = 64), even at 16 KB (16
+// blocks, E = 256), 1 to 11 us slower at 24 to 64 KB (64 to 128 blocks), where
+// each block's walk down the columns outweighs the launch.
+constexpr size_t kScanTableBytes = 16 * 1024;
 
 // slot_of[e] = the placement slot holding expert e.  Invalid placements are
 // reported and resolved deterministically (lowest slot wins, unplaced experts
@@ -263,17 +265,11 @@ __global__ void __launch_bounds__(1024) layout_scan_kernel(
     scan_counts(placement, nb, E, W, dedup, blk_counts, blk_rcounts, slot_start, L, ss);
 }
 
-// Count pass; with fuse_scan the last block to finish also runs the scan, on
-// a copy of the count tables in its (then free) dynamic shared memory.
-// done: completion counter, zero before the launch and reset to zero by the
-// last block.
 __global__ void __launch_bounds__(kThreads) layout_count_kernel(
     const int32_t* __restrict__ ids, const int32_t* __restrict__ placement, int N, int E, int k,
     int W, int dedup, int32_t* __restrict__ blk_counts, int32_t* __restrict__ blk_rcounts,
-    int* err, int fuse_scan, int* done, int32_t* __restrict__ slot_start, moe_layout L) {
+    int* err) {
     extern __shared__ uint32_t sm[];
-    __shared__ ScanSmem ss;
-    __shared__ int is_last;
     const Smem s = carve(sm, E, W);
     build_slot_of(s.slot_of, placement, E, err);
     build_masks(s, ids, N, E, k, W, dedup, err);
@@ -291,49 +287,103 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(
             blk_rcounts[(size_t)blockIdx.x * W + r] = c;
         }
     }
-    if (!fuse_scan) return;
-    // publish this block's counts, then learn whether it is the last one
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) is_last = atomicAdd(done, 1) == (int)gridDim.x - 1;
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    const int nb = gridDim.x;
-    int32_t* tab = reinterpret_cast<int32_t*>(sm);  // the masks are no longer needed
-    int32_t* rtab = tab + (size_t)nb * E;
-    for (size_t i = threadIdx.x; i < (size_t)nb * E; i += blockDim.x) tab[i] = blk_counts[i];
-    if (dedup)
-        for (size_t i = threadIdx.x; i < (size_t)nb * W; i += blockDim.x) rtab[i] = blk_rcounts[i];
-    __syncthreads();
-    scan_counts(placement, nb, E, W, dedup, tab, rtab, slot_start, L, ss);
-    __syncthreads();
-    for (size_t i = threadIdx.x; i < (size_t)nb * E; i += blockDim.x) blk_counts[i] = tab[i];
-    if (dedup)
-        for (size_t i = threadIdx.x; i < (size_t)nb * W; i += blockDim.x) blk_rcounts[i] = rtab[i];
-    if (threadIdx.x == 0) atomicExch(done, 0);
 }
 
+// Scatter-side scan of one [nb][ncol] count table held in shared memory:
+// col_base[c] = first row of this block's part of column c (the column
+// offset plus the counts of the blocks before this one); totals[c] and
+// starts[c] = the column sums and their exclusive scan.
+__device__ void block_bases(const int32_t* tab, int nb, int ncol, int* col_base, ScanSmem& ss) {
+    for (int c = threadIdx.x; c < ncol; c += blockDim.x) {
+        int tot = 0, before = 0;
+        for (int b = 0; b < nb; ++b) {
+            const int v = tab[(size_t)b * ncol + c];
+            if (b < (int)blockIdx.x) before += v;
+            tot += v;
+        }
+        ss.totals[c] = tot;
+        col_base[c] = before;
+    }
+    __syncthreads();
+    block_scan_values(ss.totals, ncol, ss.starts, ss.warp_sums, &ss.total);
+    for (int c = threadIdx.x; c < ncol; c += blockDim.x) col_base[c] += ss.starts[c];
+    __syncthreads();
+}
+
+// scan_here: derive this block's bases from the whole count table (copied
+// into shared memory after the masks) instead of reading the bases that a
+// separate scan launch wrote.
 __global__ void __launch_bounds__(kThreads) layout_scatter_kernel(
     const int32_t* __restrict__ ids, const int32_t* __restrict__ placement, int N, int E, int k,
     int W, int dedup, const int32_t* __restrict__ blk_counts,
     const int32_t* __restrict__ blk_rcounts, const int32_t* __restrict__ slot_start, moe_layout L,
-    int* err) {
+    int scan_here) {
     extern __shared__ uint32_t sm[];
+    __shared__ ScanSmem ss;
     const Smem s = carve(sm, E, W);
     build_slot_of(s.slot_of, placement, E, nullptr);  // errors were reported by the count pass
     build_masks(s, ids, N, E, k, W, dedup, nullptr);
+    int* col_base = ss.part_sums;  // first row of this block's part of each slot / rank
+    const int per_rank = E / W;
+    if (scan_here) {
+        const int nb = gridDim.x;
+        int32_t* tab = reinterpret_cast<int32_t*>(s.rbase + kLayoutWarps * W);
+        int32_t* rtab = tab + (size_t)nb * E;
+        for (size_t i = threadIdx.x; i < (size_t)nb * E; i += blockDim.x) tab[i] = blk_counts[i];
+        if (dedup)
+            for (size_t i = threadIdx.x; i < (size_t)nb * W; i += blockDim.x)
+                rtab[i] = blk_rcounts[i];
+        __syncthreads();
+        block_bases(tab, nb, E, col_base, ss);
+        if (blockIdx.x == 0) {
+            for (int p = threadIdx.x; p < E; p += blockDim.x) {
+                int e = placement ? placement[p] : p;
+                if (e < 0 || e >= E) e = 0;  // reported by the count kernel
+                L.expert_counts[e] = ss.totals[p];
+                L.expert_offsets[e] = ss.starts[p];
+                if (p % per_rank == 0) L.rank_offsets[p / per_rank] = ss.starts[p];
+            }
+            if (threadIdx.x == 0) {
+                L.expert_offsets[E] = ss.total;
+                L.rank_offsets[W] = ss.total;
+            }
+        }
+    } else {
+        for (int p = threadIdx.x; p < E; p += blockDim.x)
+            col_base[p] = slot_start[p] + blk_counts[(size_t)blockIdx.x * E + p];
+        __syncthreads();
+    }
     for (int p = threadIdx.x; p < E; p += blockDim.x) {
-        int run = slot_start[p] + blk_counts[(size_t)blockIdx.x * E + p];
+        int run = col_base[p];
 #pragma unroll
         for (int w = 0; w < kLayoutWarps; ++w) {
             s.base[w * E + p] = run;
             run += __popc(s.mask[w * E + p]);
         }
     }
+    __syncthreads();
     if (dedup) {
+        if (scan_here) {
+            const int32_t* rtab = reinterpret_cast<const int32_t*>(s.rbase + kLayoutWarps * W) +
+                                  (size_t)gridDim.x * E;
+            block_bases(rtab, gridDim.x, W, col_base, ss);
+            if (blockIdx.x == 0) {
+                for (int r = threadIdx.x; r < W; r += blockDim.x) {
+                    L.dedup_counts[r] = ss.totals[r];
+                    L.dedup_offsets[r] = ss.starts[r];
+                }
+                if (threadIdx.x == 0) {
+                    L.dedup_offsets[W] = ss.total;
+                    *L.n_dedup_rows = ss.total;
+                }
+            }
+        } else {
+            for (int r = threadIdx.x; r < W; r += blockDim.x)
+                col_base[r] = L.dedup_offsets[r] + blk_rcounts[(size_t)blockIdx.x * W + r];
+            __syncthreads();
+        }
         for (int r = threadIdx.x; r < W; r += blockDim.x) {
-            int run = L.dedup_offsets[r] + blk_rcounts[(size_t)blockIdx.x * W + r];
+            int run = col_base[r];
 #pragma unroll
             for (int w = 0; w < kLayoutWarps; ++w) {
                 s.rbase[w * W + r] = run;
@@ -346,7 +396,6 @@ __global__ void __launch_bounds__(kThreads) layout_scatter_kernel(
     const int t = blockIdx.x * kLayoutTokens + threadIdx.x;
     if (t >= N) return;
     const uint32_t lower = (1u << lane) - 1u;
-    const int per_rank = E / W;
     for (int j = 0; j < k; ++j) {
         int e = ids[(size_t)t * k + j];
         if (e < 0 || e >= E) e = 0;
@@ -377,36 +426,37 @@ cudaError_t launch_layout(const int32_t* ids, const int32_t* placement, const mo
     int32_t* blk_counts = ws_ptr<int32_t>(ws, wl.blk_counts);
     int32_t* blk_rcounts = ws_ptr<int32_t>(ws, wl.blk_rcounts);
     int32_t* slot_start = ws_ptr<int32_t>(ws, wl.slot_start);
-    int* done = ws_ptr<int>(ws, wl.err) + 1;  // completion counter of the count pass
     const int nb = layout_blocks(s.N);
     const size_t smem = smem_bytes(s.E, s.W);
-    // few count blocks: the last one scans the count tables in its shared
-    // memory (nb * (E + W) ints, less than the masks' smem_bytes)
-    const bool fuse = nb > 0 && nb <= kFuseScanBlocks;
+    // the scatter blocks scan the count tables themselves when they are small
+    const size_t table = (size_t)nb * (s.E + (s.dedup ? s.W : 0)) * sizeof(int32_t);
+    const bool scan_here = nb > 0 && table <= kScanTableBytes;
+    const size_t scatter_smem = smem + (scan_here ? table : 0);
     cudaError_t e;
     if (smem > 48 * 1024) {
         e = cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
+    }
+    if (scatter_smem > 48 * 1024) {
         e = cudaFuncSetAttribute(layout_scatter_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scatter_smem);
         if (e != cudaSuccess) return e;
     }
     if (nb > 0) {
-        layout_count_kernel<<<nb, kThreads, smem, st>>>(
-            ids, placement, s.N, s.E, s.k, s.W, s.dedup, blk_counts, blk_rcounts, err, fuse ? 1 : 0,
-            done, slot_start, L);
+        layout_count_kernel<<<nb, kThreads, smem, st>>>(ids, placement, s.N, s.E, s.k, s.W,
+                                                        s.dedup, blk_counts, blk_rcounts, err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    if (!fuse) {
+    if (!scan_here) {
         layout_scan_kernel<<<1, 1024, 0, st>>>(placement, nb, s.E, s.W, s.dedup, blk_counts,
                                                 blk_rcounts, slot_start, L);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (nb > 0) {
-        layout_scatter_kernel<<<nb, kThreads, smem, st>>>(ids, placement, s.N, s.E, s.k, s.W,
-                                                          s.dedup, blk_counts, blk_rcounts,
-                                                          slot_start, L, err);
+        layout_scatter_kernel<<<nb, kThreads, scatter_smem, st>>>(
+            ids, placement, s.N, s.E, s.k, s.W, s.dedup, blk_counts, blk_rcounts, slot_start, L,
+            scan_here ? 1 : 0);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

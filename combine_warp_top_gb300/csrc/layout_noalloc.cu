@@ -21,9 +21,6 @@
 //    that first call before any stream capture.  The address is kept for the
 //    life of the process: after cudaDeviceReset on a device it no longer names
 //    the array, so do not call this entry point on that device again.
-//  - Besides the error word, the array holds the layout's completion counter
-//    (used when a shape has at most two blocks of 256 tokens); it starts at
-//    zero (static storage) and every call leaves it at zero.
 //  - The error word at the start of the array is cleared at the start of every
 //    call.  Device-detected input problems (ids out of range, a placement that
 //    is not a permutation) are recorded there but not reported to the caller,

@@ -429,13 +429,15 @@ def moe_status_str(status: int) -> str:
 
 def layout_launches(shape: Shape) -> int:
     """Kernels moe_dispatch_layout launches for this shape: count and scatter,
-    plus a separate scan unless there are at most two count blocks of 256
-    tokens, whose last block then runs the scan (csrc/layout.cu,
-    kFuseScanBlocks)."""
+    plus a separate scan when the per-block count tables (one int32 per block
+    of 256 tokens and slot, and per block and rank with dedup) exceed the
+    16 KB that each scatter block scans itself (csrc/layout.cu,
+    kScanTableBytes)."""
     nb = (shape.N + 255) // 256
     if nb == 0:
         return 1
-    return 2 if nb <= 2 else 3
+    table = nb * (shape.E + (shape.W if shape.dedup else 0)) * 4
+    return 2 if table <= 16 * 1024 else 3
 
 
 # ---- a layer with its buffers ----------------------------------------------------------
