@@ -581,10 +581,12 @@ def measure(args, wl, world, rank, headline=True):
         # end to end through the public host-buffer API: every step copies its
         # inputs from pinned host memory and its output back, overlapped with
         # the neighbouring steps' compute (moe.HostPipeline)
-        e2e_steps = args.e2e_steps or max(3, min(args.steps, 50))
+        # 50 steps by default whatever K is: a few hundred ms of host-link
+        # traffic, long enough that the host's scheduling jitter averages out
+        e2e_steps = args.e2e_steps or 50
         host = moe.HostPipeline(runner, with_residual=True)
         batches = [(L_h, x_h, r_h, out_h)] * e2e_steps
-        host.run(batches[:2])
+        host.run(batches[:4])
         torch.cuda.synchronize()
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
