@@ -109,7 +109,6 @@ __device__ void build_masks(const Smem& s, const int32_t* __restrict__ ids, int 
     __syncthreads();
 }
 
-
 // Exclusive scan of one value per thread over a block of up to 1024 threads.
 __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -139,8 +138,8 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
     return r;
 }
 
-// Exclusive scan of n values (n up to 4 * blockDim): each thread takes a run
-// of consecutive values.  out[i] = sum of in[0..i); *total = the sum.
+// Exclusive scan of n values by the whole block: each thread takes a run of
+// consecutive values.  out[i] = sum of in[0..i); *total = the sum.
 __device__ void block_scan_values(const int* in, int n, int* out, int* warp_sums, int* total) {
     const int per = (n + blockDim.x - 1) / blockDim.x;
     const int i0 = threadIdx.x * per, i1 = min(n, i0 + per);
@@ -155,28 +154,14 @@ __device__ void block_scan_values(const int* in, int n, int* out, int* warp_sums
     __syncthreads();
 }
 
-// Exclusive scan down every column of a [nb][ncol] table, in place, by the
-// whole block (global or shared memory).  With ncol <= blockDim the rows of a
-// column are split into P = blockDim / ncol parts: each thread sums its part
-// (independent loads), the parts of a column are scanned through part_sums,
-// and each thread rewrites its rows with the running prefix; with more
-// columns than threads each thread walks whole columns.  totals[c] receives
-// the column sum.  part_sums holds blockDim ints.
+// Exclusive scan down every column of a [nb][ncol] table in global memory, in
+// place, by the whole block (ncol <= blockDim): the rows of a column are split
+// into P = blockDim / ncol parts; each thread sums its part (independent
+// loads), the parts of a column are scanned through part_sums, and each
+// thread rewrites its rows with the running prefix.  totals[c] receives the
+// column sum.  part_sums holds blockDim ints.
 __device__ void columns_scan(int32_t* __restrict__ tab, int nb, int ncol, int* part_sums,
                              int* totals) {
-    if (ncol > (int)blockDim.x) {
-        for (int c = threadIdx.x; c < ncol; c += blockDim.x) {
-            int run = 0;
-            for (int b = 0; b < nb; ++b) {
-                const int v = tab[(size_t)b * ncol + c];
-                tab[(size_t)b * ncol + c] = run;
-                run += v;
-            }
-            totals[c] = run;
-        }
-        __syncthreads();
-        return;
-    }
     const int P = blockDim.x / ncol;
     const int c = threadIdx.x % ncol, part = threadIdx.x / ncol;
     const int L = (nb + P - 1) / P;
@@ -219,7 +204,7 @@ struct ScanSmem {
 // The scan proper: per-block counts -> exclusive bases in place; column totals
 // -> slot and rank offsets, the layout's counts and offsets, and (dedup) the
 // dedup row counts and offsets.  tab / rtab: [nb][E] / [nb][W] tables in
-// global or shared memory.  Any block size; every thread of the block calls it.
+// global memory; every thread of a block of at least E threads calls it.
 __device__ void scan_counts(const int32_t* __restrict__ placement, int nb, int E, int W,
                             int dedup, int32_t* tab, int32_t* rtab,
                             int32_t* __restrict__ slot_start, const moe_layout& L, ScanSmem& ss) {
