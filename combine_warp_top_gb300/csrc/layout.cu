@@ -26,6 +26,7 @@
 //     With larger tables a one-block scan launch between the two turns the
 //     table into bases once, and the scatter blocks read theirs.
 #include "moe_internal.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -33,10 +34,10 @@ namespace {
 constexpr int kThreads = 32 * kLayoutWarps;
 // Largest per-block count table ([nb][E] + [nb][W] int32) that every scatter
 // block scans for itself in its shared memory.  Measured against the separate
-// scan launch: 2 us faster with one count block (N = 64), even at 16 KB (16
-// blocks, E = 256), 1 to 11 us slower at 24 to 64 KB (64 to 128 blocks), where
-// each block's walk down the columns outweighs the launch.
-constexpr size_t kScanTableBytes = 16 * 1024;
+// scan launch: 2 to 4.5 us faster at 32 bytes to 64 KB (1 to 128 count blocks,
+// the tables copied by cp.async while the masks are built, tall columns summed
+// in parts).
+constexpr size_t kScanTableBytes = 64 * 1024;
 
 // slot_of[e] = the placement slot holding expert e.  Invalid placements are
 // reported and resolved deterministically (lowest slot wins, unplaced experts
@@ -71,6 +72,18 @@ struct Smem {
     int* rbase;       // [kLayoutWarps][W]
 };
 
+// Word offset of the scatter kernel's copy of the count tables in its dynamic
+// shared memory: after the Smem arrays, rounded up to 16 bytes.
+__host__ __device__ inline size_t table_offset_words(int E, int W) {
+    return ((size_t)E + 2 * (size_t)kLayoutWarps * (E + W) + 3) & ~(size_t)3;
+}
+// Words that a [nb][ncol] table takes there: it is copied in whole 16-byte
+// pieces, so nb * ncol rounded up to 4.  The [nb][E] slot table comes first,
+// the [nb][W] rank table right after it.
+__host__ __device__ inline size_t padded_table_words(int nb, int ncol) {
+    return ((size_t)nb * ncol + 3) & ~(size_t)3;
+}
+
 __device__ Smem carve(uint32_t* sm, int E, int W) {
     Smem s;
     s.slot_of = reinterpret_cast<int*>(sm);
@@ -81,10 +94,20 @@ __device__ Smem carve(uint32_t* sm, int E, int W) {
     return s;
 }
 
-// Fill this block's lane masks.  Returns nothing; masks are valid after the
-// trailing __syncthreads.
-__device__ void build_masks(const Smem& s, const int32_t* __restrict__ ids, int N, int E, int k,
-                            int W, int dedup, int* err) {
+// This thread's token's k expert ids, all loads issued at once (one memory
+// round trip instead of k); entries j >= k and tokens past N are 0.
+__device__ __forceinline__ void load_token_ids(int (&ids_t)[kMaxK],
+                                               const int32_t* __restrict__ ids, int N, int k) {
+    const int t = blockIdx.x * kLayoutTokens + threadIdx.x;
+    const int32_t* row = ids + (size_t)t * k;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) ids_t[j] = (t < N && j < k) ? __ldg(row + j) : 0;
+}
+
+// Fill this block's lane masks from the token ids in ids_t.  Masks are valid
+// after the trailing __syncthreads.
+__device__ void build_masks(const Smem& s, const int (&ids_t)[kMaxK], int N, int E, int k, int W,
+                            int dedup, int* err) {
     for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x) s.mask[i] = 0;
     if (dedup)
         for (int i = threadIdx.x; i < kLayoutWarps * W; i += blockDim.x) s.rmask[i] = 0;
@@ -94,8 +117,10 @@ __device__ void build_masks(const Smem& s, const int32_t* __restrict__ ids, int 
     const int per_rank = E / W;
     if (t < N) {
         const uint32_t bit = 1u << lane;
-        for (int j = 0; j < k; ++j) {
-            int e = ids[(size_t)t * k + j];
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            if (j >= k) break;
+            int e = ids_t[j];
             if (e < 0 || e >= E) {
                 set_error(err, MOE_ERR_INVALID_ARG);
                 e = 0;
@@ -256,8 +281,10 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(
     int* err) {
     extern __shared__ uint32_t sm[];
     const Smem s = carve(sm, E, W);
+    int ids_t[kMaxK];
+    load_token_ids(ids_t, ids, N, k);
     build_slot_of(s.slot_of, placement, E, err);
-    build_masks(s, ids, N, E, k, W, dedup, err);
+    build_masks(s, ids_t, N, E, k, W, dedup, err);
     for (int p = threadIdx.x; p < E; p += blockDim.x) {
         int c = 0;
 #pragma unroll
@@ -278,16 +305,48 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(
 // col_base[c] = first row of this block's part of column c (the column
 // offset plus the counts of the blocks before this one); totals[c] and
 // starts[c] = the column sums and their exclusive scan.
+// Tall tables split the rows of a column into P parts of at least 8 rows,
+// summed by different threads (P <= blockDim / ncol; the part sums wait in
+// ss.starts until the scan overwrites it); otherwise a thread walks a whole
+// column.
 __device__ void block_bases(const int32_t* tab, int nb, int ncol, int* col_base, ScanSmem& ss) {
-    for (int c = threadIdx.x; c < ncol; c += blockDim.x) {
-        int tot = 0, before = 0;
-        for (int b = 0; b < nb; ++b) {
-            const int v = tab[(size_t)b * ncol + c];
-            if (b < (int)blockIdx.x) before += v;
-            tot += v;
+    const int P = min((int)blockDim.x / ncol, nb / 8);
+    if (P > 1) {
+        const int c = threadIdx.x % ncol, part = threadIdx.x / ncol;
+        const int L = (nb + P - 1) / P, b0 = part * L, b1 = min(nb, b0 + L);
+        int* psum = ss.starts;             // [P][ncol]
+        int* pbefore = ss.starts + P * ncol;  // [P][ncol]
+        if (part < P) {
+            int tot = 0, before = 0;
+            for (int b = b0; b < b1; ++b) {
+                const int v = tab[(size_t)b * ncol + c];
+                if (b < (int)blockIdx.x) before += v;
+                tot += v;
+            }
+            psum[part * ncol + c] = tot;
+            pbefore[part * ncol + c] = before;
         }
-        ss.totals[c] = tot;
-        col_base[c] = before;
+        __syncthreads();
+        if (threadIdx.x < ncol) {
+            int tot = 0, before = 0;
+            for (int q = 0; q < P; ++q) {
+                tot += psum[q * ncol + threadIdx.x];
+                before += pbefore[q * ncol + threadIdx.x];
+            }
+            ss.totals[threadIdx.x] = tot;
+            col_base[threadIdx.x] = before;
+        }
+    } else {
+        for (int c = threadIdx.x; c < ncol; c += blockDim.x) {
+            int tot = 0, before = 0;
+            for (int b = 0; b < nb; ++b) {
+                const int v = tab[(size_t)b * ncol + c];
+                if (b < (int)blockIdx.x) before += v;
+                tot += v;
+            }
+            ss.totals[c] = tot;
+            col_base[c] = before;
+        }
     }
     __syncthreads();
     block_scan_values(ss.totals, ncol, ss.starts, ss.warp_sums, &ss.total);
@@ -306,18 +365,28 @@ __global__ void __launch_bounds__(kThreads) layout_scatter_kernel(
     extern __shared__ uint32_t sm[];
     __shared__ ScanSmem ss;
     const Smem s = carve(sm, E, W);
+    // every global load of the prologue in flight at once: the token ids (to
+    // registers) and, with scan_here, the count tables (16-byte asynchronous
+    // copies to shared memory, waited for after the masks are built)
+    int ids_t[kMaxK];
+    load_token_ids(ids_t, ids, N, k);
+    const int nb = gridDim.x;
+    int32_t* tab = reinterpret_cast<int32_t*>(sm + table_offset_words(E, W));  // [nb][E]
+    int32_t* rtab = tab + padded_table_words(nb, E);                            // [nb][W]
+    if (scan_here) {
+        const int nE = nb * E, nW = dedup ? nb * W : 0;
+        const uint32_t t0 = ptx::smem_u32(tab), r0 = ptx::smem_u32(rtab);
+        for (int i = threadIdx.x; 4 * i < nE; i += blockDim.x)
+            ptx::cp_async_16(t0 + 16u * i, blk_counts + 4 * i, 4u * min(4, nE - 4 * i));
+        for (int i = threadIdx.x; 4 * i < nW; i += blockDim.x)
+            ptx::cp_async_16(r0 + 16u * i, blk_rcounts + 4 * i, 4u * min(4, nW - 4 * i));
+    }
     build_slot_of(s.slot_of, placement, E, nullptr);  // errors were reported by the count pass
-    build_masks(s, ids, N, E, k, W, dedup, nullptr);
+    build_masks(s, ids_t, N, E, k, W, dedup, nullptr);
     int* col_base = ss.part_sums;  // first row of this block's part of each slot / rank
     const int per_rank = E / W;
     if (scan_here) {
-        const int nb = gridDim.x;
-        int32_t* tab = reinterpret_cast<int32_t*>(s.rbase + kLayoutWarps * W);
-        int32_t* rtab = tab + (size_t)nb * E;
-        for (size_t i = threadIdx.x; i < (size_t)nb * E; i += blockDim.x) tab[i] = blk_counts[i];
-        if (dedup)
-            for (size_t i = threadIdx.x; i < (size_t)nb * W; i += blockDim.x)
-                rtab[i] = blk_rcounts[i];
+        ptx::cp_async_wait_all();
         __syncthreads();
         block_bases(tab, nb, E, col_base, ss);
         if (blockIdx.x == 0) {
@@ -349,9 +418,7 @@ __global__ void __launch_bounds__(kThreads) layout_scatter_kernel(
     __syncthreads();
     if (dedup) {
         if (scan_here) {
-            const int32_t* rtab = reinterpret_cast<const int32_t*>(s.rbase + kLayoutWarps * W) +
-                                  (size_t)gridDim.x * E;
-            block_bases(rtab, gridDim.x, W, col_base, ss);
+            block_bases(rtab, nb, W, col_base, ss);
             if (blockIdx.x == 0) {
                 for (int r = threadIdx.x; r < W; r += blockDim.x) {
                     L.dedup_counts[r] = ss.totals[r];
@@ -381,8 +448,10 @@ __global__ void __launch_bounds__(kThreads) layout_scatter_kernel(
     const int t = blockIdx.x * kLayoutTokens + threadIdx.x;
     if (t >= N) return;
     const uint32_t lower = (1u << lane) - 1u;
-    for (int j = 0; j < k; ++j) {
-        int e = ids[(size_t)t * k + j];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+        if (j >= k) break;
+        int e = ids_t[j];
         if (e < 0 || e >= E) e = 0;
         const int p = s.slot_of[e];
         const int row = s.base[warp * E + p] + __popc(s.mask[warp * E + p] & lower);
@@ -414,9 +483,15 @@ cudaError_t launch_layout(const int32_t* ids, const int32_t* placement, const mo
     const int nb = layout_blocks(s.N);
     const size_t smem = smem_bytes(s.E, s.W);
     // the scatter blocks scan the count tables themselves when they are small
-    const size_t table = (size_t)nb * (s.E + (s.dedup ? s.W : 0)) * sizeof(int32_t);
-    const bool scan_here = nb > 0 && table <= kScanTableBytes;
-    const size_t scatter_smem = smem + (scan_here ? table : 0);
+    // (copied with 16-byte asynchronous copies: the tables must start on 16
+    // bytes, which they do in any workspace that itself does)
+    const size_t table = sizeof(int32_t) * (padded_table_words(nb, s.E) +
+                                            (s.dedup ? padded_table_words(nb, s.W) : 0));
+    const bool aligned = ((reinterpret_cast<uintptr_t>(blk_counts) |
+                           reinterpret_cast<uintptr_t>(blk_rcounts)) & 15u) == 0;
+    const bool scan_here = nb > 0 && table <= kScanTableBytes && aligned;
+    const size_t scatter_smem =
+        scan_here ? sizeof(int32_t) * table_offset_words(s.E, s.W) + table : smem;
     cudaError_t e;
     if (smem > 48 * 1024) {
         e = cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -430,14 +430,16 @@ def moe_status_str(status: int) -> str:
 def layout_launches(shape: Shape) -> int:
     """Kernels moe_dispatch_layout launches for this shape: count and scatter,
     plus a separate scan when the per-block count tables (one int32 per block
-    of 256 tokens and slot, and per block and rank with dedup) exceed the
-    16 KB that each scatter block scans itself (csrc/layout.cu,
-    kScanTableBytes)."""
+    of 256 tokens and slot, and per block and rank with dedup, each rounded
+    up to 16 bytes) exceed the 64 KB that each scatter block scans itself
+    (csrc/layout.cu, kScanTableBytes; workspaces from this module are
+    256-byte aligned, as the in-shared-memory scan needs)."""
     nb = (shape.N + 255) // 256
     if nb == 0:
         return 1
-    table = nb * (shape.E + (shape.W if shape.dedup else 0)) * 4
-    return 2 if table <= 16 * 1024 else 3
+    pad4 = lambda n: (n + 3) // 4 * 4  # noqa: E731
+    table = 4 * (pad4(nb * shape.E) + (pad4(nb * shape.W) if shape.dedup else 0))
+    return 2 if table <= 64 * 1024 else 3
 
 
 # ---- a layer with its buffers ----------------------------------------------------------

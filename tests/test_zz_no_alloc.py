@@ -18,10 +18,11 @@ def _tables(layout):
     return {n: t.cpu().numpy().copy() for n, t in layout.tensors.items()}
 
 
-# N = 300: two count blocks, whose last block runs the scan itself; N = 3000:
-# twelve, with the separate scan launch.  Plain and dedup; contiguous
-# placement (NULL) and the correlated workload's permutation.
-@pytest.mark.parametrize("N", [300, 3000])
+# N = 300 and 3000: two and twelve count blocks, whose tables the scatter
+# blocks scan themselves; N = 70000: 274 blocks, whose 70 KB (plain) and
+# 105 KB (dedup) tables take the separate scan launch.  Plain and dedup;
+# contiguous placement (NULL) and the correlated workload's permutation.
+@pytest.mark.parametrize("N", [300, 3000, 70000])
 @pytest.mark.parametrize("dedup", [False, True])
 @pytest.mark.parametrize("placed", [False, True])
 def test_noalloc_layout_equals_workspace_layout_twice(N, dedup, placed):
