@@ -515,13 +515,15 @@ def measure(args, wl, world, rank, headline=True):
 
     stages = layer.stage_names()
     # external events: inside a captured graph they become timing nodes.  The
-    # timed graph carries them around the dominant stage (gate/up) only: a pair
-    # around every stage of every step cost 0.5-1.8% of the step on GB300.  The
-    # other stages are timed by a second, instrumented replay after the timed
-    # region (instrumented_stage_ms).
+    # headline's timed graph carries them around the dominant stage (gate/up)
+    # only: a pair around every stage of every step cost 0.5-1.8% of the step
+    # on GB300.  The other workloads' timed graphs carry none (one pair per
+    # step added 10 us to the 26 us tiny step).  Stages without live events are
+    # timed by a second, instrumented replay after the timed region
+    # (instrumented_stage_ms).
     mk = lambda: (torch.cuda.Event(enable_timing=True, external=use_graph),  # noqa: E731
                   torch.cuda.Event(enable_timing=True, external=use_graph))
-    timed_stages = ["gate_up"] if use_graph else stages
+    timed_stages = (["gate_up"] if headline else []) if use_graph else stages
     ev = [{s: mk() for s in timed_stages} for _ in range(args.steps)] if pipe is None else None
     gev = [[mk() for _ in range(n_mb)] for _ in range(args.steps)] if pipe is not None else None
     for i in range(args.warmup):
@@ -566,7 +568,8 @@ def measure(args, wl, world, rank, headline=True):
                     for s in timed_stages}
         if use_graph:
             # every stage, from one replay of the same K steps with timing
-            # nodes around each; gate/up keeps the timed region's figure
+            # nodes around each; the headline's gate/up keeps the timed
+            # region's figure
             full = instrumented_stage_ms(layer, L_d, x_d, r_d, stages, args.steps)
             stage_ms = {s: stage_ms.get(s, full[s]) for s in stages}
             alone_ms = stage_alone_ms(layer, L_d, x_d, r_d, stages, args.steps)
@@ -629,6 +632,10 @@ def measure(args, wl, world, rank, headline=True):
         stage_report[s] = d
 
     roof = roofline(wl, alg, stage_ms, pk, pk_src, ridge, layer, pipe, n_mb)
+    roof["timed"] = ("CUDA events around every gate/up launch of the timed region"
+                     if "gate_up" in timed_stages or pipe is not None else
+                     "CUDA events around every gate/up launch of an instrumented replay of the "
+                     "same K steps (this workload's timed region carries no timing node)")
     res = {
         "value": round(wl.N * args.steps * world / (elapsed_ms / 1e3), 1),
         "ms_per_step": round(elapsed_ms / args.steps, 4),
