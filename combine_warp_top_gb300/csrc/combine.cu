@@ -11,8 +11,8 @@
 // residual stream).
 //
 // The plain combine runs on persistent warps that each walk units of (token,
-// 2 x 512-byte column stripes), with the next unit's row indices loaded while
-// the current unit's rows are in flight.  The dedup kernels take one warp per
+// 2 x 512-byte column stripes; 4 when k <= 2), with the next unit's row
+// indices loaded while the current unit's rows are in flight.  The dedup kernels take one warp per
 // output row; each lane owns U 16-byte chunks (8 bf16 each) per step along the
 // row, the source rows of a chunk are loaded together, then accumulated in
 // fp32 in j order.  These are latency-bound chains of loads, so the kernels
@@ -165,8 +165,8 @@ __device__ __forceinline__ void finish(float (&acc)[U][8], const uint4* shared,
 // are in flight, so no unit waits on its own index load.  Sums in j order in
 // fp32, then + shared, then + residual:
 // out[t] = bf16(residual[t] + shared[t] + sum_j w[t,j] * y[pair_row[t,j]]).
-template <int kU, int kKB, bool kShared>
-__global__ void __launch_bounds__(kThreads, kShared ? 3 : 4) combine_rows_kernel(
+template <int kU, int kKB, bool kShared, int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) combine_rows_kernel(
     const uint4* __restrict__ y, const float* __restrict__ topk_w,
     const int32_t* __restrict__ pair_row, int N, int C, int k, int R, int groups,
     const uint4* __restrict__ shared, const uint4* __restrict__ residual,
@@ -441,6 +441,20 @@ __global__ void __launch_bounds__(kThreads) acc_finish_kernel(const float4* __re
 
 inline int warps_grid(long long n) { return (int)((n + kThreads / 32 - 1) / (kThreads / 32)); }
 
+// combine_rows_kernel on a persistent grid of at most kMinBlocks blocks per SM.
+template <int kU, int kKB, bool kShared, int kMinBlocks>
+cudaError_t rows(const uint4* y, const float* w, const int32_t* pair_row, const moe_shape& s,
+                 int C, int R, const uint4* sh, const uint4* res, uint4* o, cudaStream_t st) {
+    const int groups = (C + 32 * kU - 1) / (32 * kU);
+    const long long units = (long long)s.N * groups;
+    long long blocks = (units + kThreads / 32 - 1) / (kThreads / 32);
+    const long long cap = (long long)sm_count() * kMinBlocks;
+    if (blocks > cap) blocks = cap;
+    combine_rows_kernel<kU, kKB, kShared, kMinBlocks><<<(int)blocks, kThreads, 0, st>>>(
+        y, w, pair_row, s.N, C, s.k, R, groups, sh, res, o);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_acc_finish(const float* acc, const uint16_t* residual, int N, int H,
@@ -473,20 +487,12 @@ cudaError_t launch_combine(const uint16_t* y, const float* w, const moe_layout& 
         // time, the next unit's indices prefetched (measured against
         // combine_kernel<4>: 0.86 -> 0.935 of HBM on the DeepSeek-V3 shape,
         // 0.76 -> 0.84 on Mixtral's k = 2, 0.97 -> 1.0 on the skewed shape)
-        constexpr int kU = 2, kKB = 2;
-        const int groups = (C + 32 * kU - 1) / (32 * kU);
-        const long long units = (long long)s.N * groups;
-        const int per_sm = sh ? 3 : 4;
-        long long blocks = (units + kThreads / 32 - 1) / (kThreads / 32);
-        const long long cap = (long long)sm_count() * per_sm;
-        if (blocks > cap) blocks = cap;
-        if (sh)
-            combine_rows_kernel<kU, kKB, true><<<(int)blocks, kThreads, 0, st>>>(
-                yy, w, L.pair_row, s.N, C, s.k, R, groups, sh, res, o);
-        else
-            combine_rows_kernel<kU, kKB, false><<<(int)blocks, kThreads, 0, st>>>(
-                yy, w, L.pair_row, s.N, C, s.k, R, groups, nullptr, res, o);
-        return cudaGetLastError();
+        if (sh) return rows<2, 2, true, 3>(yy, w, L.pair_row, s, C, R, sh, res, o, st);
+        // k <= 2: four chunks per lane (a unit is 2 KB of each source row) at
+        // two blocks per SM, so a warp keeps as many rows in flight as with
+        // larger k (Mixtral's k = 2: 0.052 -> 0.050 ms, 0.78 -> 0.82 of HBM)
+        if (s.k <= 2) return rows<4, 2, false, 2>(yy, w, L.pair_row, s, C, R, nullptr, res, o, st);
+        return rows<2, 2, false, 4>(yy, w, L.pair_row, s, C, R, nullptr, res, o, st);
     }
     const int Rd_max = s.N * (s.k < s.W ? s.k : s.W);
     const uint4* yy = reinterpret_cast<const uint4*>(y);

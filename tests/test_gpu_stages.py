@@ -100,6 +100,24 @@ def test_layout_permuted_placement(dedup):
     check_layout(got, oracle.dispatch_layout(ids, placement, wl.E, wl.W), shape)
 
 
+# The scatter blocks copy the per-block count tables ([nb][E], then [nb][W])
+# into shared memory in 16-byte pieces and sum tall columns in parts: tables
+# whose length is not a multiple of four words (the copies' partial tails),
+# and tables tall enough (at least 16 blocks) to be split into parts.
+@pytest.mark.parametrize("placed", [False, True])
+@pytest.mark.parametrize("dedup", [False, True])
+@pytest.mark.parametrize("N,E,k,W", [(700, 21, 3, 7), (4400, 7, 3, 7), (5000, 6, 3, 3),
+                                     (20000, 12, 4, 4)])
+def test_layout_count_table_tails_and_parts(N, E, k, W, dedup, placed):
+    wl = synth.Workload("tables", N, 64, E, k, 64, W)
+    ids, _ = oracle.route(synth.make_logits(wl), k)
+    placement = synth.permutation(0, 52, E).astype(np.int32) if placed else None
+    shape = shape_of(wl, dedup)
+    got = run_layout(ids, placement, shape)
+    ref_placement = placement if placed else np.arange(E)
+    check_layout(got, oracle.dispatch_layout(ids, ref_placement, E, W), shape)
+
+
 def test_layout_skewed_and_empty_experts():
     # every token on expert 5 and one of {0, 1}: most experts empty, one full
     N, E, k, W = 1000, 16, 2, 4
