@@ -12,11 +12,12 @@
 //
 // The plain combine runs on persistent warps that each walk units of (token,
 // 2 x 512-byte column stripes; 4 when k <= 2), with the next unit's row
-// indices loaded while the current unit's rows are in flight.  The dedup kernels take one warp per
-// output row; each lane owns U 16-byte chunks (8 bf16 each) per step along the
-// row, the source rows of a chunk are loaded together, then accumulated in
-// fp32 in j order.  These are latency-bound chains of loads, so the kernels
-// are compiled with register caps that keep 24-32 warps per SM in flight.
+// indices loaded while the current unit's rows are in flight.  The dedup
+// kernels take one warp per output row; each lane owns U 16-byte chunks (8
+// bf16 each) per step along the row, the source rows of a chunk are loaded
+// together, then accumulated in fp32 in j order.  These are latency-bound
+// chains of loads, so the kernels are compiled with register caps that keep
+// 16-32 warps per SM in flight.
 #include "moe_internal.cuh"
 
 namespace moe {

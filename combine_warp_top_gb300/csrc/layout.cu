@@ -304,17 +304,16 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(
 // Scatter-side scan of one [nb][ncol] count table held in shared memory:
 // col_base[c] = first row of this block's part of column c (the column
 // offset plus the counts of the blocks before this one); totals[c] and
-// starts[c] = the column sums and their exclusive scan.
-// Tall tables split the rows of a column into P parts of at least 8 rows,
-// summed by different threads (P <= blockDim / ncol; the part sums wait in
-// ss.starts until the scan overwrites it); otherwise a thread walks a whole
-// column.
+// starts[c] = the column sums and their exclusive scan.  Tall tables split
+// the rows of a column into P parts of at least 8 rows, summed by different
+// threads (P <= blockDim / ncol; the part sums wait in ss.starts until the
+// scan overwrites it); otherwise a thread walks a whole column.
 __device__ void block_bases(const int32_t* tab, int nb, int ncol, int* col_base, ScanSmem& ss) {
     const int P = min((int)blockDim.x / ncol, nb / 8);
     if (P > 1) {
         const int c = threadIdx.x % ncol, part = threadIdx.x / ncol;
         const int L = (nb + P - 1) / P, b0 = part * L, b1 = min(nb, b0 + L);
-        int* psum = ss.starts;             // [P][ncol]
+        int* psum = ss.starts;                // [P][ncol]
         int* pbefore = ss.starts + P * ncol;  // [P][ncol]
         if (part < P) {
             int tot = 0, before = 0;
@@ -483,8 +482,8 @@ cudaError_t launch_layout(const int32_t* ids, const int32_t* placement, const mo
     const int nb = layout_blocks(s.N);
     const size_t smem = smem_bytes(s.E, s.W);
     // the scatter blocks scan the count tables themselves when they are small
-    // (copied with 16-byte asynchronous copies: the tables must start on 16
-    // bytes, which they do in any workspace that itself does)
+    // (they copy them in 16-byte pieces, so a workspace that does not start on
+    // 16 bytes takes the separate scan instead)
     const size_t table = sizeof(int32_t) * (padded_table_words(nb, s.E) +
                                             (s.dedup ? padded_table_words(nb, s.W) : 0));
     const bool aligned = ((reinterpret_cast<uintptr_t>(blk_counts) |
