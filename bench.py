@@ -45,6 +45,9 @@ def parse_args(argv=None):
     p.add_argument("--tokens", type=int, default=None, help="override N (profiling cases)")
     p.add_argument("--experts", type=int, default=None, help="override E (profiling cases)")
     p.add_argument("--dedup", choices=["auto", "on", "off"], default="auto")
+    p.add_argument("--weights", choices=["packed", "row_major"], default="packed",
+                   help="expert weights as moe_pack_weights' tile-contiguous copy (packed once "
+                        "before timing) or in nn.Linear layout")
     p.add_argument("--gemm", choices=["auto", "single", "pair"], default="auto",
                    help="grouped-GEMM kernel (the shape's gemm field)")
     p.add_argument("--placement-search", action="store_true",
@@ -485,8 +488,9 @@ def measure(args, wl, world, rank, headline=True):
     microbatch = args.microbatch if headline else 0
     if fuse_combine and (microbatch or shared is not None):
         raise SystemExit("--fuse-combine runs the plain layer: no --microbatch, no --shared-expert")
+    pack = args.weights == "packed"
     layer = moe.MoELayer(shape, w_gate, w_up, w_down, placement_d, shared=shared,
-                         fuse_combine=fuse_combine)
+                         fuse_combine=fuse_combine, pack=pack)
 
     x_h = torch.from_numpy(synth.make_x(wl, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
     r_h = torch.from_numpy(synth.make_residual(wl, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -500,7 +504,7 @@ def measure(args, wl, world, rank, headline=True):
     pipe = None
     if microbatch:
         pipe = moe.MicrobatchPipeline(shape, w_gate, w_up, w_down, placement_d,
-                                      microbatch=microbatch, shared=shared)
+                                      microbatch=microbatch, shared=shared, pack=pack)
     runner = pipe if pipe is not None else layer
     n_mb = len(pipe.chunks()) if pipe is not None else 0
 
@@ -754,6 +758,9 @@ def run_ours(args):
         "fused_combine": bool(args.fuse_combine),
         "microbatch": args.microbatch or None,
         "gemm": args.gemm,
+        "weights": (("packed once before timing (moe_pack_weights: every 64-deep slice of "
+                     "a 256-row weight tile contiguous)") if args.weights == "packed"
+                    else "row-major (nn.Linear layout)"),
         "launch": ("one CUDA graph of the K timed steps, timing nodes around gate/up only; "
                    "the other stages' times from a second, instrumented replay of the K steps")
                   if r["graph"] else "eager, one C call per stage",

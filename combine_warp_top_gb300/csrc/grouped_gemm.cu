@@ -11,6 +11,10 @@
 //             up columns of the same rows, so the epilogue can apply
 //             h = SiLU(g) * u straight out of TMEM and store bf16 h.
 //   down:     a 128x256 tile of y = h Wd^T, stored as bf16.
+// The weight operand B comes from the row-major [E, rows, K] matrices (a 3-D
+// map, 256 strided 128-byte pieces per k-block) or from their packed copy
+// (moe_pack_weights: each k-block of a 256-row tile one contiguous 32 KB
+// block of a [rows, 64] map), which the HBM-bound shapes stream faster.
 // Roles (192 threads, 320 with gathered rows): warp 0 issues TMA loads into a
 // 4-stage shared-memory ring (128B swizzle; with gathered rows only B, while
 // warps 6-9 copy the A rows in with cp.async), warp 1 owns TMEM and issues
@@ -102,7 +106,8 @@ __global__ void __launch_bounds__(threads_for(kGather), 1)
                         int E, int K, int n_out,
                         __nv_bfloat16* __restrict__ out, int* err,
                         const int32_t* __restrict__ a_rows, int a_total, int a_src_rows,
-                        const uint16_t* __restrict__ a_src, int a_keep, const CombineArgs cmb) {
+                        const uint16_t* __restrict__ a_src, int a_keep, const CombineArgs cmb,
+                        int b_packed) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* tiles = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -177,7 +182,11 @@ __global__ void __launch_bounds__(threads_for(kGather), 1)
                     mbar_expect_tx(full, kGather ? B_BYTES : STAGE_BYTES);
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-                    if (kSwiGLU) {
+                    if (b_packed) {
+                        // packed weights: the tile's 256 x 64 operand slice is one
+                        // contiguous block of the [rows, 64] map
+                        tma_load_2d(b_s, &tmB0, full, 0, ((e * NB + nb) * KB + kb) * kPackRows);
+                    } else if (kSwiGLU) {
                         tma_load_3d(b_s, &tmB0, full, kb * BK, n0, e);
                         tma_load_3d(b_s + B_BYTES / 2, &tmB1, full, kb * BK, n0, e);
                     } else {
@@ -503,6 +512,18 @@ bool map_3d(CUtensorMap* m, const void* ptr, uint64_t E, uint64_t rows, uint64_t
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Map over packed weights (E experts x n_blocks n-blocks x ceil(K/64) k-blocks
+// of 256 x 64 bf16) as a [rows, 64] matrix; box = box_rows rows.  *second is
+// set to the same map (the kernels take a second B map for row-major up
+// weights).
+bool map_packed(CUtensorMap* m, CUtensorMap* second, const void* ptr, int E, int n_blocks, int K,
+                uint32_t box_rows) {
+    const long long rows = packed_rows(E, n_blocks, K);
+    if (rows >= (1LL << 31) || !map_2d(m, ptr, (uint64_t)rows, 64, box_rows)) return false;
+    *second = *m;
+    return true;
+}
+
 namespace {
 
 bool set_smem_attr() {
@@ -548,9 +569,10 @@ moe_status launch_gate_up(const uint16_t* rows, const GemmGroup& g, int H, int I
         memset(&a, 0, sizeof(a));  // unused: the gather warps read `rows` directly
     else
         ok_a = map_2d(&a, rows, g.R, H, BM);
-    if (!ok_a || !map_3d(&bg, wg, g.E, I, H, kMmaN / 2) ||
-        !map_3d(&bu, wu, g.E, I, H, kMmaN / 2) || !map_2d(&o, h, g.R, I, 32))
-        return MOE_ERR_UNSUPPORTED;
+    const bool ok_b = g.packed ? map_packed(&bg, &bu, wg, g.E, (I + 127) / 128, H, kMmaN)
+                               : map_3d(&bg, wg, g.E, I, H, kMmaN / 2) &&
+                                     map_3d(&bu, wu, g.E, I, H, kMmaN / 2);
+    if (!ok_a || !ok_b || !map_2d(&o, h, g.R, I, 32)) return MOE_ERR_UNSUPPORTED;
     if (!set_smem_attr()) return MOE_ERR_CUDA;
     int grid;
     const moe_status ss = schedule(g, (I + kMmaN / 2 - 1) / (kMmaN / 2), st, &grid);
@@ -559,20 +581,21 @@ moe_status launch_gate_up(const uint16_t* rows, const GemmGroup& g, int H, int I
     if (gather)
         grouped_gemm_kernel<true, true, false><<<grid, threads_for(true), kSmemBytes, st>>>(
             a, bg, bu, o, g.offsets, g.counts, g.E, H, I, hb, g.err, gather, (int)g.R,
-            (int)src_rows, rows, keep_src ? 1 : 0, CombineArgs{});
+            (int)src_rows, rows, keep_src ? 1 : 0, CombineArgs{}, g.packed ? 1 : 0);
     else
         grouped_gemm_kernel<true, false, false><<<grid, kThreads, kSmemBytes, st>>>(
             a, bg, bu, o, g.offsets, g.counts, g.E, H, I, hb, g.err, nullptr, 0, 0,
-            nullptr, 0, CombineArgs{});
+            nullptr, 0, CombineArgs{}, g.packed ? 1 : 0);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status launch_down(const uint16_t* h, const GemmGroup& g, int H, int I, const uint16_t* wd,
                        uint16_t* y, cudaStream_t st) {
     if (g.R == 0) return MOE_OK;
-    CUtensorMap a, bd, o;
-    if (!map_2d(&a, h, g.R, I, BM) || !map_3d(&bd, wd, g.E, H, I, kMmaN) ||
-        !map_2d(&o, y, g.R, H, 32))
+    CUtensorMap a, bd, unused, o;
+    const bool ok_b = g.packed ? map_packed(&bd, &unused, wd, g.E, (H + 255) / 256, I, kMmaN)
+                               : map_3d(&bd, wd, g.E, H, I, kMmaN);
+    if (!map_2d(&a, h, g.R, I, BM) || !ok_b || !map_2d(&o, y, g.R, H, 32))
         return MOE_ERR_UNSUPPORTED;
     if (!set_smem_attr()) return MOE_ERR_CUDA;
     int grid;
@@ -580,24 +603,26 @@ moe_status launch_down(const uint16_t* h, const GemmGroup& g, int H, int I, cons
     if (ss != MOE_OK) return ss;
     grouped_gemm_kernel<false, false, false><<<grid, kThreads, kSmemBytes, st>>>(
         a, bd, bd, o, g.offsets, g.counts, g.E, I, H,
-        reinterpret_cast<__nv_bfloat16*>(y), g.err, nullptr, 0, 0, nullptr, 0, CombineArgs{});
+        reinterpret_cast<__nv_bfloat16*>(y), g.err, nullptr, 0, 0, nullptr, 0, CombineArgs{},
+        g.packed ? 1 : 0);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status launch_down_combine(const uint16_t* h, const GemmGroup& g, int H, int I,
                                const uint16_t* wd, const CombineArgs& cmb, cudaStream_t st) {
     if (g.R == 0) return MOE_OK;
-    CUtensorMap a, bd, o;
+    CUtensorMap a, bd, unused, o;
     memset(&o, 0, sizeof(o));  // unused: the epilogue adds into cmb.acc
-    if (!map_2d(&a, h, g.R, I, BM) || !map_3d(&bd, wd, g.E, H, I, kMmaN))
-        return MOE_ERR_UNSUPPORTED;
+    const bool ok_b = g.packed ? map_packed(&bd, &unused, wd, g.E, (H + 255) / 256, I, kMmaN)
+                               : map_3d(&bd, wd, g.E, H, I, kMmaN);
+    if (!map_2d(&a, h, g.R, I, BM) || !ok_b) return MOE_ERR_UNSUPPORTED;
     if (!set_smem_attr()) return MOE_ERR_CUDA;
     int grid;
     const moe_status ss = schedule(g, (H + kMmaN - 1) / kMmaN, st, &grid);
     if (ss != MOE_OK) return ss;
     grouped_gemm_kernel<false, false, true><<<grid, kThreads, kSmemBytes, st>>>(
         a, bd, bd, o, g.offsets, g.counts, g.E, I, H, nullptr, g.err, nullptr, 0, 0,
-        nullptr, 0, cmb);
+        nullptr, 0, cmb, g.packed ? 1 : 0);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

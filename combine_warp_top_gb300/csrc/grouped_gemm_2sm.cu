@@ -160,7 +160,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                              const int32_t* __restrict__ expert_offsets,
                              const int32_t* __restrict__ expert_counts,
                              int E, int K, int n_out, __nv_bfloat16* __restrict__ out,
-                             int* err, int* tile_counter) {
+                             int* err, int* tile_counter, int b_packed) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* tiles = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -254,7 +254,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     }
                     tma_load_2d_pair(a_s, &tmA, full, kb * BK, row0);
-                    if (kSwiGLU) {
+                    if (b_packed) {
+                        // packed weights: this CTA's 128 rows of the tile's 256 x 64
+                        // operand slice (gate rows in the leader, up rows in the peer)
+                        tma_load_2d_pair(b_s, &tmB0, full, 0,
+                                         ((e * NB + nb) * KB + kb) * kPackRows +
+                                             (int)rank * (kMmaN / 2));
+                    } else if (kSwiGLU) {
                         // leader holds the gate half of N, the peer the up half
                         tma_load_3d_pair(b_s, leader ? &tmB0 : &tmB1, full, kb * BK, n0, e);
                     } else {
@@ -478,8 +484,10 @@ moe_status launch_gate_up_pair(const uint16_t* rows, const GemmGroup& g, int H, 
                                cudaStream_t st) {
     if (g.R == 0) return MOE_OK;
     CUtensorMap a, bg, bu, o;
-    if (!map_2d(&a, rows, g.R, H, BMC) || !map_3d(&bg, wg, g.E, I, H, kMmaN / 2) ||
-        !map_3d(&bu, wu, g.E, I, H, kMmaN / 2) || !map_2d(&o, h, g.R, I, 32))
+    const bool ok_b = g.packed ? map_packed(&bg, &bu, wg, g.E, (I + 127) / 128, H, kMmaN / 2)
+                               : map_3d(&bg, wg, g.E, I, H, kMmaN / 2) &&
+                                     map_3d(&bu, wu, g.E, I, H, kMmaN / 2);
+    if (!map_2d(&a, rows, g.R, H, BMC) || !ok_b || !map_2d(&o, h, g.R, I, 32))
         return MOE_ERR_UNSUPPORTED;
     if (!set_pair_smem_attr()) return MOE_ERR_CUDA;
     int grid;
@@ -487,16 +495,17 @@ moe_status launch_gate_up_pair(const uint16_t* rows, const GemmGroup& g, int H, 
     if (ss != MOE_OK) return ss;
     grouped_gemm_pair_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(
         a, bg, bu, o, g.offsets, g.counts, g.E, H, I,
-        reinterpret_cast<__nv_bfloat16*>(h), g.err, g.prefix + g.E + 1);
+        reinterpret_cast<__nv_bfloat16*>(h), g.err, g.prefix + g.E + 1, g.packed ? 1 : 0);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status launch_down_pair(const uint16_t* h, const GemmGroup& g, int H, int I,
                             const uint16_t* wd, uint16_t* y, cudaStream_t st) {
     if (g.R == 0) return MOE_OK;
-    CUtensorMap a, bd, o;
-    if (!map_2d(&a, h, g.R, I, BMC) || !map_3d(&bd, wd, g.E, H, I, kMmaN / 2) ||
-        !map_2d(&o, y, g.R, H, 32))
+    CUtensorMap a, bd, unused, o;
+    const bool ok_b = g.packed ? map_packed(&bd, &unused, wd, g.E, (H + 255) / 256, I, kMmaN / 2)
+                               : map_3d(&bd, wd, g.E, H, I, kMmaN / 2);
+    if (!map_2d(&a, h, g.R, I, BMC) || !ok_b || !map_2d(&o, y, g.R, H, 32))
         return MOE_ERR_UNSUPPORTED;
     if (!set_pair_smem_attr()) return MOE_ERR_CUDA;
     int grid;
@@ -504,7 +513,7 @@ moe_status launch_down_pair(const uint16_t* h, const GemmGroup& g, int H, int I,
     if (ss != MOE_OK) return ss;
     grouped_gemm_pair_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(
         a, bd, bd, o, g.offsets, g.counts, g.E, I, H,
-        reinterpret_cast<__nv_bfloat16*>(y), g.err, g.prefix + g.E + 1);
+        reinterpret_cast<__nv_bfloat16*>(y), g.err, g.prefix + g.E + 1, g.packed ? 1 : 0);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

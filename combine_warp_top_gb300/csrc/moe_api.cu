@@ -32,7 +32,18 @@ moe_status check_shape(const moe_shape* s) {
     if (s->gemm != MOE_GEMM_AUTO && s->gemm != MOE_GEMM_SINGLE_CTA &&
         s->gemm != MOE_GEMM_CTA_PAIR)
         return MOE_ERR_INVALID_ARG;
+    if (s->weights != MOE_WEIGHTS_ROW_MAJOR && s->weights != MOE_WEIGHTS_PACKED)
+        return MOE_ERR_INVALID_ARG;
+    // the GEMMs address packed rows with 32-bit TMA coordinates
+    if (s->weights == MOE_WEIGHTS_PACKED &&
+        (packed_gate_up_rows(*s) >= (1LL << 31) || packed_down_rows(*s) >= (1LL << 31)))
+        return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
+}
+
+// w_up is read only in the row-major layout (the packed gate/up weights hold both).
+inline bool up_given(const moe_shape* s, const uint16_t* w_up) {
+    return w_up != nullptr || s->weights == MOE_WEIGHTS_PACKED;
 }
 
 moe_status check_layout(const moe_layout* L, const moe_shape* s) {
@@ -66,7 +77,8 @@ bool use_pair(long long R, int E, int32_t gemm) {
 GemmGroup routed_group(const moe_layout& L, const moe_shape& s, void* ws) {
     const Workspace wl = workspace_layout(s);
     return GemmGroup{L.expert_counts, L.expert_offsets, s.E, (long long)s.N * s.k,
-                     ws_ptr<int32_t>(ws, wl.mblk_prefix), ws_ptr<int>(ws, wl.err)};
+                     ws_ptr<int32_t>(ws, wl.mblk_prefix), ws_ptr<int>(ws, wl.err),
+                     s.weights == MOE_WEIGHTS_PACKED};
 }
 
 // The shared expert's GEMM problem: all N token rows as one segment.
@@ -115,6 +127,31 @@ extern "C" {
 size_t moe_workspace_bytes(const moe_shape* shape) {
     if (check_shape(shape) != MOE_OK) return 0;
     return workspace_layout(*shape).total;
+}
+
+size_t moe_packed_gate_up_bytes(const moe_shape* shape) {
+    if (check_shape(shape) != MOE_OK) return 0;
+    return (size_t)packed_gate_up_rows(*shape) * 64 * sizeof(uint16_t);
+}
+
+size_t moe_packed_down_bytes(const moe_shape* shape) {
+    if (check_shape(shape) != MOE_OK) return 0;
+    return (size_t)packed_down_rows(*shape) * 64 * sizeof(uint16_t);
+}
+
+moe_status moe_pack_weights(const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                            const moe_shape* shape, uint16_t* gate_up_packed,
+                            uint16_t* down_packed, void* stream) {
+    MOE_RANGE();
+    if (!shape) return MOE_ERR_INVALID_ARG;
+    moe_shape s = *shape;
+    s.weights = MOE_WEIGHTS_ROW_MAJOR;  // not read here
+    MOE_TRY(check_shape(&s));
+    if (gate_up_packed && (!w_gate || !w_up)) return MOE_ERR_INVALID_ARG;
+    if (down_packed && !w_down) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w_gate, w_up, w_down, gate_up_packed, down_packed)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_pack(w_gate, w_up, w_down, s, gate_up_packed, down_packed,
+                                   as_stream(stream)));
 }
 
 moe_status moe_route(const float* logits, const moe_shape* shape, int32_t* topk_ids,
@@ -190,7 +227,7 @@ moe_status moe_ffn_gate_up(const uint16_t* rows, const moe_layout* layout, const
     MOE_TRY(check_layout(layout, shape));
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (shape->N == 0) return MOE_OK;
-    if (!rows || !w_gate || !w_up || !h) return MOE_ERR_INVALID_ARG;
+    if (!rows || !w_gate || !up_given(shape, w_up) || !h) return MOE_ERR_INVALID_ARG;
     if (!aligned16(rows, w_gate, w_up, h)) return MOE_ERR_INVALID_ARG;
     const GemmGroup g = routed_group(*layout, *shape, ws);
     if (use_pair(g.R, g.E, shape->gemm))
@@ -207,7 +244,8 @@ moe_status moe_ffn_gate_up_gather(const uint16_t* src, const int32_t* row_index,
     MOE_TRY(check_layout(layout, shape));
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (shape->N == 0) return MOE_OK;
-    if (!src || !row_index || !w_gate || !w_up || !h) return MOE_ERR_INVALID_ARG;
+    if (!src || !row_index || !w_gate || !up_given(shape, w_up) || !h)
+        return MOE_ERR_INVALID_ARG;
     if (!aligned16(src, w_gate, w_up, h)) return MOE_ERR_INVALID_ARG;
     if (src_rows <= 0 || src_rows >= ((int64_t)1 << 31)) return MOE_ERR_INVALID_ARG;
     return launch_gate_up(src, routed_group(*layout, *shape, ws), shape->H, shape->I, w_gate, w_up,
@@ -259,7 +297,8 @@ moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const mo
     MOE_TRY(check_layout(layout, shape));
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (shape->N == 0) return MOE_OK;
-    if (!xd || !w_gate || !w_up || !w_down || !h || !y) return MOE_ERR_INVALID_ARG;
+    if (!xd || !w_gate || !up_given(shape, w_up) || !w_down || !h || !y)
+        return MOE_ERR_INVALID_ARG;
     if (!aligned16(xd, w_gate, w_up, w_down, h, y)) return MOE_ERR_INVALID_ARG;
     (void)xe;
     if (shape->dedup) {
@@ -336,8 +375,8 @@ moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32
     MOE_TRY(check_layout(layout, shape));
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (shape->N == 0) return MOE_OK;
-    if (!logits || !x || !w_gate || !w_up || !w_down || !topk_ids || !topk_w || !xd || !h ||
-        !y || !out)
+    if (!logits || !x || !w_gate || !up_given(shape, w_up) || !w_down || !topk_ids ||
+        !topk_w || !xd || !h || !y || !out)
         return MOE_ERR_INVALID_ARG;
     if (!aligned16(x, w_gate, w_up, w_down, residual, xd, xe, h, y, partial, out))
         return MOE_ERR_INVALID_ARG;

@@ -115,7 +115,22 @@ struct GemmGroup {
     long long R;
     int32_t* prefix;
     int* err;
+    bool packed = false;  // weights in the packed layout (moe_pack_weights)
 };
+
+// Packed expert weights: blocks of kPackRows x 64 bf16 (32 KB), one per
+// (expert, n-block, 64-deep k-block), as rows of a [rows, 64] matrix.  An
+// n-block is 128 gate + 128 up columns (gate/up) or 256 output columns (down).
+constexpr int kPackRows = 256;
+inline long long packed_rows(int E, int n_blocks, int K) {
+    return (long long)E * n_blocks * ((K + 63) / 64) * kPackRows;
+}
+inline long long packed_gate_up_rows(const moe_shape& s) {
+    return packed_rows(s.E, (s.I + 127) / 128, s.H);
+}
+inline long long packed_down_rows(const moe_shape& s) {
+    return packed_rows(s.E, (s.H + 255) / 256, s.I);
+}
 
 // Inputs of the combine fused into the down GEMM's epilogue: row i of y is
 // added, times its routing weight, into acc[row_token[i], :] (fp32 [N, H]).
@@ -146,6 +161,10 @@ cudaError_t launch_wait_selftest(long long limit_cycles, int* err, cudaStream_t 
 // counts = {N}, offsets = {0, N}: one dense segment of N rows.
 cudaError_t launch_dense_group(int N, int32_t* counts, int32_t* offsets, cudaStream_t st);
 
+// moe_pack_weights (pack.cu): either output may be null.
+cudaError_t launch_pack(const uint16_t* wg, const uint16_t* wu, const uint16_t* wd,
+                        const moe_shape& s, uint16_t* gate_up, uint16_t* down, cudaStream_t st);
+
 cudaError_t launch_coselection(const int32_t* ids, const moe_shape& s, int32_t* W, int* err,
                                cudaStream_t st);
 
@@ -158,6 +177,8 @@ moe_status placement_search(const int32_t* W, int E, int ranks, int nodes, long 
 bool map_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
 bool map_3d(CUtensorMap* m, const void* ptr, uint64_t E, uint64_t rows, uint64_t cols,
             uint32_t box_rows);
+bool map_packed(CUtensorMap* m, CUtensorMap* second, const void* ptr, int E, int n_blocks, int K,
+                uint32_t box_rows);
 
 // CTA-pair GEMMs (grouped_gemm_2sm.cu): 256-row tiles on tcgen05 cta_group::2.
 moe_status launch_gate_up_pair(const uint16_t* rows, const GemmGroup& g, int H, int I,

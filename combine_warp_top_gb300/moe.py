@@ -17,9 +17,11 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
-SHAPE_FIELDS = ("N", "H", "E", "k", "W", "I", "dedup", "gemm")
+SHAPE_FIELDS = ("N", "H", "E", "k", "W", "I", "dedup", "gemm", "weights")
 # moe_gemm_kernel values of include/moe.h
 GEMM_KERNELS = {"auto": 0, "single": 1, "pair": 2}
+# moe_weight_layout values of include/moe.h
+WEIGHT_LAYOUTS = {"row_major": 0, "packed": 1}
 LAYOUT_FIELDS = ("expert_counts", "expert_offsets", "rank_offsets", "row_token", "pair_row",
                  "dedup_counts", "dedup_offsets", "dedup_row_token", "pair_dedup_row",
                  "expand_src", "n_dedup_rows")
@@ -56,6 +58,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     shp, lay = ctypes.POINTER(MoeShape), ctypes.POINTER(MoeLayout)
     sigs = {
         "moe_workspace_bytes": (S, [shp]),
+        "moe_packed_gate_up_bytes": (S, [shp]),
+        "moe_packed_down_bytes": (S, [shp]),
+        "moe_pack_weights": (I32, [P, P, P, shp, P, P, P]),
         "moe_route": (I32, [P, shp, P, P, P]),
         "moe_route_full_softmax": (I32, [P, shp, P, P, P]),
         "moe_route_sigmoid_bias": (I32, [P, P, shp, P, P, P]),
@@ -176,12 +181,17 @@ class Shape:
     # which grouped-GEMM kernel runs: "auto", "single" (128-row tiles, one CTA)
     # or "pair" (256-row tiles on a 2-CTA cluster); see moe_gemm_kernel
     gemm: str = "auto"
+    # layout of the expert weights the calls take: "row_major" (nn.Linear) or
+    # "packed" (moe_pack_weights); see moe_weight_layout
+    weights: str = "row_major"
 
     def c(self) -> MoeShape:
         if self.gemm not in GEMM_KERNELS:
             raise ValueError(f"gemm must be one of {sorted(GEMM_KERNELS)}")
+        if self.weights not in WEIGHT_LAYOUTS:
+            raise ValueError(f"weights must be one of {sorted(WEIGHT_LAYOUTS)}")
         return MoeShape(self.N, self.H, self.E, self.k, self.W, self.I, int(bool(self.dedup)),
-                        GEMM_KERNELS[self.gemm])
+                        GEMM_KERNELS[self.gemm], WEIGHT_LAYOUTS[self.weights])
 
     @property
     def R(self) -> int:
@@ -229,6 +239,62 @@ def workspace(shape: Shape, device="cuda") -> torch.Tensor:
 
 def _rows_d(shape: Shape) -> int:
     return shape.R_d_max if shape.dedup else shape.R
+
+
+def moe_packed_gate_up_bytes(shape: Shape) -> int:
+    return int(load().moe_packed_gate_up_bytes(ctypes.byref(shape.c())))
+
+
+def moe_packed_down_bytes(shape: Shape) -> int:
+    return int(load().moe_packed_down_bytes(ctypes.byref(shape.c())))
+
+
+def _gate_up_w(shape: Shape, w_gate, w_up):
+    """Pointers of the gate/up weights in the shape's layout (packed: both in
+    w_gate, w_up not read and may be None)."""
+    s = shape
+    if s.weights == "packed":
+        return (_bf16(w_gate, moe_packed_gate_up_bytes(s) // 2, "w_gate (packed gate/up)"),
+                _bf16(w_up, 0, "w_up"))
+    return (_bf16(w_gate, s.E * s.I * s.H, "w_gate"), _bf16(w_up, s.E * s.I * s.H, "w_up"))
+
+
+def _down_w(shape: Shape, w_down):
+    s = shape
+    if s.weights == "packed":
+        return _bf16(w_down, moe_packed_down_bytes(s) // 2, "w_down (packed)")
+    return _bf16(w_down, s.E * s.H * s.I, "w_down")
+
+
+def moe_pack_weights(w_gate, w_up, w_down, shape: Shape, gate_up_packed, down_packed,
+                     stream=None):
+    """Row-major weights -> the packed layout (either output may be None)."""
+    s = dataclasses.replace(shape, weights="row_major")
+    gu = down = None
+    if gate_up_packed is not None:
+        gu = _bf16(gate_up_packed, moe_packed_gate_up_bytes(s) // 2, "gate_up_packed")
+        w_gate = _bf16(w_gate, s.E * s.I * s.H, "w_gate")
+        w_up = _bf16(w_up, s.E * s.I * s.H, "w_up")
+    else:
+        w_gate = w_up = None
+    if down_packed is not None:
+        down = _bf16(down_packed, moe_packed_down_bytes(s) // 2, "down_packed")
+        w_down = _bf16(w_down, s.E * s.H * s.I, "w_down")
+    else:
+        w_down = None
+    _check(load().moe_pack_weights(w_gate, w_up, w_down, ctypes.byref(s.c()), gu, down,
+                                   _stream(stream)), "moe_pack_weights")
+
+
+def pack_weights(shape: Shape, w_gate, w_up, w_down, stream=None):
+    """Allocates and fills the packed gate/up and down weights of `shape`;
+    returns (gate_up_packed, down_packed), flat bf16 device tensors."""
+    s = dataclasses.replace(shape, weights="row_major")
+    dev = w_gate.device
+    gu = torch.empty(moe_packed_gate_up_bytes(s) // 2, dtype=torch.bfloat16, device=dev)
+    dn = torch.empty(moe_packed_down_bytes(s) // 2, dtype=torch.bfloat16, device=dev)
+    moe_pack_weights(w_gate, w_up, w_down, s, gu, dn, stream)
+    return gu, dn
 
 
 def moe_route(logits, shape: Shape, topk_ids, topk_w, stream=None):
@@ -282,9 +348,8 @@ def moe_expert_ffn(xd, layout: Layout, shape: Shape, w_gate, w_up, w_down, xe, h
                    stream=None):
     s = shape
     _check(load().moe_expert_ffn(_bf16(xd, _rows_d(s) * s.H, "xd"), _lay(layout, s),
-                                 ctypes.byref(s.c()), _bf16(w_gate, s.E * s.I * s.H, "w_gate"),
-                                 _bf16(w_up, s.E * s.I * s.H, "w_up"),
-                                 _bf16(w_down, s.E * s.H * s.I, "w_down"), _ptr(xe),
+                                 ctypes.byref(s.c()), *_gate_up_w(s, w_gate, w_up),
+                                 _down_w(s, w_down), _ptr(xe),
                                  _bf16(h, s.R * s.I, "h"), _bf16(y, s.R * s.H, "y"), *_ws(ws),
                                  _stream(stream)), "moe_expert_ffn")
 
@@ -299,8 +364,8 @@ def moe_expand(xd, layout: Layout, shape: Shape, xe, stream=None):
 def moe_ffn_gate_up(rows, layout: Layout, shape: Shape, w_gate, w_up, h, ws, stream=None):
     s = shape
     _check(load().moe_ffn_gate_up(_bf16(rows, s.R * s.H, "rows"), _lay(layout, s),
-                                  ctypes.byref(s.c()), _bf16(w_gate, s.E * s.I * s.H, "w_gate"),
-                                  _bf16(w_up, s.E * s.I * s.H, "w_up"), _bf16(h, s.R * s.I, "h"),
+                                  ctypes.byref(s.c()), *_gate_up_w(s, w_gate, w_up),
+                                  _bf16(h, s.R * s.I, "h"),
                                   *_ws(ws), _stream(stream)), "moe_ffn_gate_up")
 
 
@@ -312,8 +377,7 @@ def moe_ffn_gate_up_gather(src, row_index, layout: Layout, shape: Shape, w_gate,
     _check(load().moe_ffn_gate_up_gather(_bf16(src, src_rows * s.H, "src"),
                                          _i32(row_index, s.R, "row_index"), src_rows,
                                          _lay(layout, s), ctypes.byref(s.c()),
-                                         _bf16(w_gate, s.E * s.I * s.H, "w_gate"),
-                                         _bf16(w_up, s.E * s.I * s.H, "w_up"),
+                                         *_gate_up_w(s, w_gate, w_up),
                                          _bf16(h, s.R * s.I, "h"), *_ws(ws), _stream(stream)),
            "moe_ffn_gate_up_gather")
 
@@ -322,8 +386,7 @@ def moe_ffn_down_combine(h, topk_w, layout: Layout, shape: Shape, w_down, residu
                          ws, stream=None):
     s = shape
     _check(load().moe_ffn_down_combine(_bf16(h, s.R * s.I, "h"), _f32(topk_w, s.R, "topk_w"),
-                                       _lay(layout, s), ctypes.byref(s.c()),
-                                       _bf16(w_down, s.E * s.H * s.I, "w_down"),
+                                       _lay(layout, s), ctypes.byref(s.c()), _down_w(s, w_down),
                                        _bf16(residual, s.N * s.H, "residual"),
                                        _f32(acc, s.N * s.H, "acc"), _bf16(out, s.N * s.H, "out"),
                                        *_ws(ws), _stream(stream)), "moe_ffn_down_combine")
@@ -338,8 +401,8 @@ def moe_layer_skips_dispatch(shape: Shape) -> bool:
 def moe_ffn_down(h, layout: Layout, shape: Shape, w_down, y, ws, stream=None):
     s = shape
     _check(load().moe_ffn_down(_bf16(h, s.R * s.I, "h"), _lay(layout, s), ctypes.byref(s.c()),
-                               _bf16(w_down, s.E * s.H * s.I, "w_down"),
-                               _bf16(y, s.R * s.H, "y"), *_ws(ws), _stream(stream)),
+                               _down_w(s, w_down), _bf16(y, s.R * s.H, "y"), *_ws(ws),
+                               _stream(stream)),
            "moe_ffn_down")
 
 
@@ -360,8 +423,7 @@ def moe_layer_forward(logits, x, placement, w_gate, w_up, w_down, residual, shap
     xd_rows = 0 if moe_layer_skips_dispatch(s) else _rows_d(s)
     _check(load().moe_layer_forward(
         _f32(logits, s.N * s.E, "logits"), _bf16(x, s.N * s.H, "x"),
-        _i32(placement, s.E, "placement"), _bf16(w_gate, s.E * s.I * s.H, "w_gate"),
-        _bf16(w_up, s.E * s.I * s.H, "w_up"), _bf16(w_down, s.E * s.H * s.I, "w_down"),
+        _i32(placement, s.E, "placement"), *_gate_up_w(s, w_gate, w_up), _down_w(s, w_down),
         _bf16(residual, s.N * s.H, "residual"), ctypes.byref(s.c()),
         _i32(topk_ids, s.R, "topk_ids"), _f32(topk_w, s.R, "topk_w"), _lay(layout, s),
         _bf16(xd, xd_rows * s.H, "xd"), _ptr(xe), _bf16(h, s.R * s.I, "h"),
@@ -447,16 +509,25 @@ def layout_launches(shape: Shape) -> int:
 class MoELayer:
     """Owns the device buffers of one layer shape (all allocated by torch) and
     runs moe_layer_forward on them.  Weights are bf16 tensors [E, I, H] (gate,
-    up) and [E, H, I] (down); placement int32 [E] or None."""
+    up) and [E, H, I] (down) when shape.weights is "row_major", or the packed
+    tensors of pack_weights (w_up None) when it is "packed"; placement int32
+    [E] or None."""
 
     def __init__(self, shape: Shape, w_gate, w_up, w_down, placement=None, device="cuda",
-                 shared=None, fuse_combine=False):
+                 shared=None, fuse_combine=False, pack=True):
         """shared: optional (w_gate_s [I_s, H], w_up_s [I_s, H], w_down_s [H, I_s])
         of a shared expert run on every token.  fuse_combine: run the down GEMM
         with the combine in its epilogue (moe_ffn_down_combine, fp32
-        accumulator) instead of moe_ffn_down + moe_combine."""
+        accumulator) instead of moe_ffn_down + moe_combine.  pack: copy
+        row-major weights once into the packed layout (moe_pack_weights) and
+        run the layer on that copy (the layer's shape becomes "packed"); the
+        results are bit-identical, the weight stream faster."""
         if fuse_combine and shared is not None:
             raise ValueError("the combine fused into the down GEMM adds no shared expert")
+        if pack and shape.weights == "row_major":
+            w_gate, w_down = pack_weights(shape, w_gate, w_up, w_down)
+            w_up = None
+            shape = dataclasses.replace(shape, weights="packed")
         self.shape = shape
         self.fuse_combine = fuse_combine
         self.w_gate, self.w_up, self.w_down = w_gate, w_up, w_down
@@ -706,9 +777,14 @@ class MicrobatchPipeline:
     order), so the results are bit-identical."""
 
     def __init__(self, shape: Shape, w_gate, w_up, w_down, placement=None, microbatch=2048,
-                 depth=2, shared=None, device="cuda"):
+                 depth=2, shared=None, device="cuda", pack=True):
+        """pack: as for MoELayer (one packed copy, shared by the buffer sets)."""
         if depth < 2:
             raise ValueError("the two-stream schedule needs at least two buffer sets")
+        if pack and shape.weights == "row_major":
+            w_gate, w_down = pack_weights(shape, w_gate, w_up, w_down)
+            w_up = None
+            shape = dataclasses.replace(shape, weights="packed")
         self.shape = shape
         self.mb = max(1, min(microbatch, shape.N))
         self.depth = depth

@@ -66,17 +66,40 @@ typedef enum {
     MOE_GEMM_CTA_PAIR = 2
 } moe_gemm_kernel;
 
+/* Layout of the routed experts' weights in every call that takes them
+ * (moe_shape.weights).
+ *  MOE_WEIGHTS_ROW_MAJOR  nn.Linear layout: w_gate, w_up bf16 [E, I, H];
+ *                         w_down bf16 [E, H, I].
+ *  MOE_WEIGHTS_PACKED     the tile-contiguous copies that moe_pack_weights
+ *                         writes: w_gate points to the packed gate/up weights
+ *                         (both matrices), w_up is not read (may be NULL), and
+ *                         w_down points to the packed down weights.  A GEMM
+ *                         then reads each 64-deep slice of a 256-row weight
+ *                         tile as one contiguous 32 KB block instead of 256
+ *                         strided 128-byte pieces, which lets the weight
+ *                         stream of an HBM-bound layer run closer to the DRAM's
+ *                         sequential read rate.  Results are bit-identical to
+ *                         the row-major form.
+ * The shared expert's weights (moe_shared_expert_ffn) are always row-major. */
+typedef enum {
+    MOE_WEIGHTS_ROW_MAJOR = 0,
+    MOE_WEIGHTS_PACKED = 1
+} moe_weight_layout;
+
 /* N tokens of width H; E experts, top-k; W ranks; SwiGLU intermediate width I;
  * dedup != 0 selects the deduplicating dispatcher ("Expert Coupling" Sec. V-A):
  * one row per distinct (token, rank) instead of one per (token, expert).
- * gemm: a moe_gemm_kernel value (0 = automatic choice); any other value is
- * refused with MOE_ERR_INVALID_ARG.  Every behaviour of the library is set by
- * these fields and the call's arguments: nothing is read from the
- * environment. */
+ * gemm: a moe_gemm_kernel value (0 = automatic choice); weights: a
+ * moe_weight_layout value (0 = row-major); any other value of either is
+ * refused with MOE_ERR_INVALID_ARG, and packed weights of more than 2^31 rows
+ * of 64 bf16 (256 GB) with MOE_ERR_UNSUPPORTED.  Every behaviour of the
+ * library is set by these fields and the call's arguments: nothing is read
+ * from the environment. */
 typedef struct {
     int32_t N, H, E, k, W, I;
     int32_t dedup;
     int32_t gemm;
+    int32_t weights;
 } moe_shape;
 
 /* Dispatch layout: caller-owned device arrays of int32, written by
@@ -117,6 +140,35 @@ typedef struct {
  * int32 is the error word); the calls keep it valid afterwards.  One workspace
  * must not be shared by calls running concurrently. */
 size_t moe_workspace_bytes(const moe_shape* shape);
+
+/* Bytes of the packed gate/up weights and of the packed down weights that
+ * moe_pack_weights writes for this shape (0 if the shape is invalid):
+ *   gate/up  E * ceil(I/128) * ceil(H/64) blocks of 256 x 64 bf16 (32 KB)
+ *   down     E * ceil(H/256) * ceil(I/64) blocks of 256 x 64 bf16 */
+size_t moe_packed_gate_up_bytes(const moe_shape* shape);
+size_t moe_packed_down_bytes(const moe_shape* shape);
+
+/* Copies row-major expert weights (w_gate, w_up bf16 [E, I, H]; w_down bf16
+ * [E, H, I]) into the layout of MOE_WEIGHTS_PACKED, on the device (a storage
+ * layout of this library: the gated MLP of FarSkip-Collective Sec. 2.1 is the
+ * same computation on either).  Block
+ * (e, b, q) sits at block index (e * NB + b) * KB + q and holds 256 rows of
+ * 64 bf16, row-major (128 bytes a row):
+ *   gate/up (NB = ceil(I/128), KB = ceil(H/64)): row r < 128 is
+ *     w_gate[e, 128b + r, 64q .. 64q + 63] and row 128 + r the same slice of
+ *     w_up[e, 128b + r, :], so one block is the 256-column operand slice of a
+ *     gate/up tile (128 gate and the matching 128 up columns);
+ *   down (NB = ceil(H/256), KB = ceil(I/64)): row r is
+ *     w_down[e, 256b + r, 64q .. 64q + 63];
+ * entries past the matrix (rows >= I or H, columns >= H or I) are zero.
+ * Pure copies, done once per set of weights (a reformat at load time, not a
+ * per-step cost).  gate_up_packed (moe_packed_gate_up_bytes) and down_packed
+ * (moe_packed_down_bytes) are device buffers that must not overlap the
+ * inputs; either may be NULL, and its inputs are then not read.
+ * shape->weights is not read.  Asynchronous on stream. */
+moe_status moe_pack_weights(const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                            const moe_shape* shape, uint16_t* gate_up_packed,
+                            uint16_t* down_packed, void* stream);
 
 /* Top-k routing ("Expert Coupling" Appendix A-A1, Table II: fp32 gate, top-k
  * of E; FarSkip-Collective Sec. 2.1: G is a sparse top-k selection).
@@ -167,8 +219,10 @@ moe_status moe_dispatch(const uint16_t* x, const moe_layout* layout, const moe_s
  * stages 4-6).  For every plain row i of expert e:
  *   h[i, :] = bf16( SiLU(x_i Wg[e]^T) * (x_i Wu[e]^T) )      bf16 [N*k, I]
  *   y[i, :] = bf16( h[i, :] Wd[e]^T )                          bf16 [N*k, H]
- * with fp32 accumulation on the tensor cores.  Weights in nn.Linear layout:
- * w_gate, w_up bf16 [E, I, H]; w_down bf16 [E, H, I].
+ * with fp32 accumulation on the tensor cores.  Weights in the layout that
+ * shape->weights names (moe_weight_layout): nn.Linear layout w_gate, w_up
+ * bf16 [E, I, H], w_down bf16 [E, H, I]; or packed, with w_up unused.  The
+ * same holds for every call below that takes expert weights.
  * Plain: xd holds the expert-major rows [N*k, H].
  * Dedup: xd holds the dedup rows; the gate/up GEMM reads them in expert-major
  *        order through layout->expand_src (the receiver's "group" step, done
@@ -263,8 +317,8 @@ moe_status moe_combine(const uint16_t* y, const float* topk_w, const moe_layout*
  * experts, reading x directly (no dispatch):
  *   h_s = bf16(SiLU(x Wg_s^T) * (x Wu_s^T))   bf16 [N, I_shared]
  *   y_s = bf16(h_s Wd_s^T)                    bf16 [N, H]
- * w_gate_s, w_up_s bf16 [I_shared, H]; w_down_s bf16 [H, I_shared];
- * I_shared % 8 == 0.  ws: the layer's workspace (a reserved corner holds this
+ * w_gate_s, w_up_s bf16 [I_shared, H]; w_down_s bf16 [H, I_shared], row-major
+ * whatever shape->weights says; I_shared % 8 == 0.  ws: the layer's workspace (a reserved corner holds this
  * call's tile counters). */
 moe_status moe_shared_expert_ffn(const uint16_t* x, const moe_shape* shape, int32_t I_shared,
                                  const uint16_t* w_gate_s, const uint16_t* w_up_s,

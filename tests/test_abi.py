@@ -151,6 +151,32 @@ def test_gemm_kernel_choice_is_an_argument(lib):
         moe.Shape(64, 128, 8, 2, 2, 64, gemm="fast").c()
 
 
+def test_weight_layout_field_and_packed_sizes(lib):
+    """shape.weights takes the moe_weight_layout values only; the packed sizes
+    are the block counts of the header's definition (gate/up: E * ceil(I/128)
+    * ceil(H/64) blocks, down: E * ceil(H/256) * ceil(I/64) blocks, 32 KB
+    each), whatever the field says; the packed calls accept w_up = NULL."""
+    bad = moe.MoeShape(300, 256, 8, 2, 4, 384, 0, 0, 2)
+    assert lib.moe_workspace_bytes(ctypes.byref(bad)) == 0
+    for weights in ("row_major", "packed"):
+        s = moe.Shape(300, 256, 8, 2, 4, 384, weights=weights)
+        assert moe.moe_workspace_bytes(s) > 0
+        assert moe.moe_packed_gate_up_bytes(s) == 8 * 3 * 4 * 32768
+        assert moe.moe_packed_down_bytes(s) == 8 * 1 * 6 * 32768
+    s = moe.Shape(4096, 7168, 256, 8, 8, 2048)
+    assert moe.moe_packed_gate_up_bytes(s) == 2 * 256 * 2048 * 7168 * 2  # no padding
+    assert moe.moe_packed_down_bytes(s) == 256 * 7168 * 2048 * 2
+    with pytest.raises(ValueError):
+        moe.Shape(64, 128, 8, 2, 2, 64, weights="tiled").c()
+    # packed weights of 2^31 rows of 64 bf16 or more are refused (32-bit TMA rows)
+    huge = moe.Shape(16, 65536, 1024, 2, 1, 65536, weights="packed")
+    assert moe.moe_workspace_bytes(huge) == 0
+    # a packed call needs no w_up: refused on the missing rows pointer, not on w_up
+    ok = moe.Shape(64, 128, 8, 2, 2, 64, weights="packed")
+    st = lib.moe_ffn_gate_up(None, None, ctypes.byref(ok.c()), None, None, None, None, 0, None)
+    assert st == 1
+
+
 def test_library_sources_read_no_environment():
     csrc = os.path.join(ROOT, "combine_warp_top_gb300", "csrc")
     for fn in os.listdir(csrc):
