@@ -491,6 +491,10 @@ def measure(args, wl, world, rank, headline=True):
     pack = args.weights == "packed"
     layer = moe.MoELayer(shape, w_gate, w_up, w_down, placement_d, shared=shared,
                          fuse_combine=fuse_combine, pack=pack)
+    if pack and not microbatch:
+        # the layer holds its packed copy; the row-major matrices can go
+        w_gate = w_up = w_down = None
+        torch.cuda.empty_cache()
 
     x_h = torch.from_numpy(synth.make_x(wl, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
     r_h = torch.from_numpy(synth.make_residual(wl, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
