@@ -58,8 +58,45 @@ __device__ __forceinline__ int take_max(uint32_t (&key)[VPL], int lane, uint32_t
     return (int)idx;
 }
 
+// One compare-exchange of a sorting network: position a ends with the larger
+// key, ties to the lower slot (the lower expert index of the lane).
+__device__ __forceinline__ void cex(uint32_t& ka, int& sa, uint32_t& kb, int& sb) {
+    const bool swap = kb > ka || (kb == ka && sb < sa);
+    const uint32_t k0 = swap ? kb : ka, k1 = swap ? ka : kb;
+    const int s0 = swap ? sb : sa, s1 = swap ? sa : sb;
+    ka = k0;
+    kb = k1;
+    sa = s0;
+    sb = s1;
+}
+
+// The lane's VPL (key, slot) pairs in descending key order (Batcher's
+// odd-even merge networks for 2, 4 and 8 entries).
+template <int VPL>
+__device__ __forceinline__ void sort_lane(uint32_t (&key)[VPL], int (&slot)[VPL]) {
+    if constexpr (VPL == 2) {
+        cex(key[0], slot[0], key[1], slot[1]);
+    } else if constexpr (VPL == 4) {
+        constexpr int net[5][2] = {{0, 1}, {2, 3}, {0, 2}, {1, 3}, {1, 2}};
+#pragma unroll
+        for (int c = 0; c < 5; ++c)
+            cex(key[net[c][0]], slot[net[c][0]], key[net[c][1]], slot[net[c][1]]);
+    } else if constexpr (VPL == 8) {
+        constexpr int net[19][2] = {{0, 1}, {2, 3}, {4, 5}, {6, 7}, {0, 2}, {1, 3}, {4, 6},
+                                    {5, 7}, {1, 2}, {5, 6}, {0, 4}, {1, 5}, {2, 6}, {3, 7},
+                                    {2, 4}, {3, 5}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+        for (int c = 0; c < 19; ++c)
+            cex(key[net[c][0]], slot[net[c][0]], key[net[c][1]], slot[net[c][1]]);
+    }
+}
+
 // kRenorm: weights are a softmax over the k selected logits; otherwise the
 // full softmax over all E logits, read at the selected experts.
+//
+// For E <= 256 (VPL <= 8) each lane first sorts its own slots, so a round
+// compares the lanes' heads only and the winner pops its head: the same
+// picks in the same order as take_max, with a shorter chain per round.
 template <int VPL, bool kRenorm>
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int N, int E,
                                                     int k, int32_t* __restrict__ ids,
@@ -81,12 +118,36 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
     // k <= E: every round finds a non-empty slot
     int my_id = -1;
     float my_val = 0.f;
-    for (int j = 0; j < k; ++j) {
-        uint32_t m;
-        const int idx = take_max<VPL>(key, lane, m);
-        if (lane == j) {
-            my_id = idx;
-            my_val = key_value(m);
+    if constexpr (VPL <= 8) {
+        int slot[VPL];
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) slot[i] = i;
+        sort_lane<VPL>(key, slot);
+        for (int j = 0; j < k; ++j) {
+            const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
+            const uint32_t cand = key[0] == m ? (uint32_t)(slot[0] * 32 + lane) : 0xffffffffu;
+            const uint32_t idx = __reduce_min_sync(0xffffffffu, cand);
+            if ((int)(idx & 31u) == lane) {
+#pragma unroll
+                for (int i = 0; i + 1 < VPL; ++i) {
+                    key[i] = key[i + 1];
+                    slot[i] = slot[i + 1];
+                }
+                key[VPL - 1] = 0;
+            }
+            if (lane == j) {
+                my_id = (int)idx;
+                my_val = key_value(m);
+            }
+        }
+    } else {
+        for (int j = 0; j < k; ++j) {
+            uint32_t m;
+            const int idx = take_max<VPL>(key, lane, m);
+            if (lane == j) {
+                my_id = idx;
+                my_val = key_value(m);
+            }
         }
     }
 
