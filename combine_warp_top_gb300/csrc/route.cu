@@ -200,18 +200,49 @@ __global__ void __launch_bounds__(256) route_sigmoid_kernel(const float* __restr
     }
     int my_id = -1;
     float my_s = 0.f;
-    for (int j = 0; j < k; ++j) {
-        uint32_t m;
-        const int idx = take_max<VPL>(key, lane, m);
-        // the winner's score, from the lane that holds it
-        float s_slot = 0.f;
+    if constexpr (VPL <= 8) {
+        // as in route_kernel: each lane sorts its slots once, rounds compare heads
+        int slot[VPL];
 #pragma unroll
-        for (int i = 0; i < VPL; ++i)
-            if (i == (idx >> 5)) s_slot = sc[i];
-        const float bs = __shfl_sync(0xffffffffu, s_slot, idx & 31);
-        if (lane == j) {
-            my_id = idx;
-            my_s = bs;
+        for (int i = 0; i < VPL; ++i) slot[i] = i;
+        sort_lane<VPL>(key, slot);
+        for (int j = 0; j < k; ++j) {
+            const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
+            const uint32_t cand = key[0] == m ? (uint32_t)(slot[0] * 32 + lane) : 0xffffffffu;
+            const uint32_t idx = __reduce_min_sync(0xffffffffu, cand);
+            // the winner's score, from the lane that holds it (its head slot)
+            float s_head = 0.f;
+#pragma unroll
+            for (int i = 0; i < VPL; ++i)
+                if (i == slot[0]) s_head = sc[i];
+            const float bs = __shfl_sync(0xffffffffu, s_head, (int)(idx & 31u));
+            if ((int)(idx & 31u) == lane) {
+#pragma unroll
+                for (int i = 0; i + 1 < VPL; ++i) {
+                    key[i] = key[i + 1];
+                    slot[i] = slot[i + 1];
+                }
+                key[VPL - 1] = 0;
+            }
+            if (lane == j) {
+                my_id = (int)idx;
+                my_s = bs;
+            }
+        }
+    } else {
+        for (int j = 0; j < k; ++j) {
+            uint32_t m;
+            const int idx = take_max<VPL>(key, lane, m);
+            // the winner's score, from the lane that holds it
+            float s_slot = 0.f;
+#pragma unroll
+            for (int i = 0; i < VPL; ++i)
+                if (i == (idx >> 5)) s_slot = sc[i];
+            const float bs = __shfl_sync(0xffffffffu, s_slot, idx & 31);
+            if (lane == j) {
+                my_id = idx;
+                my_s = bs;
+            }
         }
     }
     float sum = lane < k ? my_s : 0.f;
