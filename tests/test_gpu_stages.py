@@ -118,6 +118,29 @@ def test_layout_count_table_tails_and_parts(N, E, k, W, dedup, placed):
     check_layout(got, oracle.dispatch_layout(ids, ref_placement, E, W), shape)
 
 
+@pytest.mark.parametrize("dedup", [False, True])
+@pytest.mark.parametrize("name", ["ragged", "wide", "e256", "k32"])
+def test_layout_with_a_workspace_off_16_bytes(name, dedup):
+    """A workspace that starts 4 bytes past a 16-byte boundary: the count
+    tables cannot be copied in 16-byte pieces, so the layout takes its separate
+    scan launch; the tables must not change."""
+    wl = SMALL[name]
+    ids, _ = oracle.route(synth.make_logits(wl), wl.k)
+    shape = shape_of(wl, dedup)
+    want = run_layout(ids, None, shape)
+    n = moe.moe_workspace_bytes(shape)
+    big = torch.zeros(n + 16, dtype=torch.uint8, device="cuda")
+    ws = big[4:4 + n]
+    assert ws.data_ptr() % 16 == 4
+    lay = moe.Layout(shape)
+    moe.moe_dispatch_layout(dev_i32(ids), None, shape, lay, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_error(ws) == 0
+    for key, t in lay.tensors.items():
+        assert np.array_equal(t.cpu().numpy(), want[key]), key
+    check_layout(want, oracle.dispatch_layout(ids, np.arange(wl.E), wl.E, wl.W), shape)
+
+
 def test_layout_skewed_and_empty_experts():
     # every token on expert 5 and one of {0, 1}: most experts empty, one full
     N, E, k, W = 1000, 16, 2, 4
