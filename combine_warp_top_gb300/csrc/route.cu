@@ -91,12 +91,35 @@ __device__ __forceinline__ void sort_lane(uint32_t (&key)[VPL], int (&slot)[VPL]
     }
 }
 
+// One round over lanes whose slots are sorted (sort_lane): the largest head key
+// over the warp, ties to the lowest expert index (slot * 32 + lane); the
+// winning lane pops its head.  m receives the key, head this lane's head slot
+// before the round (the caller can read a per-slot value of the winner from
+// it).  The same picks in the same order as take_max.
+template <int VPL>
+__device__ __forceinline__ uint32_t take_head(uint32_t (&key)[VPL], int (&slot)[VPL], int lane,
+                                              uint32_t& m, int& head) {
+    m = __reduce_max_sync(0xffffffffu, key[0]);
+    head = slot[0];
+    const uint32_t cand = key[0] == m ? (uint32_t)(slot[0] * 32 + lane) : 0xffffffffu;
+    const uint32_t idx = __reduce_min_sync(0xffffffffu, cand);
+    if ((int)(idx & 31u) == lane) {
+#pragma unroll
+        for (int i = 0; i + 1 < VPL; ++i) {
+            key[i] = key[i + 1];
+            slot[i] = slot[i + 1];
+        }
+        key[VPL - 1] = 0;
+    }
+    return idx;
+}
+
 // kRenorm: weights are a softmax over the k selected logits; otherwise the
 // full softmax over all E logits, read at the selected experts.
 //
 // For E <= 256 (VPL <= 8) each lane first sorts its own slots, so a round
-// compares the lanes' heads only and the winner pops its head: the same
-// picks in the same order as take_max, with a shorter chain per round.
+// compares the lanes' heads only and the winner pops its head (take_head),
+// a shorter chain per round than take_max's scan of every slot.
 template <int VPL, bool kRenorm>
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int N, int E,
                                                     int k, int32_t* __restrict__ ids,
@@ -124,17 +147,9 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
         for (int i = 0; i < VPL; ++i) slot[i] = i;
         sort_lane<VPL>(key, slot);
         for (int j = 0; j < k; ++j) {
-            const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
-            const uint32_t cand = key[0] == m ? (uint32_t)(slot[0] * 32 + lane) : 0xffffffffu;
-            const uint32_t idx = __reduce_min_sync(0xffffffffu, cand);
-            if ((int)(idx & 31u) == lane) {
-#pragma unroll
-                for (int i = 0; i + 1 < VPL; ++i) {
-                    key[i] = key[i + 1];
-                    slot[i] = slot[i + 1];
-                }
-                key[VPL - 1] = 0;
-            }
+            uint32_t m;
+            int head;
+            const uint32_t idx = take_head<VPL>(key, slot, lane, m, head);
             if (lane == j) {
                 my_id = (int)idx;
                 my_val = key_value(m);
@@ -207,23 +222,15 @@ __global__ void __launch_bounds__(256) route_sigmoid_kernel(const float* __restr
         for (int i = 0; i < VPL; ++i) slot[i] = i;
         sort_lane<VPL>(key, slot);
         for (int j = 0; j < k; ++j) {
-            const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
-            const uint32_t cand = key[0] == m ? (uint32_t)(slot[0] * 32 + lane) : 0xffffffffu;
-            const uint32_t idx = __reduce_min_sync(0xffffffffu, cand);
+            uint32_t m;
+            int head;
+            const uint32_t idx = take_head<VPL>(key, slot, lane, m, head);
             // the winner's score, from the lane that holds it (its head slot)
             float s_head = 0.f;
 #pragma unroll
             for (int i = 0; i < VPL; ++i)
-                if (i == slot[0]) s_head = sc[i];
+                if (i == head) s_head = sc[i];
             const float bs = __shfl_sync(0xffffffffu, s_head, (int)(idx & 31u));
-            if ((int)(idx & 31u) == lane) {
-#pragma unroll
-                for (int i = 0; i + 1 < VPL; ++i) {
-                    key[i] = key[i + 1];
-                    slot[i] = slot[i + 1];
-                }
-                key[VPL - 1] = 0;
-            }
             if (lane == j) {
                 my_id = (int)idx;
                 my_s = bs;
