@@ -48,7 +48,7 @@ def parse_args(argv=None):
     p.add_argument("--weights", choices=["packed", "row_major"], default="packed",
                    help="expert weights as moe_pack_weights' tile-contiguous copy (packed once "
                         "before timing) or in nn.Linear layout")
-    p.add_argument("--gemm", choices=["auto", "single", "pair"], default="auto",
+    p.add_argument("--gemm", choices=["auto", "single", "pair", "fused"], default="auto",
                    help="grouped-GEMM kernel (the shape's gemm field)")
     p.add_argument("--placement-search", action="store_true",
                    help="place experts by the co-selection search before timing the layer")
@@ -106,6 +106,8 @@ def algorithmic(wl, R_d, fused_dispatch=False):
         "dispatch": dict(bytes=N * H * 2 + rows_d * H * 2),
         "gate_up": dict(bytes=2 * E * I * H * 2 + a_rows * H * 2 + R * I * 2, flops=4 * R * H * I),
         "down": dict(bytes=E * H * I * 2 + R * I * 2 + R * H * 2, flops=2 * R * H * I),
+        # both GEMMs in one kernel with h on chip: weights, the rows once, y out
+        "ffn": dict(bytes=3 * E * I * H * 2 + a_rows * H * 2 + R * H * 2, flops=6 * R * H * I),
         # dedup: the partial rows stay in registers (one-pass dedup combine)
         "combine": dict(bytes=R * H * 2 + 2 * N * H * 2 + R * 8),
         # down GEMM with the combine in its epilogue: weights, h in, residual
@@ -522,6 +524,7 @@ def measure(args, wl, world, rank, headline=True):
             pipe.forward(L_d, x_d, r_d, out=layer.out, gemm_events=gev[i])
 
     stages = layer.stage_names()
+    dom = dominant_stage(layer)
     # external events: inside a captured graph they become timing nodes.  The
     # headline's timed graph carries them around the dominant stage (gate/up)
     # only: a pair around every stage of every step cost 0.5-1.8% of the step
@@ -531,7 +534,7 @@ def measure(args, wl, world, rank, headline=True):
     # (instrumented_stage_ms).
     mk = lambda: (torch.cuda.Event(enable_timing=True, external=use_graph),  # noqa: E731
                   torch.cuda.Event(enable_timing=True, external=use_graph))
-    timed_stages = (["gate_up"] if headline else []) if use_graph else stages
+    timed_stages = ([dom] if headline else []) if use_graph else stages
     ev = [{s: mk() for s in timed_stages} for _ in range(args.steps)] if pipe is None else None
     gev = [[mk() for _ in range(n_mb)] for _ in range(args.steps)] if pipe is not None else None
     for i in range(args.warmup):
@@ -583,9 +586,10 @@ def measure(args, wl, world, rank, headline=True):
             alone_ms = stage_alone_ms(layer, L_d, x_d, r_d, stages, args.steps)
             runner.check_device_errors()
     else:
-        # gate/up launches of all microbatches of a step, on the GEMM stream
-        stage_ms = {"gate_up": statistics.mean(sum(a.elapsed_time(b) for a, b in g) for g in gev)}
-        stages = ["gate_up"]
+        # gate/up (or fused FFN) launches of all microbatches of a step, on the
+        # GEMM stream
+        stage_ms = {dom: statistics.mean(sum(a.elapsed_time(b) for a, b in g) for g in gev)}
+        stages = [dom]
 
     e2e = None
     if headline:
@@ -640,9 +644,10 @@ def measure(args, wl, world, rank, headline=True):
         stage_report[s] = d
 
     roof = roofline(wl, alg, stage_ms, pk, pk_src, ridge, layer, pipe, n_mb)
-    roof["timed"] = ("CUDA events around every gate/up launch of the timed region"
-                     if "gate_up" in timed_stages or pipe is not None else
-                     "CUDA events around every gate/up launch of an instrumented replay of the "
+    what = "fused FFN" if dom == "ffn" else "gate/up"
+    roof["timed"] = (f"CUDA events around every {what} launch of the timed region"
+                     if dom in timed_stages or pipe is not None else
+                     f"CUDA events around every {what} launch of an instrumented replay of the "
                      "same K steps (this workload's timed region carries no timing node)")
     res = {
         "value": round(wl.N * args.steps * world / (elapsed_ms / 1e3), 1),
@@ -682,9 +687,15 @@ def dispatch_rows(wl, shape, L_d, placement_d):
             "max_over_mean_expert_load": round(float(counts.max() / counts.mean()), 3)}
 
 
+def dominant_stage(layer):
+    """The stage of the layer's dominant kernel: the gate/up GEMM, or the fused
+    expert FFN where the layer runs both GEMMs as one kernel."""
+    return "ffn" if layer.fused_ffn else "gate_up"
+
+
 def roofline(wl, alg, stage_ms, pk, pk_src, ridge, layer, pipe, n_mb):
-    """The roofline object of the dominant kernel, the gate/up GEMM."""
-    dom = "gate_up"
+    """The roofline object of the dominant kernel (dominant_stage)."""
+    dom = dominant_stage(layer)
     a = alg[dom]
     if a["flops"] / a["bytes"] > ridge:
         achieved = a["flops"] / stage_ms[dom] / 1e9
@@ -695,12 +706,15 @@ def roofline(wl, alg, stage_ms, pk, pk_src, ridge, layer, pipe, n_mb):
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 3)
-    roof["traffic"] = recorded_traffic(wl)
+    roof["traffic"] = recorded_traffic(wl) if dom == "gate_up" else None
     if roof["frac"] > 1.0:
         roof["note"] = ("above 1: the peak is a copy probe (half its bytes writes); this kernel "
                         "mostly reads, and its DRAM traffic is at least its algorithmic bytes, "
                         "so no L2 hit inflates the figure")
-    if wl.dedup:
+    if dom == "ffn":
+        roof["kernel"] = ("fused_ffn_kernel (moe_ffn_fused: gate/up, SwiGLU and down in one "
+                          "kernel, h kept on chip, rows gathered by its own warps)")
+    elif wl.dedup:
         roof["kernel"] = ("grouped_gemm_kernel<SwiGLU, gathered rows> (moe_ffn_gate_up_gather: "
                           "the dedup expansion done by the GEMM's gather warps)")
     elif layer.fused_dispatch:

@@ -30,8 +30,9 @@ moe_status check_shape(const moe_shape* s) {
     if (s->H % 8 != 0 || s->I % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if ((long long)s->N * s->k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
     if (s->gemm != MOE_GEMM_AUTO && s->gemm != MOE_GEMM_SINGLE_CTA &&
-        s->gemm != MOE_GEMM_CTA_PAIR)
+        s->gemm != MOE_GEMM_CTA_PAIR && s->gemm != MOE_GEMM_FUSED)
         return MOE_ERR_INVALID_ARG;
+    if (s->gemm == MOE_GEMM_FUSED && !fused_ffn_supported(s->H)) return MOE_ERR_UNSUPPORTED;
     if (s->weights != MOE_WEIGHTS_ROW_MAJOR && s->weights != MOE_WEIGHTS_PACKED)
         return MOE_ERR_INVALID_ARG;
     // the GEMMs address packed rows with 32-bit TMA coordinates
@@ -68,9 +69,20 @@ inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK 
 // rows per expert the single-CTA 128-row tiles waste less.  The shape's gemm
 // field can name either kernel instead of the automatic choice.
 bool use_pair(long long R, int E, int32_t gemm) {
-    if (gemm == MOE_GEMM_SINGLE_CTA) return false;
+    if (gemm == MOE_GEMM_SINGLE_CTA || gemm == MOE_GEMM_FUSED) return false;
     if (gemm == MOE_GEMM_CTA_PAIR) return true;
     return R >= 512LL * E;
+}
+
+// moe_layer_forward runs the expert FFN as one kernel with h on chip when the
+// shape names it, and by default for H <= kAutoFusedMaxH: there it measured
+// faster than the two GEMMs on every shape tried (h never goes to HBM and one
+// launch goes), while at H = 256 the two GEMMs were faster on the
+// tensor-heavy shapes.
+constexpr int kAutoFusedMaxH = 128;
+bool layer_fuses_ffn(const moe_shape& s) {
+    return s.gemm == MOE_GEMM_FUSED ||
+           (s.gemm == MOE_GEMM_AUTO && s.H <= kAutoFusedMaxH && fused_ffn_supported(s.H));
 }
 
 // The routed experts' GEMM problem: the plain expert-major rows of the layout.
@@ -288,6 +300,29 @@ moe_status moe_ffn_down_combine(const uint16_t* h, const float* topk_w, const mo
     return cuda_status(launch_acc_finish(acc, residual, shape->N, shape->H, out, st));
 }
 
+moe_status moe_ffn_fused(const uint16_t* src, const int32_t* row_index, int64_t src_rows,
+                         const moe_layout* layout, const moe_shape* shape, const uint16_t* w_gate,
+                         const uint16_t* w_up, const uint16_t* w_down, uint16_t* y, void* ws,
+                         size_t ws_bytes, void* stream) {
+    MOE_RANGE();
+    MOE_TRY(check_shape(shape));
+    MOE_TRY(check_layout(layout, shape));
+    MOE_TRY(check_ws(shape, ws, ws_bytes));
+    if (!fused_ffn_supported(shape->H)) return MOE_ERR_UNSUPPORTED;
+    if (shape->N == 0) return MOE_OK;
+    if (!src || !w_gate || !up_given(shape, w_up) || !w_down || !y) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(src, w_gate, w_up, w_down, y)) return MOE_ERR_INVALID_ARG;
+    if (src_rows <= 0 || src_rows >= ((int64_t)1 << 31)) return MOE_ERR_INVALID_ARG;
+    // without an index the problem's rows are the first N*k rows of src
+    if (!row_index && src_rows < (int64_t)shape->N * shape->k) return MOE_ERR_INVALID_ARG;
+    return launch_ffn_fused(src, row_index, src_rows, routed_group(*layout, *shape, ws), shape->H,
+                            shape->I, w_gate, w_up, w_down, y, as_stream(stream));
+}
+
+int32_t moe_ffn_fused_supported(const moe_shape* shape) {
+    return shape && check_shape(shape) == MOE_OK && fused_ffn_supported(shape->H) ? 1 : 0;
+}
+
 moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const moe_shape* shape,
                           const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
                           uint16_t* xe, uint16_t* h, uint16_t* y, void* ws, size_t ws_bytes,
@@ -297,14 +332,20 @@ moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const mo
     MOE_TRY(check_layout(layout, shape));
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (shape->N == 0) return MOE_OK;
-    if (!xd || !w_gate || !up_given(shape, w_up) || !w_down || !h || !y)
+    const bool fused = shape->gemm == MOE_GEMM_FUSED;  // h stays on chip: not written
+    if (!xd || !w_gate || !up_given(shape, w_up) || !w_down || (!h && !fused) || !y)
         return MOE_ERR_INVALID_ARG;
     if (!aligned16(xd, w_gate, w_up, w_down, h, y)) return MOE_ERR_INVALID_ARG;
     (void)xe;
+    const int64_t rd_max = (int64_t)shape->N * (shape->k < shape->W ? shape->k : shape->W);
+    if (fused)
+        return shape->dedup ? moe_ffn_fused(xd, layout->expand_src, rd_max, layout, shape, w_gate,
+                                            w_up, w_down, y, ws, ws_bytes, stream)
+                            : moe_ffn_fused(xd, nullptr, (int64_t)shape->N * shape->k, layout,
+                                            shape, w_gate, w_up, w_down, y, ws, ws_bytes, stream);
     if (shape->dedup) {
         // the expansion to expert-major order is done by the GEMM's gather
         // warps: cheaper than writing the N*k rows out and reading them back
-        const int64_t rd_max = (int64_t)shape->N * (shape->k < shape->W ? shape->k : shape->W);
         MOE_TRY(moe_ffn_gate_up_gather(xd, layout->expand_src, rd_max, layout, shape, w_gate,
                                        w_up, h, ws, ws_bytes, stream));
     } else {
@@ -375,18 +416,30 @@ moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32
     MOE_TRY(check_layout(layout, shape));
     MOE_TRY(check_ws(shape, ws, ws_bytes));
     if (shape->N == 0) return MOE_OK;
+    const bool fused = layer_fuses_ffn(*shape);  // h stays on chip: not written
     if (!logits || !x || !w_gate || !up_given(shape, w_up) || !w_down || !topk_ids ||
-        !topk_w || !xd || !h || !y || !out)
+        !topk_w || !xd || (!h && !fused) || !y || !out)
         return MOE_ERR_INVALID_ARG;
     if (!aligned16(x, w_gate, w_up, w_down, residual, xd, xe, h, y, partial, out))
         return MOE_ERR_INVALID_ARG;
     MOE_TRY(moe_route(logits, shape, topk_ids, topk_w, stream));
     MOE_TRY(moe_dispatch_layout(topk_ids, placement, shape, layout, ws, ws_bytes, stream));
-    if (moe_layer_skips_dispatch(shape)) {
+    if (moe_layer_skips_dispatch(shape) && fused) {
+        // dispatch copy, both GEMMs and SwiGLU in one kernel: rows of x through row_token
+        MOE_TRY(moe_ffn_fused(x, layout->row_token, shape->N, layout, shape, w_gate, w_up, w_down,
+                              y, ws, ws_bytes, stream));
+    } else if (moe_layer_skips_dispatch(shape)) {
         // the dispatch copy fused into the gate/up GEMM: rows of x through row_token
         MOE_TRY(moe_ffn_gate_up_gather(x, layout->row_token, shape->N, layout, shape, w_gate,
                                        w_up, h, ws, ws_bytes, stream));
         MOE_TRY(moe_ffn_down(h, layout, shape, w_down, y, ws, ws_bytes, stream));
+    } else if (fused) {
+        // only the dedup form dispatches before the fused FFN: its dedup rows
+        // are expanded to expert-major order by the kernel's gather warps
+        MOE_TRY(moe_dispatch(x, layout, shape, xd, stream));
+        const int64_t rd_max = (int64_t)shape->N * (shape->k < shape->W ? shape->k : shape->W);
+        MOE_TRY(moe_ffn_fused(xd, layout->expand_src, rd_max, layout, shape, w_gate, w_up,
+                              w_down, y, ws, ws_bytes, stream));
     } else {
         MOE_TRY(moe_dispatch(x, layout, shape, xd, stream));
         MOE_TRY(moe_expert_ffn(xd, layout, shape, w_gate, w_up, w_down, xe, h, y, ws, ws_bytes,
@@ -395,8 +448,14 @@ moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32
     return moe_combine(y, topk_w, layout, shape, partial, residual, out, stream);
 }
 
+int32_t moe_layer_fuses_ffn(const moe_shape* shape) {
+    return shape && check_shape(shape) == MOE_OK && layer_fuses_ffn(*shape) ? 1 : 0;
+}
+
 int32_t moe_layer_skips_dispatch(const moe_shape* shape) {
     if (!shape || check_shape(shape) != MOE_OK || shape->dedup) return 0;
+    // the fused FFN gathers its plain rows from x itself
+    if (layer_fuses_ffn(*shape)) return 1;
     // plain rows are gathered when the single-CTA GEMM runs (the weight-streaming
     // regime, where fusing the copy saves its HBM traffic); the CTA-pair kernel
     // has no gather mode

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 SHAPE_FIELDS = ("N", "H", "E", "k", "W", "I", "dedup", "gemm", "weights")
 # moe_gemm_kernel values of include/moe.h
-GEMM_KERNELS = {"auto": 0, "single": 1, "pair": 2}
+GEMM_KERNELS = {"auto": 0, "single": 1, "pair": 2, "fused": 3}
 # moe_weight_layout values of include/moe.h
 WEIGHT_LAYOUTS = {"row_major": 0, "packed": 1}
 LAYOUT_FIELDS = ("expert_counts", "expert_offsets", "rank_offsets", "row_token", "pair_row",
@@ -71,12 +71,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_ffn_gate_up": (I32, [P, lay, shp, P, P, P, P, S, P]),
         "moe_ffn_down": (I32, [P, lay, shp, P, P, P, S, P]),
         "moe_ffn_gate_up_gather": (I32, [P, P, ctypes.c_int64, lay, shp, P, P, P, P, S, P]),
+        "moe_ffn_fused": (I32, [P, P, ctypes.c_int64, lay, shp, P, P, P, P, P, S, P]),
+        "moe_ffn_fused_supported": (ctypes.c_int32, [shp]),
         "moe_combine": (I32, [P, P, lay, shp, P, P, P, P]),
         "moe_ffn_down_combine": (I32, [P, P, lay, shp, P, P, P, P, P, S, P]),
         "moe_layer_forward": (I32, [P, P, P, P, P, P, P, shp, P, P, lay, P, P, P, P, P, P, P, S,
                                     P]),
         "moe_dispatch_layout_noalloc": (I32, [P, P, shp, lay, P]),
         "moe_layer_skips_dispatch": (ctypes.c_int32, [shp]),
+        "moe_layer_fuses_ffn": (ctypes.c_int32, [shp]),
         "moe_coselection": (I32, [P, shp, P, P, S, P]),
         "moe_shared_expert_ffn": (I32, [P, shp, ctypes.c_int32, P, P, P, P, P, P, S, P]),
         "moe_combine_shared": (I32, [P, P, lay, shp, P, P, P, P, P]),
@@ -178,8 +181,9 @@ class Shape:
     W: int
     I: int
     dedup: bool = False
-    # which grouped-GEMM kernel runs: "auto", "single" (128-row tiles, one CTA)
-    # or "pair" (256-row tiles on a 2-CTA cluster); see moe_gemm_kernel
+    # which grouped-GEMM kernel runs: "auto", "single" (128-row tiles, one CTA),
+    # "pair" (256-row tiles on a 2-CTA cluster) or "fused" (the whole expert
+    # FFN in one kernel with h on chip, H <= 256); see moe_gemm_kernel
     gemm: str = "auto"
     # layout of the expert weights the calls take: "row_major" (nn.Linear) or
     # "packed" (moe_pack_weights); see moe_weight_layout
@@ -382,6 +386,23 @@ def moe_ffn_gate_up_gather(src, row_index, layout: Layout, shape: Shape, w_gate,
            "moe_ffn_gate_up_gather")
 
 
+def moe_ffn_fused(src, row_index, layout: Layout, shape: Shape, w_gate, w_up, w_down, y, ws,
+                  stream=None):
+    """The expert FFN with h kept on chip: y for the problem's rows, row i
+    being src[row_index[i]] (row_index None: src[i]); src is [src_rows, H]."""
+    s = shape
+    src_rows = src.numel() // s.H
+    _check(load().moe_ffn_fused(_bf16(src, src_rows * s.H, "src"),
+                                _i32(row_index, s.R, "row_index"), src_rows, _lay(layout, s),
+                                ctypes.byref(s.c()), *_gate_up_w(s, w_gate, w_up),
+                                _down_w(s, w_down), _bf16(y, s.R * s.H, "y"), *_ws(ws),
+                                _stream(stream)), "moe_ffn_fused")
+
+
+def moe_ffn_fused_supported(shape: Shape) -> bool:
+    return bool(load().moe_ffn_fused_supported(ctypes.byref(shape.c())))
+
+
 def moe_ffn_down_combine(h, topk_w, layout: Layout, shape: Shape, w_down, residual, acc, out,
                          ws, stream=None):
     s = shape
@@ -396,6 +417,12 @@ def moe_layer_skips_dispatch(shape: Shape) -> bool:
     """True when the layer gathers its plain rows inside the gate/up GEMM
     (no moe_dispatch copy) for this shape."""
     return bool(load().moe_layer_skips_dispatch(ctypes.byref(shape.c())))
+
+
+def moe_layer_fuses_ffn(shape: Shape) -> bool:
+    """True when the layer runs its expert FFN as the one fused kernel
+    (moe_ffn_fused, h kept on chip) for this shape."""
+    return bool(load().moe_layer_fuses_ffn(ctypes.byref(shape.c())))
 
 
 def moe_ffn_down(h, layout: Layout, shape: Shape, w_down, y, ws, stream=None):
@@ -524,6 +551,8 @@ class MoELayer:
         results are bit-identical, the weight stream faster."""
         if fuse_combine and shared is not None:
             raise ValueError("the combine fused into the down GEMM adds no shared expert")
+        if fuse_combine and shape.gemm == "fused":
+            raise ValueError("the fused expert FFN has no down GEMM to put the combine in")
         if pack and shape.weights == "row_major":
             w_gate, w_down = pack_weights(shape, w_gate, w_up, w_down)
             w_up = None
@@ -546,6 +575,9 @@ class MoELayer:
         rows_d = shape.R_d_max if shape.dedup else shape.R
         # plain rows gathered inside the gate/up GEMM need no dispatch buffer
         self.fused_dispatch = moe_layer_skips_dispatch(shape)
+        # the expert FFN as one kernel (h on chip), unless the combine is to go
+        # into the down GEMM's epilogue
+        self.fused_ffn = moe_layer_fuses_ffn(shape) and not fuse_combine
         self.xd = torch.empty(1 if self.fused_dispatch else max(rows_d, 1), H, **bf)
         self.xe = None  # the dedup expansion happens inside the gate/up GEMM
         self.h = torch.empty(max(shape.R, 1), I, **bf)
@@ -581,7 +613,7 @@ class MoELayer:
             self.forward(logits, x, residual, out)
         return g
 
-    STAGES = ("route", "layout", "dispatch", "gate_up", "down", "shared", "combine",
+    STAGES = ("route", "layout", "dispatch", "gate_up", "ffn", "down", "shared", "combine",
               "down_combine")
 
     def stage_names(self):
@@ -589,10 +621,13 @@ class MoELayer:
         separate dispatch when the gate/up GEMM gathers the plain rows from x,
         no shared expert unless one is set."""
         fused = ("down_combine",) if self.fuse_combine else ("down", "combine")
+        # fused FFN: one "ffn" stage (moe_ffn_fused) instead of gate_up + down
+        ffn = ("ffn",) if self.fused_ffn else ("gate_up", "down")
         return [n for n in self.STAGES
                 if (n != "dispatch" or not self.fused_dispatch)
                 and (n != "shared" or self.shared is not None)
-                and (n not in ("down", "combine", "down_combine") or n in fused)]
+                and (n not in ("down", "combine", "down_combine") or n in fused)
+                and (n not in ("gate_up", "ffn", "down") or n in ffn)]
 
     def forward_stages(self, logits, x, residual=None, out=None, stream=None, events=None):
         """The same kernels as forward(), one C call per stage of the pages'
@@ -619,6 +654,8 @@ class MoELayer:
             moe_dispatch(x, self.layout, s, self.xd, st)
         elif name == "gate_up":
             self._gate_up(x, st)
+        elif name == "ffn":
+            self._ffn_fused(x, st)
         elif name == "down_combine":
             moe_ffn_down_combine(self.h, self.topk_w, self.layout, s, self.w_down, residual,
                                  self.acc, out, self.ws, st)
@@ -634,6 +671,19 @@ class MoELayer:
                 moe_combine(self.y, self.topk_w, self.layout, s, self.partial, residual, out, st)
         else:
             raise ValueError(f"unknown stage {name}")
+
+    def _ffn_fused(self, x, st):
+        """The expert FFN as moe_layer_forward runs it when it fuses the FFN:
+        one kernel, rows gathered like the gate/up stage's (dedup rows through
+        expand_src, plain rows of x through row_token)."""
+        s, lay = self.shape, self.layout
+        if s.dedup:
+            src, index = self.xd, lay["expand_src"]
+        elif self.fused_dispatch:
+            src, index = x, lay["row_token"]
+        else:
+            src, index = self.xd, None
+        moe_ffn_fused(src, index, lay, s, self.w_gate, self.w_up, self.w_down, self.y, self.ws, st)
 
     def _gate_up(self, x, st):
         """The gate/up stage as moe_layer_forward runs it: dedup rows expanded
@@ -660,7 +710,8 @@ class MoELayer:
         dispatch = 0 if self.fused_dispatch else 1
         # fused combine: GEMM + finish (the accumulator memset is a copy-engine op)
         down_combine = 2 if self.fuse_combine else 1 + 1
-        return 1 + layout_launches(s) + dispatch + 1 + down_combine + shared
+        gate_up = 0 if self.fused_ffn else 1  # the fused FFN is one launch with the down
+        return 1 + layout_launches(s) + dispatch + gate_up + down_combine + shared
 
     def forward_host(self, logits_h, x_h, residual_h, out_h, dev_inputs=None, stream=None):
         """Whole layer from host buffers: copy the step's inputs host->device,
@@ -845,7 +896,14 @@ class MicrobatchPipeline:
             mat.wait_event(a_done[m])
             if gemm_events is not None:
                 gemm_events[m][0].record(mat)
-            if s.dedup:
+            ffn_fused = moe_layer_fuses_ffn(sm)
+            if ffn_fused:
+                # the whole expert FFN in one kernel (h on chip)
+                src, index = ((L.xd, L.layout["expand_src"]) if s.dedup else
+                              (x[t0:t1], L.layout["row_token"]) if fused else (L.xd, None))
+                moe_ffn_fused(src, index, L.layout, sm, self.w[0], self.w[1], self.w[2], L.y,
+                              L.ws, mat)
+            elif s.dedup:
                 moe_ffn_gate_up_gather(L.xd, L.layout["expand_src"], L.layout, sm, self.w[0],
                                        self.w[1], L.h, L.ws, mat)
             elif fused:
@@ -855,7 +913,8 @@ class MicrobatchPipeline:
                 moe_ffn_gate_up(L.xd, L.layout, sm, self.w[0], self.w[1], L.h, L.ws, mat)
             if gemm_events is not None:
                 gemm_events[m][1].record(mat)
-            moe_ffn_down(L.h, L.layout, sm, self.w[2], L.y, L.ws, mat)
+            if not ffn_fused:
+                moe_ffn_down(L.h, L.layout, sm, self.w[2], L.y, L.ws, mat)
             if self.shared is not None:
                 moe_shared_expert_ffn(x[t0:t1], sm, L.I_shared, *self.shared, L.h_s, L.y_s,
                                       L.ws, mat)
@@ -878,6 +937,7 @@ class MicrobatchPipeline:
             s = self.shape
             sub = dataclasses.replace(s, N=t1 - t0)
             dispatch = 0 if moe_layer_skips_dispatch(sub) else 1
-            total += 1 + layout_launches(sub) + dispatch + 1 + 1 + 1 + (
+            ffn = 1 if moe_layer_fuses_ffn(sub) else 2  # one fused launch, or gate/up + down
+            total += 1 + layout_launches(sub) + dispatch + ffn + 1 + (
                 3 if self.shared is not None else 0)
         return total

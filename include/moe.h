@@ -49,21 +49,30 @@ typedef enum {
     MOE_ERR_DEVICE_ASSERT = 6  /* a device-side consistency check failed */
 } moe_status;
 
-/* Which tensor-core kernel runs the grouped GEMMs (moe_shape.gemm).  Both give
+/* Which tensor-core kernel runs the grouped GEMMs (moe_shape.gemm).  All give
  * the same results to fp32 accumulation order; they differ in speed only.
  *  MOE_GEMM_AUTO        the CTA-pair kernel when the problem has at least 512
  *                       rows per expert on average (N*k >= 512*E), else the
- *                       single-CTA kernel
+ *                       single-CTA kernel; moe_layer_forward, when H <= 128,
+ *                       runs the expert FFN as the fused kernel instead (as
+ *                       with MOE_GEMM_FUSED; moe_layer_fuses_ffn)
  *  MOE_GEMM_SINGLE_CTA  128-row tiles, one CTA each (cta_group::1); the only
  *                       kernel with a gather mode
  *  MOE_GEMM_CTA_PAIR    256-row tiles shared by a 2-CTA cluster (cta_group::2)
+ *  MOE_GEMM_FUSED       moe_expert_ffn and moe_layer_forward run the expert FFN
+ *                       as one kernel that keeps h on chip (moe_ffn_fused; h
+ *                       is not written and may be NULL there); the other GEMM
+ *                       calls run the single-CTA kernel.  Only for H <= 256:
+ *                       a shape with a larger H and this value is refused
+ *                       with MOE_ERR_UNSUPPORTED.
  * Calls that gather rows inside the GEMM (moe_ffn_gate_up_gather, the dedup
  * form of moe_expert_ffn) and moe_ffn_down_combine always run the single-CTA
  * kernel for their gathered / fused launch. */
 typedef enum {
     MOE_GEMM_AUTO = 0,
     MOE_GEMM_SINGLE_CTA = 1,
-    MOE_GEMM_CTA_PAIR = 2
+    MOE_GEMM_CTA_PAIR = 2,
+    MOE_GEMM_FUSED = 3
 } moe_gemm_kernel;
 
 /* Layout of the routed experts' weights in every call that takes them
@@ -229,6 +238,8 @@ moe_status moe_dispatch(const uint16_t* x, const moe_layout* layout, const moe_s
  *        by the GEMM's gather warps instead of a copy into xe).
  * xe is not used and may be NULL (kept so that callers of the materialised
  * form, moe_expand + moe_ffn_gate_up, can share one buffer set).
+ * shape->gemm == MOE_GEMM_FUSED: one moe_ffn_fused call (xd, through
+ * expand_src when dedup); h is not written and may be NULL.
  * ws: workspace of moe_workspace_bytes(shape) bytes. */
 moe_status moe_expert_ffn(const uint16_t* xd, const moe_layout* layout, const moe_shape* shape,
                           const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
@@ -291,6 +302,29 @@ moe_status moe_ffn_down_combine(const uint16_t* h, const float* topk_w, const mo
                                 const uint16_t* residual, float* acc, uint16_t* out, void* ws,
                                 size_t ws_bytes, void* stream);
 
+/* The expert FFN with h kept on chip (kernel-fusion page, "Fusing the layer
+ * into one kernel": the expert's intermediate activations stay in the SM's
+ * local memory between the two MatMuls).  One kernel computes, for every
+ * plain row i of expert e,
+ *   y[i, :] = bf16( bf16(SiLU(x_i Wg[e]^T) * (x_i Wu[e]^T)) Wd[e]^T )   bf16 [N*k, H]
+ * with x_i = src[row_index[i], :] (row_index NULL: src[i, :], i < N*k, and
+ * then src_rows >= N*k), src bf16 [src_rows, H], 0 < src_rows < 2^31; indices
+ * out of range read row 0.  h never leaves the SM: a 128-row tile's h is made
+ * 64 columns at a time into shared memory and consumed there by the down MMA,
+ * whose 128 x H fp32 accumulator stays in TMEM, which is why H <= 256 is
+ * required (MOE_ERR_UNSUPPORTED otherwise); I is not limited.  Same roundings
+ * and fp32 accumulation orders as moe_ffn_gate_up + moe_ffn_down.  With
+ * src = x and row_index = layout->row_token it includes the plain dispatch;
+ * with src = the dedup rows and row_index = layout->expand_src the dedup
+ * expansion.  Weights as shape->weights says. */
+moe_status moe_ffn_fused(const uint16_t* src, const int32_t* row_index, int64_t src_rows,
+                         const moe_layout* layout, const moe_shape* shape, const uint16_t* w_gate,
+                         const uint16_t* w_up, const uint16_t* w_down, uint16_t* y, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/* 1 when moe_ffn_fused accepts this shape (a valid shape with H <= 256), else 0. */
+int32_t moe_ffn_fused_supported(const moe_shape* shape);
+
 /* Combine (kernel-fusion page, "Expert parallelism: dispatch and combine" and
  * stage 7 "reduce"; residual add of FarSkip-Collective Sec. 3).
  * Plain: out[t, :] = bf16( residual[t, :] + sum_j topk_w[t, j] * y[pair_row[t, j], :] ),
@@ -339,7 +373,10 @@ moe_status moe_combine_shared(const uint16_t* y, const float* topk_w, const moe_
  * each of them -- except that, in the plain form, when
  * moe_layer_skips_dispatch(shape) is 1 the dispatch copy is fused into the
  * gate/up GEMM (moe_ffn_gate_up_gather(x, row_token)) and xd is not written.
- * xe is not used (may be NULL). */
+ * When moe_layer_fuses_ffn(shape) is 1 the expert FFN is moe_ffn_fused
+ * (plain: moe_ffn_fused(x, row_token), no dispatch copy; dedup:
+ * moe_ffn_fused(xd, expand_src) after moe_dispatch) and h is not written (may
+ * be NULL).  xe is not used (may be NULL). */
 moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32_t* placement,
                              const uint16_t* w_gate, const uint16_t* w_up,
                              const uint16_t* w_down, const uint16_t* residual,
@@ -349,11 +386,17 @@ moe_status moe_layer_forward(const float* logits, const uint16_t* x, const int32
                              size_t ws_bytes, void* stream);
 
 /* 1 when moe_layer_forward, for this shape, gathers the plain rows inside the
- * gate/up GEMM instead of running moe_dispatch first; 0 otherwise (dedup
- * form, or a shape whose GEMMs run on the CTA-pair kernel, which has no
- * gather mode).  A function of the shape alone (its gemm field included).
- * Lets a caller that runs the stages itself do the same. */
+ * gate/up GEMM (or inside the fused FFN) instead of running moe_dispatch
+ * first; 0 otherwise (dedup form, or a shape whose GEMMs run on the CTA-pair
+ * kernel, which has no gather mode).  A function of the shape alone (its gemm
+ * field included).  Lets a caller that runs the stages itself do the same. */
 int32_t moe_layer_skips_dispatch(const moe_shape* shape);
+
+/* 1 when moe_layer_forward, for this shape, runs the expert FFN as the one
+ * fused kernel (moe_ffn_fused: gemm MOE_GEMM_FUSED, or MOE_GEMM_AUTO with
+ * H <= 128), 0 when it runs the two GEMMs (or the shape is invalid).  A
+ * function of the shape alone. */
+int32_t moe_layer_fuses_ffn(const moe_shape* shape);
 
 /* Co-selection counts of "Expert Coupling" Sec. V-A / Appendix A-D Algorithm 1:
  * coselect[e*E + e'] = number of tokens whose topk_ids contain both e and e'

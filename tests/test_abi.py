@@ -2,6 +2,7 @@
 that include/moe.h declares; its host-side argument checks answer without
 touching the device."""
 import ctypes
+import dataclasses
 import os
 import re
 
@@ -132,7 +133,7 @@ def test_gemm_kernel_choice_is_an_argument(lib):
     outside moe_gemm_kernel are refused, and whether the layer fuses its plain
     dispatch into the gate/up GEMM follows from the field (no environment or
     other global state is consulted)."""
-    bad = moe.MoeShape(4096, 7168, 8, 2, 8, 2048, 0, 3)
+    bad = moe.MoeShape(4096, 7168, 8, 2, 8, 2048, 0, 4)
     assert lib.moe_workspace_bytes(ctypes.byref(bad)) == 0
     assert lib.moe_route(None, ctypes.byref(bad), None, None, None) == 1
     # 8192 rows over 8 experts: the automatic choice is the CTA-pair kernel,
@@ -149,6 +150,48 @@ def test_gemm_kernel_choice_is_an_argument(lib):
     assert not moe.moe_layer_skips_dispatch(moe.Shape(4096, 7168, 256, 8, 8, 2048, dedup=True))
     with pytest.raises(ValueError):
         moe.Shape(64, 128, 8, 2, 2, 64, gemm="fast").c()
+
+
+def test_fused_ffn_limits(lib):
+    """The fused expert FFN (h on chip) takes H <= 256 only: its 128 x H fp32 y
+    tile lives in TMEM next to the gate/up accumulators.  A shape that names
+    it with a larger H is refused as unsupported by every call; with it the
+    plain layer gathers its rows from x (no dispatch copy), the dedup layer
+    does not."""
+    assert moe.GEMM_KERNELS["fused"] == 3
+    for H in (8, 128, 200, 256):
+        s = moe.Shape(300, H, 8, 2, 4, 384, gemm="fused")
+        assert moe.moe_ffn_fused_supported(s)
+        assert moe.moe_workspace_bytes(s) > 0
+        assert moe.moe_layer_skips_dispatch(s)
+        assert not moe.moe_layer_skips_dispatch(dataclasses.replace(s, dedup=True))
+        # I is not limited
+        assert moe.moe_ffn_fused_supported(moe.Shape(300, H, 8, 2, 4, 14336))
+    # the layer fuses its FFN when the shape names the fused kernel, and by
+    # default for H <= 128; then it gathers plain rows from x itself,
+    # whichever kernel the separate GEMM calls would run
+    for gemm, H, want in (("auto", 128, True), ("auto", 8, True), ("auto", 136, False),
+                          ("auto", 256, False), ("fused", 256, True), ("auto", 264, False),
+                          ("auto", 7168, False), ("fused", 200, True), ("single", 128, False),
+                          ("pair", 128, False)):
+        s = moe.Shape(16384, H, 16, 4, 4, 1408, gemm=gemm)
+        assert moe.moe_layer_fuses_ffn(s) == want, (gemm, H)
+        assert moe.moe_layer_skips_dispatch(s) == (want or gemm == "single")
+    assert not moe.moe_layer_fuses_ffn(moe.Shape(64, 264, 8, 2, 2, 64, gemm="fused"))
+    wide = moe.Shape(300, 264, 8, 2, 4, 384, gemm="fused")
+    assert moe.moe_workspace_bytes(wide) == 0
+    assert lib.moe_route(None, ctypes.byref(wide.c()), None, None, None) == 2
+    assert not moe.moe_ffn_fused_supported(moe.Shape(300, 264, 8, 2, 4, 384))
+    assert not moe.moe_ffn_fused_supported(moe.Shape(4096, 7168, 256, 8, 8, 2048))
+    # refused on the host before anything is launched
+    s = moe.Shape(64, 128, 8, 2, 2, 64)
+    lay = moe.MoeLayout()
+    ws = ctypes.create_string_buffer(moe.moe_workspace_bytes(s))
+    big = moe.Shape(64, 264, 8, 2, 2, 64)
+    assert lib.moe_ffn_fused(None, None, 64, ctypes.byref(lay), ctypes.byref(big.c()), None, None,
+                             None, None, ws, len(ws), None) == 1  # empty layout first
+    assert lib.moe_ffn_fused(None, None, 64, None, ctypes.byref(s.c()), None, None, None, None,
+                             ws, len(ws), None) == 1
 
 
 def test_weight_layout_field_and_packed_sizes(lib):
