@@ -1,5 +1,6 @@
 """Parity of the whole layer on seeded random shapes: sizes, expert counts,
-rank counts, top-k, routing skew, dedup, placement, GEMM kernel and combine form
+rank counts, top-k, routing skew, dedup, placement, GEMM kernel (the fused
+expert FFN included where H <= 256) and combine form
 are drawn together, so that combinations no hand-picked case names are checked
 against the oracle too (ids, counts and R_d exactly, out within the layer's
 float tolerance).
@@ -37,8 +38,10 @@ def draw_case(i):
                         zipf_alpha=1.2 if logits == "zipf" else 0.0)
     dedup = bool(rng.random() < 0.5)
     placed = bool(rng.random() < 0.5) and E > 1
-    gemm = str(rng.choice(["auto", "single", "pair"]))
-    fuse = (not dedup) and bool(rng.random() < 0.25)
+    gemm = str(rng.choice(["auto", "single", "pair", "fused"]))
+    if gemm == "fused" and H > 256:  # the fused FFN keeps a 128 x H tile of y in TMEM
+        gemm = "auto"
+    fuse = (not dedup) and gemm != "fused" and bool(rng.random() < 0.25)
     residual = bool(rng.random() < 0.8)
     return wl, dedup, placed, gemm, fuse, residual
 
