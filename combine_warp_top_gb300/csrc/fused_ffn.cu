@@ -25,6 +25,10 @@
 // and u, 64-column k-blocks of h for y, 16-deep MMAs in order), and h is
 // rounded to bf16 the same way.
 //
+// This 64-column form runs for I < 1024; from I = 1024 on the wide form of
+// fused_ffn_wide.cu (128-column chunks, N = 256 gate/up MMAs) takes over,
+// whose stages are long enough that the one MMA-issuing thread keeps up.
+//
 // Roles (320 threads): warp 0 TMA-loads weight k-blocks into a ring (gate and
 // up halves of 64 rows, or the down k-block of round_up(H, 32) rows); warp 1
 // owns TMEM and issues tcgen05.mma; warps 2-5 turn g|u into h and drain y;
@@ -521,6 +525,9 @@ moe_status launch_ffn_fused(const uint16_t* src, const int32_t* row_index, long 
                             cudaStream_t st) {
     if (g.R == 0) return MOE_OK;
     if (!fused_ffn_supported(H)) return MOE_ERR_UNSUPPORTED;
+    // long I: 128-column chunks keep the tensor pipe ahead of the MMA thread
+    if (I >= kFusedWideMinI)
+        return launch_ffn_fused_wide(src, row_index, src_rows, g, H, I, wg, wu, wd, y, st);
     const SmemPlan plan = smem_plan(H);
     const int NY = y_cols(H);
     CUtensorMap mg, mu, md, my, unused;

@@ -190,12 +190,19 @@ moe_status launch_down_pair(const uint16_t* h, const GemmGroup& g, int H, int I,
 // The expert FFN in one kernel with h kept on chip (fused_ffn.cu): y for the
 // problem's rows, gathered like launch_gate_up's (row_index == nullptr: row i
 // of src).  Needs H <= kFusedMaxH (the 128 x H fp32 y tile lives in TMEM).
+// From I = kFusedWideMinI on, the form on 128-column chunks of I
+// (fused_ffn_wide.cu) runs instead of the 64-column one; same results.
 constexpr int kFusedMaxH = 256;
+constexpr int kFusedWideMinI = 1024;
 bool fused_ffn_supported(int H);
 moe_status launch_ffn_fused(const uint16_t* src, const int32_t* row_index, long long src_rows,
                             const GemmGroup& g, int H, int I, const uint16_t* wg,
                             const uint16_t* wu, const uint16_t* wd, uint16_t* y,
                             cudaStream_t st);
+moe_status launch_ffn_fused_wide(const uint16_t* src, const int32_t* row_index,
+                                 long long src_rows, const GemmGroup& g, int H, int I,
+                                 const uint16_t* wg, const uint16_t* wu, const uint16_t* wd,
+                                 uint16_t* y, cudaStream_t st);
 
 int sm_count();
 

@@ -1,7 +1,8 @@
 """The expert FFN with h kept on chip (moe_ffn_fused, gemm "fused"): the layer
 against the oracle's forward pass, and y bit for bit against the two-kernel
 path (same h rounding, same fp32 accumulation orders), on every small shape
-with H <= 256, plain and dedup, row-major and packed weights; a shape with
+with H <= 256 and on ragged I >= 1024 (the wide, 128-column-chunk form),
+plain and dedup, row-major and packed weights; a shape with
 several tiles per CTA and many chunks of I checked on every (expert, 128-row
 tile) and on every segment's last row; the direct call on materialised rows
 and through an index; the microbatch pipeline."""
@@ -55,6 +56,30 @@ def test_fused_layer_against_oracle_and_two_kernels(name, dedup, pack):
     assert np.array_equal(fused.topk_ids.view(wl.N, wl.k).cpu().numpy(), ref["topk_ids"])
     assert_close(host_f64(out), ref["out"], f"{name} fused out")
     single, out_s = run_layer(wl, w, "single", dedup, pack, pl)
+    R = wl.N * wl.k
+    assert np.array_equal(host_u16(fused.y[:R]), host_u16(single.y[:R])), "y"
+    assert torch.equal(out.view(torch.int16), out_s.view(torch.int16))
+
+
+# I >= 1024 runs the wide form (128-column chunks of I): ragged I with an odd
+# number of 64-column down k-blocks (1032: the last chunk has one), a partial
+# last chunk (1096), H = 256 (three ring stages) and a small H
+WIDE = [synth.Workload("wide_i1032", 300, 200, 8, 2, 1032, 4),
+        synth.Workload("wide_i1096", 257, 256, 6, 3, 1096, 3),
+        synth.Workload("wide_i1408_h64", 500, 64, 16, 4, 1408, 4)]
+
+
+@pytest.mark.parametrize("pack", [False, True])
+@pytest.mark.parametrize("dedup", [False, True])
+@pytest.mark.parametrize("wl", WIDE, ids=lambda w: w.name)
+def test_fused_wide_form_against_oracle_and_two_kernels(wl, dedup, pack):
+    wh = [synth.make_weight(wl, m) for m in ("gate", "up", "down")]
+    w = [dev_bf16(a) for a in wh]
+    fused, out = run_layer(wl, w, "fused", dedup, pack)
+    ref = oracle.layer_forward(synth.make_logits(wl), synth.make_x(wl), *wh, wl.k, wl.W,
+                               residual=synth.make_residual(wl), dedup=dedup)
+    assert_close(host_f64(out), ref["out"], f"{wl.name} fused out")
+    single, out_s = run_layer(wl, w, "single", dedup, pack)
     R = wl.N * wl.k
     assert np.array_equal(host_u16(fused.y[:R]), host_u16(single.y[:R])), "y"
     assert torch.equal(out.view(torch.int16), out_s.view(torch.int16))
