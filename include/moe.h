@@ -310,10 +310,11 @@ moe_status moe_ffn_down_combine(const uint16_t* h, const float* topk_w, const mo
  * with x_i = src[row_index[i], :] (row_index NULL: src[i, :], i < N*k, and
  * then src_rows >= N*k), src bf16 [src_rows, H], 0 < src_rows < 2^31; indices
  * out of range read row 0.  h never leaves the SM: a 128-row tile's h is made
- * 64 columns at a time into shared memory and consumed there by the down MMA,
- * whose 128 x H fp32 accumulator stays in TMEM, which is why H <= 256 is
- * required (MOE_ERR_UNSUPPORTED otherwise); I is not limited.  Same roundings
- * and fp32 accumulation orders as moe_ffn_gate_up + moe_ffn_down.  With
+ * 64 columns at a time (128 from I = 1024 on) into shared memory and consumed
+ * there by the down MMA, whose 128 x H fp32 accumulator stays in TMEM, which is
+ * why H <= 256 is required (MOE_ERR_UNSUPPORTED otherwise); I is not limited.
+ * Same roundings and fp32 accumulation orders as moe_ffn_gate_up +
+ * moe_ffn_down: y is bit-identical to theirs.  With
  * src = x and row_index = layout->row_token it includes the plain dispatch;
  * with src = the dedup rows and row_index = layout->expand_src the dedup
  * expansion.  Weights as shape->weights says. */
