@@ -75,14 +75,16 @@ bool use_pair(long long R, int E, int32_t gemm) {
 }
 
 // moe_layer_forward runs the expert FFN as one kernel with h on chip when the
-// shape names it, and by default for H <= kAutoFusedMaxH: there it measured
-// faster than the two GEMMs on every shape tried (h never goes to HBM and one
-// launch goes), while at H = 256 the two GEMMs were faster on the
-// tensor-heavy shapes.
-constexpr int kAutoFusedMaxH = 128;
+// shape names it, and by default for H <= 128, and for H <= 256 in the plain
+// form: there it measured faster than the two GEMMs on all but two of the
+// shapes tried (h never goes to HBM and one launch goes); on dedup layers
+// with H = 256 the two GEMMs (gathered gate/up) were faster.
+constexpr int kAutoFusedMaxH = 128;        // any form
+constexpr int kAutoFusedMaxHPlain = 256;   // the plain form
 bool layer_fuses_ffn(const moe_shape& s) {
-    return s.gemm == MOE_GEMM_FUSED ||
-           (s.gemm == MOE_GEMM_AUTO && s.H <= kAutoFusedMaxH && fused_ffn_supported(s.H));
+    if (s.gemm == MOE_GEMM_FUSED) return true;
+    if (s.gemm != MOE_GEMM_AUTO || !fused_ffn_supported(s.H)) return false;
+    return s.H <= (s.dedup ? kAutoFusedMaxH : kAutoFusedMaxHPlain);
 }
 
 // The routed experts' GEMM problem: the plain expert-major rows of the layout.

@@ -168,16 +168,20 @@ def test_fused_ffn_limits(lib):
         # I is not limited
         assert moe.moe_ffn_fused_supported(moe.Shape(300, H, 8, 2, 4, 14336))
     # the layer fuses its FFN when the shape names the fused kernel, and by
-    # default for H <= 128; then it gathers plain rows from x itself,
-    # whichever kernel the separate GEMM calls would run
-    for gemm, H, want in (("auto", 128, True), ("auto", 8, True), ("auto", 136, False),
-                          ("auto", 256, False), ("fused", 256, True), ("auto", 264, False),
+    # default for H <= 256 (plain form; dedup: H <= 128); then it gathers
+    # plain rows from x itself, whichever kernel the separate GEMM calls would run
+    for gemm, H, want in (("auto", 128, True), ("auto", 8, True), ("auto", 136, True),
+                          ("auto", 256, True), ("fused", 256, True), ("auto", 264, False),
                           ("auto", 7168, False), ("fused", 200, True), ("single", 128, False),
                           ("pair", 128, False)):
         s = moe.Shape(16384, H, 16, 4, 4, 1408, gemm=gemm)
         assert moe.moe_layer_fuses_ffn(s) == want, (gemm, H)
         assert moe.moe_layer_skips_dispatch(s) == (want or gemm == "single")
     assert not moe.moe_layer_fuses_ffn(moe.Shape(64, 264, 8, 2, 2, 64, gemm="fused"))
+    # dedup layers fuse by default only up to H = 128
+    assert moe.moe_layer_fuses_ffn(moe.Shape(300, 128, 8, 2, 4, 384, dedup=True))
+    assert not moe.moe_layer_fuses_ffn(moe.Shape(300, 136, 8, 2, 4, 384, dedup=True))
+    assert moe.moe_layer_fuses_ffn(moe.Shape(300, 256, 8, 2, 4, 384, dedup=True, gemm="fused"))
     wide = moe.Shape(300, 264, 8, 2, 4, 384, gemm="fused")
     assert moe.moe_workspace_bytes(wide) == 0
     assert lib.moe_route(None, ctypes.byref(wide.c()), None, None, None) == 2

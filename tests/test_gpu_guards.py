@@ -185,7 +185,7 @@ def test_layer_forward_stays_in_bounds(wl, dedup, gemm):
         # the plain rows were gathered inside the GEMM: xd is never written
         assert outs["xd"].untouched(0, shape.R * shape.H)
     if moe.moe_layer_fuses_ffn(shape):
-        # the fused expert FFN (the default for H <= 128) keeps h on chip
+        # the fused expert FFN (the default for small H) keeps h on chip
         assert outs["h"].untouched(0, outs["h"].n)
     for n in ("xe", "partial", "acc"):
         assert outs[n].untouched(0, outs[n].n), n

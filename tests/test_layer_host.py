@@ -18,21 +18,26 @@ def layer(shape, fuse_combine=False, shared=None):
 
 
 @pytest.mark.parametrize("shape,stages", [
-    # H <= 128: the expert FFN is the one fused kernel, plain rows gathered from x
+    # small H: the expert FFN is the one fused kernel, plain rows gathered from x
     (moe.Shape(64, 128, 8, 2, 2, 256), ["route", "layout", "ffn", "combine"]),
     # dedup: the dedup rows are dispatched first, then expanded by the fused kernel
     (moe.Shape(64, 128, 8, 2, 2, 256, dedup=True),
      ["route", "layout", "dispatch", "ffn", "combine"]),
-    # H > 128, few rows per expert: single-CTA GEMMs, dispatch fused into gate/up
+    # H > 256, few rows per expert: single-CTA GEMMs, dispatch fused into gate/up
     (moe.Shape(4096, 7168, 256, 8, 8, 2048), ["route", "layout", "gate_up", "down", "combine"]),
+    # H <= 256 without dedup: fused by default; with dedup only up to H = 128
+    (moe.Shape(300, 256, 8, 2, 4, 384), ["route", "layout", "ffn", "combine"]),
+    (moe.Shape(300, 256, 8, 2, 4, 384, dedup=True),
+     ["route", "layout", "dispatch", "gate_up", "down", "combine"]),
     # many rows per expert: the CTA-pair GEMMs, which have no gather mode
     (moe.Shape(8192, 4096, 8, 2, 8, 14336),
      ["route", "layout", "dispatch", "gate_up", "down", "combine"]),
     # the two GEMMs named explicitly at H = 128
     (moe.Shape(64, 128, 8, 2, 2, 256, gemm="single"),
      ["route", "layout", "gate_up", "down", "combine"]),
-    # the fused kernel named explicitly at H = 256 (not the default there)
-    (moe.Shape(300, 256, 8, 2, 4, 384, gemm="fused"), ["route", "layout", "ffn", "combine"]),
+    # the fused kernel named explicitly on a dedup layer at H = 256
+    (moe.Shape(300, 256, 8, 2, 4, 384, dedup=True, gemm="fused"),
+     ["route", "layout", "dispatch", "ffn", "combine"]),
 ])
 def test_stages_follow_the_library(shape, stages):
     lay = layer(shape)
