@@ -59,6 +59,21 @@ def test_algorithmic_bytes_of_the_deepseek_layer():
                                          32768 * 2048 * 2)
 
 
+def test_algorithmic_bytes_of_the_fused_ffn_and_its_roofline_stage():
+    """The fused expert FFN's algorithmic bytes: all three weight matrices, the
+    rows it gathers once (x when plain, the dedup rows when dedup) and y out;
+    h, which never leaves the SM, is not counted.  Where the layer fuses the
+    FFN, the roofline object describes that kernel."""
+    import types
+    wl = bench.workload(bench.parse_args(["--workload", "tiny"]))
+    E, H, I, N, k = wl.E, wl.H, wl.I, wl.N, wl.k
+    alg = bench.algorithmic(wl, R_d=0, fused_dispatch=True)
+    assert alg["ffn"]["bytes"] == 3 * E * I * H * 2 + N * H * 2 + N * k * H * 2
+    assert alg["ffn"]["flops"] == alg["gate_up"]["flops"] + alg["down"]["flops"]
+    assert bench.dominant_stage(types.SimpleNamespace(fused_ffn=True)) == "ffn"
+    assert bench.dominant_stage(types.SimpleNamespace(fused_ffn=False)) == "gate_up"
+
+
 def test_workload_overrides():
     wl = bench.workload(bench.parse_args(["--tokens", "512", "--experts", "32"]))
     assert (wl.N, wl.E, wl.W, wl.H) == (512, 32, 8, 7168)
