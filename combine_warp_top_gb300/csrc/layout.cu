@@ -8,8 +8,8 @@
 // expert IDs) and Appendix A-A2 (the receiver expands rows to expert-major
 // order).
 //
-// Two launches (three when the count tables exceed kScanTableBytes), all
-// deterministic:
+// Two launches (three when the count tables exceed kScanTableBytes, one when
+// all tokens fit one block of 256), all deterministic:
 //  1. count:   per block of 256 tokens, one 32-bit mask per (warp, slot) and
 //              per (warp, rank) records which lanes (tokens) hit it; the block
 //              count of a key is the sum of the popcounts.  OR-ing the rank
@@ -24,7 +24,9 @@
 //              base plus the popcount of the lower lanes' bits, so tokens
 //              ascend inside every segment exactly as in a stable sort.
 //     With larger tables a one-block scan launch between the two turns the
-//     table into bases once, and the scatter blocks read theirs.
+//     table into bases once, and the scatter blocks read theirs.  With one
+//     block (N <= 256) the scatter block's own masks are the whole table, so
+//     it counts them itself and the count launch is skipped.
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 
@@ -355,12 +357,15 @@ __device__ void block_bases(const int32_t* tab, int nb, int ncol, int* col_base,
 
 // scan_here: derive this block's bases from the whole count table (copied
 // into shared memory after the masks) instead of reading the bases that a
-// separate scan launch wrote.
+// separate scan launch wrote.  self_count (a grid of one block, with
+// scan_here): the table is this block's own mask popcounts, no count launch
+// ran, and the invalid ids / placement it would have reported are reported
+// here (err).
 __global__ void __launch_bounds__(kThreads) layout_scatter_kernel(
     const int32_t* __restrict__ ids, const int32_t* __restrict__ placement, int N, int E, int k,
     int W, int dedup, const int32_t* __restrict__ blk_counts,
     const int32_t* __restrict__ blk_rcounts, const int32_t* __restrict__ slot_start, moe_layout L,
-    int scan_here) {
+    int scan_here, int self_count, int* err) {
     extern __shared__ uint32_t sm[];
     __shared__ ScanSmem ss;
     const Smem s = carve(sm, E, W);
@@ -372,7 +377,7 @@ __global__ void __launch_bounds__(kThreads) layout_scatter_kernel(
     const int nb = gridDim.x;
     int32_t* tab = reinterpret_cast<int32_t*>(sm + table_offset_words(E, W));  // [nb][E]
     int32_t* rtab = tab + padded_table_words(nb, E);                            // [nb][W]
-    if (scan_here) {
+    if (scan_here && !self_count) {
         const int nE = nb * E, nW = dedup ? nb * W : 0;
         const uint32_t t0 = ptx::smem_u32(tab), r0 = ptx::smem_u32(rtab);
         for (int i = threadIdx.x; 4 * i < nE; i += blockDim.x)
@@ -380,12 +385,32 @@ __global__ void __launch_bounds__(kThreads) layout_scatter_kernel(
         for (int i = threadIdx.x; 4 * i < nW; i += blockDim.x)
             ptx::cp_async_16(r0 + 16u * i, blk_rcounts + 4 * i, 4u * min(4, nW - 4 * i));
     }
-    build_slot_of(s.slot_of, placement, E, nullptr);  // errors were reported by the count pass
-    build_masks(s, ids_t, N, E, k, W, dedup, nullptr);
+    // errors were reported by the count pass, unless there was none
+    int* const perr = self_count ? err : nullptr;
+    build_slot_of(s.slot_of, placement, E, perr);
+    build_masks(s, ids_t, N, E, k, W, dedup, perr);
     int* col_base = ss.part_sums;  // first row of this block's part of each slot / rank
     const int per_rank = E / W;
     if (scan_here) {
-        ptx::cp_async_wait_all();
+        if (self_count) {
+            // the only block: its mask popcounts are the count table
+            for (int p = threadIdx.x; p < E; p += blockDim.x) {
+                int c = 0;
+#pragma unroll
+                for (int w = 0; w < kLayoutWarps; ++w) c += __popc(s.mask[w * E + p]);
+                tab[p] = c;
+            }
+            if (dedup) {
+                for (int r = threadIdx.x; r < W; r += blockDim.x) {
+                    int c = 0;
+#pragma unroll
+                    for (int w = 0; w < kLayoutWarps; ++w) c += __popc(s.rmask[w * W + r]);
+                    rtab[r] = c;
+                }
+            }
+        } else {
+            ptx::cp_async_wait_all();
+        }
         __syncthreads();
         block_bases(tab, nb, E, col_base, ss);
         if (blockIdx.x == 0) {
@@ -489,6 +514,8 @@ cudaError_t launch_layout(const int32_t* ids, const int32_t* placement, const mo
     const bool aligned = ((reinterpret_cast<uintptr_t>(blk_counts) |
                            reinterpret_cast<uintptr_t>(blk_rcounts)) & 15u) == 0;
     const bool scan_here = nb > 0 && table <= kScanTableBytes && aligned;
+    // one block: it counts its own masks (no count launch)
+    const bool self_count = scan_here && nb == 1;
     const size_t scatter_smem =
         scan_here ? sizeof(int32_t) * table_offset_words(s.E, s.W) + table : smem;
     cudaError_t e;
@@ -502,7 +529,7 @@ cudaError_t launch_layout(const int32_t* ids, const int32_t* placement, const mo
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scatter_smem);
         if (e != cudaSuccess) return e;
     }
-    if (nb > 0) {
+    if (nb > 0 && !self_count) {
         layout_count_kernel<<<nb, kThreads, smem, st>>>(ids, placement, s.N, s.E, s.k, s.W,
                                                         s.dedup, blk_counts, blk_rcounts, err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -515,7 +542,7 @@ cudaError_t launch_layout(const int32_t* ids, const int32_t* placement, const mo
     if (nb > 0) {
         layout_scatter_kernel<<<nb, kThreads, scatter_smem, st>>>(
             ids, placement, s.N, s.E, s.k, s.W, s.dedup, blk_counts, blk_rcounts, slot_start, L,
-            scan_here ? 1 : 0);
+            scan_here ? 1 : 0, self_count ? 1 : 0, err);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -78,13 +78,18 @@ bool use_pair(long long R, int E, int32_t gemm) {
 // shape names it, and by default for H <= 128, and for H <= 256 in the plain
 // form: there it measured faster than the two GEMMs on all but two of the
 // shapes tried (h never goes to HBM and one launch goes); on dedup layers
-// with H = 256 the two GEMMs (gathered gate/up) were faster.
+// with H = 256 the two GEMMs (gathered gate/up) were faster.  One CTA walks
+// all of I for its 128-row tile, so a layer with few rows and a long I
+// (N*k < 4096 rows and I > 256) keeps the two GEMMs, which spread over I.
 constexpr int kAutoFusedMaxH = 128;        // any form
 constexpr int kAutoFusedMaxHPlain = 256;   // the plain form
+constexpr long long kAutoFusedMinRows = 4096;
+constexpr int kAutoFusedShortI = 256;
 bool layer_fuses_ffn(const moe_shape& s) {
     if (s.gemm == MOE_GEMM_FUSED) return true;
     if (s.gemm != MOE_GEMM_AUTO || !fused_ffn_supported(s.H)) return false;
-    return s.H <= (s.dedup ? kAutoFusedMaxH : kAutoFusedMaxHPlain);
+    if (s.H > (s.dedup ? kAutoFusedMaxH : kAutoFusedMaxHPlain)) return false;
+    return (long long)s.N * s.k >= kAutoFusedMinRows || s.I <= kAutoFusedShortI;
 }
 
 // The routed experts' GEMM problem: the plain expert-major rows of the layout.

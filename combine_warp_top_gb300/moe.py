@@ -522,9 +522,10 @@ def layout_launches(shape: Shape) -> int:
     of 256 tokens and slot, and per block and rank with dedup, each rounded
     up to 16 bytes) exceed the 64 KB that each scatter block scans itself
     (csrc/layout.cu, kScanTableBytes; workspaces from this module are
-    256-byte aligned, as the in-shared-memory scan needs)."""
+    256-byte aligned, as the in-shared-memory scan needs); the scatter alone
+    when one block of 256 tokens holds them all."""
     nb = (shape.N + 255) // 256
-    if nb == 0:
+    if nb <= 1:
         return 1
     pad4 = lambda n: (n + 3) // 4 * 4  # noqa: E731
     table = 4 * (pad4(nb * shape.E) + (pad4(nb * shape.W) if shape.dedup else 0))
@@ -700,7 +701,7 @@ class MoELayer:
             moe_ffn_gate_up(self.xd, lay, s, self.w_gate, self.w_up, self.h, self.ws, st)
 
     def kernel_launches_per_step(self) -> int:
-        """Kernels of this library launched by one forward (route 1, layout 2 or
+        """Kernels of this library launched by one forward (route 1, layout 1 to
         3, dispatch 1 unless fused into the gate/up GEMM, each GEMM 1, combine 1,
         shared expert 3)."""
         s = self.shape

@@ -54,9 +54,9 @@ typedef enum {
  *  MOE_GEMM_AUTO        the CTA-pair kernel when the problem has at least 512
  *                       rows per expert on average (N*k >= 512*E), else the
  *                       single-CTA kernel; moe_layer_forward, when H <= 128
- *                       (H <= 256 without dedup), runs the expert FFN as the
- *                       fused kernel instead (as with MOE_GEMM_FUSED;
- *                       moe_layer_fuses_ffn)
+ *                       (H <= 256 without dedup) and N*k >= 4096 or
+ *                       I <= 256, runs the expert FFN as the fused kernel
+ *                       instead (as with MOE_GEMM_FUSED; moe_layer_fuses_ffn)
  *  MOE_GEMM_SINGLE_CTA  128-row tiles, one CTA each (cta_group::1); the only
  *                       kernel with a gather mode
  *  MOE_GEMM_CTA_PAIR    256-row tiles shared by a 2-CTA cluster (cta_group::2)
@@ -396,8 +396,9 @@ int32_t moe_layer_skips_dispatch(const moe_shape* shape);
 
 /* 1 when moe_layer_forward, for this shape, runs the expert FFN as the one
  * fused kernel (moe_ffn_fused: gemm MOE_GEMM_FUSED, or MOE_GEMM_AUTO with
- * H <= 128, or H <= 256 and dedup == 0), 0 when it runs the two GEMMs (or the
- * shape is invalid).  A function of the shape alone. */
+ * H <= 128, or H <= 256 and dedup == 0, and N*k >= 4096 or I <= 256), 0 when
+ * it runs the two GEMMs (or the shape is invalid).  A function of the shape
+ * alone. */
 int32_t moe_layer_fuses_ffn(const moe_shape* shape);
 
 /* Co-selection counts of "Expert Coupling" Sec. V-A / Appendix A-D Algorithm 1:

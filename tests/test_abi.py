@@ -178,9 +178,13 @@ def test_fused_ffn_limits(lib):
         assert moe.moe_layer_fuses_ffn(s) == want, (gemm, H)
         assert moe.moe_layer_skips_dispatch(s) == (want or gemm == "single")
     assert not moe.moe_layer_fuses_ffn(moe.Shape(64, 264, 8, 2, 2, 64, gemm="fused"))
+    # few rows and a long I: the two GEMMs (which spread over I); a short I fuses
+    assert not moe.moe_layer_fuses_ffn(moe.Shape(200, 128, 16, 4, 4, 512))
+    assert moe.moe_layer_fuses_ffn(moe.Shape(64, 128, 8, 2, 2, 256))
+    assert moe.moe_layer_fuses_ffn(moe.Shape(1024, 128, 16, 4, 4, 512))
     # dedup layers fuse by default only up to H = 128
-    assert moe.moe_layer_fuses_ffn(moe.Shape(300, 128, 8, 2, 4, 384, dedup=True))
-    assert not moe.moe_layer_fuses_ffn(moe.Shape(300, 136, 8, 2, 4, 384, dedup=True))
+    assert moe.moe_layer_fuses_ffn(moe.Shape(4096, 128, 8, 2, 4, 384, dedup=True))
+    assert not moe.moe_layer_fuses_ffn(moe.Shape(4096, 136, 8, 2, 4, 384, dedup=True))
     assert moe.moe_layer_fuses_ffn(moe.Shape(300, 256, 8, 2, 4, 384, dedup=True, gemm="fused"))
     wide = moe.Shape(300, 264, 8, 2, 4, 384, gemm="fused")
     assert moe.moe_workspace_bytes(wide) == 0

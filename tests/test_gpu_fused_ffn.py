@@ -46,10 +46,11 @@ def test_fused_layer_against_oracle_and_two_kernels(name, dedup, pack):
     assert fused.kernel_launches_per_step() == moe.MoELayer(
         moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=dedup, gemm="single"), *w, pl,
         pack=False).kernel_launches_per_step() - 1
-    # the automatic choice runs the same kernel for H <= 256 without dedup and
-    # for H <= 128 with it (the two GEMMs otherwise): the same bits either way
+    # the automatic choice (the fused kernel or the two GEMMs, by the shape):
+    # the same bits either way
     auto, out_a = run_layer(wl, w, "auto", dedup, pack, pl)
-    assert auto.fused_ffn == (wl.H <= 128 or not dedup)
+    assert auto.fused_ffn == moe.moe_layer_fuses_ffn(
+        moe.Shape(wl.N, wl.H, wl.E, wl.k, wl.W, wl.I, dedup=dedup))
     assert torch.equal(out.view(torch.int16), out_a.view(torch.int16))
     ref = oracle.layer_forward(synth.make_logits(wl), synth.make_x(wl), *wh, wl.k, wl.W,
                                placement=placement, residual=synth.make_residual(wl), dedup=dedup)

@@ -26,7 +26,9 @@ def layer(shape, fuse_combine=False, shared=None):
     # H > 256, few rows per expert: single-CTA GEMMs, dispatch fused into gate/up
     (moe.Shape(4096, 7168, 256, 8, 8, 2048), ["route", "layout", "gate_up", "down", "combine"]),
     # H <= 256 without dedup: fused by default; with dedup only up to H = 128
-    (moe.Shape(300, 256, 8, 2, 4, 384), ["route", "layout", "ffn", "combine"]),
+    (moe.Shape(4096, 256, 8, 2, 4, 384), ["route", "layout", "ffn", "combine"]),
+    # few rows (N*k < 4096) and I > 256: the two GEMMs
+    (moe.Shape(300, 256, 8, 2, 4, 384), ["route", "layout", "gate_up", "down", "combine"]),
     (moe.Shape(300, 256, 8, 2, 4, 384, dedup=True),
      ["route", "layout", "dispatch", "gate_up", "down", "combine"]),
     # many rows per expert: the CTA-pair GEMMs, which have no gather mode
@@ -47,13 +49,14 @@ def test_stages_follow_the_library(shape, stages):
 
 
 def test_launch_counts():
-    """route 1 + layout 2 (or 3) + dispatch (unless gathered) + FFN (1 fused,
-    2 as two GEMMs) + combine 1."""
+    """route 1 + layout (1 for one block of 256 tokens, else 2, or 3 with a
+    separate scan) + dispatch (unless gathered) + FFN (1 fused, 2 as two
+    GEMMs) + combine 1."""
     fused = layer(moe.Shape(64, 128, 8, 2, 2, 256))
     two = layer(moe.Shape(64, 128, 8, 2, 2, 256, gemm="single"))
-    assert fused.kernel_launches_per_step() == 1 + 2 + 0 + 1 + 1
-    assert two.kernel_launches_per_step() == 1 + 2 + 0 + 2 + 1
-    dedup = layer(moe.Shape(64, 128, 8, 2, 2, 256, dedup=True))
+    assert fused.kernel_launches_per_step() == 1 + 1 + 0 + 1 + 1
+    assert two.kernel_launches_per_step() == 1 + 1 + 0 + 2 + 1
+    dedup = layer(moe.Shape(257, 128, 8, 2, 2, 256, dedup=True))  # two layout blocks
     assert dedup.kernel_launches_per_step() == 1 + 2 + 1 + 1 + 1
     big = layer(moe.Shape(70000, 128, 64, 6, 32, 256))  # count tables over 64 KB: a scan launch
     assert moe.layout_launches(big.shape) == 3
@@ -76,4 +79,4 @@ def test_shared_expert_stage():
     sh = (torch.zeros(64, 128, **bf), torch.zeros(64, 128, **bf), torch.zeros(128, 64, **bf))
     lay = layer(moe.Shape(64, 128, 8, 2, 2, 256), shared=sh)
     assert lay.stage_names() == ["route", "layout", "ffn", "shared", "combine"]
-    assert lay.kernel_launches_per_step() == 1 + 2 + 1 + 1 + 3
+    assert lay.kernel_launches_per_step() == 1 + 1 + 1 + 1 + 3
